@@ -1,0 +1,431 @@
+"""Benchmark of the LCT codec hot path on GB300 (one JSON line on stdout).
+
+A step is one pass of the whole hot path over one synthetic batch:
+  1. lct_encode         shift estimate + block encode (byte split, stream
+                        packing, overflow placement)
+  2. lct_decode         streams -> BF16
+  3. lct_sgd_step_fused W <- W - eta*M on the compressed W (the tensor just
+                        encoded) and a compressed momentum M
+value = uncompressed BF16 bytes passed through the codec per second: encode
+2N + decode 2N + fused SGD 6N (decodes W and M, encodes W) per step.
+
+Default workload: 2^24 BF16 values ~ Laplace(0, 0.01), Laplace codebook,
+CLEAN blocks; M ~ Laplace(0, 1e-3).  L2 is flushed (256 MiB write) before
+every timed step, outside the step's events.
+
+--impl reference times the CPU oracle (single thread) on the same workload.
+Under torchrun every rank runs its own replica (weak scaling, no collective
+on the data path); timing is the max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+WORKLOAD_TEXT = {
+    "laplace_16m": "2^24 BF16 ~ Laplace(0,0.01), Laplace codebook, CLEAN; step = encode + decode + fused SGD "
+                   "(M ~ Laplace(0,1e-3))",
+    "heavy_64m": "2^26 BF16 Student-t(3)*1e-3 with 0.1% x1e4 outliers and 1% subnormals, power-law codebook, "
+                 "MEDIUM; step = encode + decode + fused SGD (M ~ Laplace(0,1e-3))",
+    "gelu_act": "[8,4096,3072] GELU(N(0,1)) with 30% zeros, Gaussian(1) codebook, HIGH; step = encode + decode + "
+                "fused SGD (M ~ Laplace(0,1e-3))",
+    "sgd_162m": "162,000,000 BF16 W ~ N(0,0.02), M ~ N(0,1e-3), Gaussian codebooks, CLEAN; step = encode + decode "
+                "+ fused SGD",
+}
+SGD_MOMENTUM = {"laplace_16m": ("laplace", 1e-3), "heavy_64m": ("laplace", 1e-3), "gelu_act": ("laplace", 1e-3),
+                "sgd_162m": ("gaussian", 1e-3)}
+ETA = float(np.float32(1e-3))
+L2_FLUSH_BYTES = 256 << 20
+
+
+def load_baseline():
+    with open(os.path.join(ROOT, "BASELINE.json")) as f:
+        return json.load(f)
+
+
+def hbm_peak():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    return int(os.environ.get("RANK", "0")), int(os.environ.get("LOCAL_RANK", "0")), ws
+
+
+# ----------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while running."""
+    FIELDS = ["clocks.sm", "clocks.max.sm", "power.draw", "clocks_event_reasons.active",
+              "clocks_event_reasons.hw_slowdown", "clocks_event_reasons.hw_thermal_slowdown",
+              "clocks_event_reasons.sw_thermal_slowdown", "clocks_event_reasons.sw_power_cap"]
+
+    def __init__(self, bus_id: str | None):
+        self.bus_id = bus_id
+        self.proc = None
+        self.lines: list[str] = []
+
+    def start(self):
+        cmd = ["nvidia-smi", "--query-gpu=" + ",".join(self.FIELDS), "--format=csv,noheader,nounits", "-lms", "200"]
+        if self.bus_id:
+            cmd += ["-i", self.bus_id]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.thread.join(timeout=2)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) != len(self.FIELDS):
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax.append(float(parts[1]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[4:]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ------------------------------------------------------------ GPU arm
+
+def algorithmic_bytes(sizes, ovf_used: int) -> int:
+    """Bytes a codec pass must move for one tensor: compressed form
+    (sign-fraction + slots + markers + offsets + overflow) plus 2 bytes per
+    value on the uncompressed side."""
+    return int(sizes.sf_bytes + sizes.slot_bytes + sizes.marker_bytes + sizes.blk_off_bytes + ovf_used)
+
+
+def run_gpu(args):
+    import torch
+    import torch.distributed as dist
+
+    rank, local_rank, world = dist_env()
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local_rank)
+    from lossless_bf16_tensor_gb300 import binding as B
+    from lossless_bf16_tensor_gb300 import synth
+
+    wl = synth.WORKLOADS[args.workload]
+    n = wl["n"]
+    level = B.LEVELS[wl["level"]]
+    x_np = synth.generate(args.workload)
+    mm, ms = SGD_MOMENTUM[args.workload]
+    m_np = synth.laplace(n, ms, seed=2) if mm == "laplace" else synth.momentum(args.workload)
+    cb = B.lct_codebook_build(wl["model"], wl["scale"], wl["shape"])
+    cbm = B.lct_codebook_build(mm, ms)
+
+    stream = torch.cuda.current_stream()
+    x = torch.from_numpy(x_np.view(np.int16)).cuda()
+    md = torch.from_numpy(m_np.view(np.int16)).cuda()
+    X = B.CompressedTensor(n, level)
+    Mc = B.CompressedTensor(n, level)
+    Wn = B.CompressedTensor(n, level)
+    y = torch.empty_like(x)
+    B.lct_encode(md, cbm, Mc)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.int32, device="cuda")
+
+    def step(evs=None):
+        if evs:
+            evs[0].record(stream)
+        B.lct_encode(x, cb, X, stream)
+        if evs:
+            evs[1].record(stream)
+        B.lct_decode(X, cb, y, stream)
+        if evs:
+            evs[2].record(stream)
+        B.lct_sgd_step_fused(X, cb, Mc, cbm, ETA, Wn, stream)
+        if evs:
+            evs[3].record(stream)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    # correctness of what is timed: the round trip is exact and nothing latched
+    assert torch.equal(y, x), "decode(encode(x)) != x"
+    for t in (X, Mc, Wn):
+        assert t.state().status == 0
+
+    bus = None
+    try:
+        bus = torch.cuda.get_device_properties(local_rank).pci_bus_id
+    except AttributeError:
+        pass
+    clocks = ClockSampler(None if world == 1 and bus is None else bus)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.4)
+    for k in range(args.steps):
+        flush.zero_()
+        step(evs[k])
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    clk = clocks.stop()
+    enc = [e[0].elapsed_time(e[1]) for e in evs]
+    dec = [e[1].elapsed_time(e[2]) for e in evs]
+    sgd = [e[2].elapsed_time(e[3]) for e in evs]
+    total_ms = sum(a + b + c for a, b, c in zip(enc, dec, sgd))
+    if world > 1:
+        t = torch.tensor([total_ms], dtype=torch.float64, device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_step = total_ms / args.steps
+
+    sx, sm_, sw = X.state(), Mc.state(), Wn.state()
+    sizes = X.sizes
+    bytes_x = algorithmic_bytes(sizes, sx.ovf_used)
+    bytes_m = algorithmic_bytes(sizes, sm_.ovf_used)
+    bytes_w = algorithmic_bytes(sizes, sw.ovf_used)
+    alg = {"encode": 2 * n + bytes_x, "decode": 2 * n + bytes_x, "sgd": bytes_x + bytes_m + bytes_w}
+    t_ms = {"encode": statistics.mean(enc), "decode": statistics.mean(dec), "sgd": statistics.mean(sgd)}
+    peak, peak_kind = hbm_peak()
+    frac = {k: alg[k] / (t_ms[k] * 1e-3) / 1e9 / peak for k in alg}
+    dom = max(t_ms, key=t_ms.get)
+    achieved = alg[dom] / (t_ms[dom] * 1e-3) / 1e9
+    uncompressed_per_step = 10 * n
+    value = uncompressed_per_step * world / (ms_step * 1e-3) / 1e9
+
+    traffic = None
+    tpath = os.path.join(ROOT, "profiles", "traffic.json")
+    if os.path.exists(tpath):
+        with open(tpath) as f:
+            tr = json.load(f)
+        entry = tr.get(args.workload, {}).get(dom)
+        if entry and entry.get("source_hash") == kernel_source_hash():
+            traffic = entry["bytes_per_launch"]
+
+    # ---- end to end through the public API with host buffers
+    e2e = None
+    if not args.no_e2e:
+        hx = torch.from_numpy(x_np.view(np.int16)).pin_memory()
+        hy = torch.empty(n, dtype=torch.int16).pin_memory()
+        hh = torch.empty(64, dtype=torch.uint8).pin_memory()
+        xs = torch.empty_like(x)
+
+        def e2e_step():
+            xs.copy_(hx, non_blocking=True)
+            B.lct_encode(xs, cb, X, stream)
+            B.lct_decode(X, cb, y, stream)
+            hy.copy_(y, non_blocking=True)
+            B.lct_sgd_step_fused(X, cb, Mc, cbm, ETA, Wn, stream)
+            hh.copy_(Wn.regions["header"], non_blocking=True)
+
+        for _ in range(2):
+            e2e_step()
+        torch.cuda.synchronize()
+        ee = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+        for k in range(args.steps):
+            flush.zero_()
+            ee[k][0].record(stream)
+            e2e_step()
+            ee[k][1].record(stream)
+        torch.cuda.synchronize()
+        assert torch.equal(hy, hx)
+        e_ms = sum(a.elapsed_time(b) for a, b in ee) / args.steps
+        if world > 1:
+            t = torch.tensor([e_ms], dtype=torch.float64, device="cuda")
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e_ms = float(t.item())
+        e2e = {"value": round(uncompressed_per_step * world / (e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+               "ms_per_step": round(e_ms, 4), "h2d_bytes_per_step": 2 * n, "d2h_bytes_per_step": 2 * n + 64}
+
+    if rank != 0:
+        return None
+    base = load_baseline()
+    ratio_all_in = 2.0 * n / (sizes.fixed_bytes + sx.ovf_used)
+    ratio_payload = 2.0 * n / (sizes.sf_bytes + sizes.slot_bytes + sx.ovf_used)
+    cpu = None if args.no_cpu_baseline or world > 1 else cpu_baseline(args.workload, args.cpu_blocks)
+    line = {
+        "metric": base["metric"],
+        "value": round(value, 2),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_step, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "u32+f32",
+        "data": "synthetic",
+        "config": {"workload": WORKLOAD_TEXT[args.workload], "name": args.workload, "n": n,
+                   "level": wl["level"], "l2": "flushed before every step (256 MiB write, outside the events)",
+                   "parallelism": "replicas" if world > 1 else "single"},
+        "roofline": {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 1), "peak": peak,
+                     "peak_kind": peak_kind, "unit": "GB/s", "frac": round(achieved / peak, 4),
+                     "traffic": traffic, "algorithmic_bytes_per_launch": alg[dom]},
+        "breakdown": {
+            "encode_gbs_uncompressed": round(2 * n / (t_ms["encode"] * 1e-3) / 1e9, 1),
+            "decode_gbs_uncompressed": round(2 * n / (t_ms["decode"] * 1e-3) / 1e9, 1),
+            "sgd_gelem_per_s": round(n / (t_ms["sgd"] * 1e-3) / 1e9, 3),
+            "ms": {k: round(v, 4) for k, v in t_ms.items()},
+            "hbm_frac_of_%s" % peak_kind: {k: round(v, 4) for k, v in frac.items()},
+            "compression_ratio_all_in": round(ratio_all_in, 5),
+            "compression_ratio_payload": round(ratio_payload, 5),
+            "overflow_bytes": int(sx.ovf_used),
+        },
+        "clocks": clk,
+        "e2e": e2e,
+        "gpu_launches": 5 * args.steps,
+        "cpu_baseline": cpu,
+    }
+    return line
+
+
+def kernel_source_hash() -> str:
+    import hashlib
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "lossless_bf16_tensor_gb300", "csrc")
+    for fn in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, fn), "rb") as f:
+            h.update(fn.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+# ------------------------------------------------------ oracle (CPU) arm
+
+def oracle_step_time(workload: str, nblocks_sample: int | None):
+    """Time the oracle on the workload (or its first `nblocks_sample` blocks):
+    encode, decode, fused SGD, as one step.  Returns (seconds, values)."""
+    import oracle
+    from lossless_bf16_tensor_gb300 import synth
+    wl = synth.WORKLOADS[workload]
+    x = synth.generate(workload)
+    mm, ms = SGD_MOMENTUM[workload]
+    m = synth.laplace(x.size, ms, seed=2) if mm == "laplace" else synth.momentum(workload)
+    level = {"CLEAN": 0, "MEDIUM": 1, "HIGH": 2}[wl["level"]]
+    block, _ = oracle.geometry(level)
+    if nblocks_sample:
+        k = min(x.size, nblocks_sample * block)
+        x, m = x[:k], m[:k]
+    model = {"gaussian": 0, "laplace": 1, "powerlaw": 2}
+    cb = oracle.codebook_build(model[wl["model"]], wl["scale"], wl["shape"])
+    cbm = oracle.codebook_build(model[mm], ms)
+    M = oracle.encode(m, cbm, level)
+    t0 = time.perf_counter()
+    X = oracle.encode(x, cb, level)
+    rc, y = oracle.decode(X, cb)
+    oracle.sgd_step(X, cb, M, cbm, ETA)
+    dt = time.perf_counter() - t0
+    assert rc == 0 and np.array_equal(y, x)
+    return dt, x.size
+
+
+def cpu_model() -> str:
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith(("model name", "cpu part")):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return "unknown"
+
+
+def cpu_baseline(workload: str, nblocks_sample: int | None):
+    dt, nvals = oracle_step_time(workload, nblocks_sample)
+    return {"value": round(10 * nvals / dt / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": "%d values of the %s workload (%s), one step: encode + decode + fused SGD; "
+                      "host %s, %d logical CPUs, oracle single-threaded" % (
+                          nvals, workload, "first %d blocks" % nblocks_sample if nblocks_sample else "all",
+                          cpu_model(), os.cpu_count() or 0),
+            "seconds": round(dt, 3)}
+
+
+def run_reference(args):
+    rank, _, world = dist_env()
+    if rank != 0:
+        return None
+    base = load_baseline()
+    times, nvals = [], 0
+    for _ in range(args.warmup):
+        oracle_step_time(args.workload, args.cpu_blocks)
+    for _ in range(args.steps):
+        dt, nvals = oracle_step_time(args.workload, args.cpu_blocks)
+        times.append(dt)
+    s = sum(times) / len(times)
+    value = 10 * nvals / s / 1e9
+    sample = "%d values of %s per step (%s)" % (nvals, args.workload,
+                                               "first %d blocks" % args.cpu_blocks if args.cpu_blocks else "all")
+    return {"impl": "reference", "metric": base["metric"], "value": round(value, 4), "unit": "GB/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(s * 1e3, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "u32+f32",
+            "data": "synthetic",
+            "config": {"workload": WORKLOAD_TEXT[args.workload], "name": args.workload},
+            "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["lct", "reference"], default="lct")
+    ap.add_argument("--workload", default="laplace_16m", choices=sorted(WORKLOAD_TEXT))
+    ap.add_argument("--cpu-blocks", type=int, default=0, help="oracle sample: first N blocks (0 = whole workload)")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    args = ap.parse_args()
+    if args.impl == "reference":
+        # each oracle step is a bounded sample of the workload (32 blocks
+        # unless given) so that --steps K --warmup W ends within minutes
+        if not args.cpu_blocks:
+            args.cpu_blocks = 32
+        line = run_reference(args)
+    else:
+        if args.gpus > 1 and int(os.environ.get("WORLD_SIZE", "1")) == 1:
+            raise SystemExit("--gpus > 1 runs under torchrun (one process per GPU)")
+        line = run_gpu(args)
+    if line is not None:
+        print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,268 @@
+// Host entry points of liblct (the C ABI declared in include/lct.h):
+// argument checks, sizing, and kernel launches.  No device memory is ever
+// allocated here; every buffer belongs to the caller.
+#include <cstdint>
+#include <cstring>
+
+#include "../../include/lct.h"
+#include "../../include/lct_debug.h"
+#include "codec_dev.cuh"
+#include "internal.h"
+
+namespace lct {
+namespace {
+
+uint64_t nblocks_for(uint64_t n, const Geometry &g) { return (n + g.block - 1) / g.block; }
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+struct Range {
+    uintptr_t lo, hi;  // [lo, hi)
+};
+Range range_of(const void *p, uint64_t bytes)
+{
+    const uintptr_t a = reinterpret_cast<uintptr_t>(p);
+    return {a, a + bytes};
+}
+bool overlap(Range a, Range b) { return a.lo < b.hi && b.lo < a.hi && a.lo != a.hi && b.lo != b.hi; }
+
+void fill_sizes(uint64_t n, const Geometry &g, lct_sizes *s)
+{
+    std::memset(s, 0, sizeof(*s));
+    const uint64_t nb = nblocks_for(n, g);
+    s->n = n;
+    s->nblocks = nb;
+    s->block = g.block;
+    s->slot_words = g.slot_words;
+    s->header_bytes = LCT_HEADER_BYTES;
+    s->sf_bytes = n;
+    s->slot_bytes = nb * g.slot_words * kStreams * 4ull;
+    s->marker_bytes = nb * kStreams * 2ull;
+    s->blk_off_bytes = (nb + 1) * 8ull;
+    s->fixed_bytes = s->header_bytes + s->sf_bytes + s->slot_bytes + s->marker_bytes + s->blk_off_bytes;
+    s->worst_ovf_bytes = n;
+    s->work_bytes = nb * 8ull;
+}
+
+// Host-side checks of one tensor descriptor; fills its sizes.
+lct_status check_tensor(const lct_tensor *t, bool writer, lct_sizes *s)
+{
+    Geometry g;
+    if (!t || t->n > kMaxN || !level_geometry(t->level, &g)) return LCT_ERR_INVALID_ARG;
+    fill_sizes(t->n, g, s);
+    if (!t->d_header || !aligned16(t->d_header)) return LCT_ERR_INVALID_ARG;
+    if (t->n > 0) {
+        if (!t->d_sf || !t->d_slots || !t->d_markers || !t->d_blk_off) return LCT_ERR_INVALID_ARG;
+        if (!aligned16(t->d_sf) || !aligned16(t->d_slots) || !aligned16(t->d_markers) ||
+            !aligned16(t->d_blk_off))
+            return LCT_ERR_INVALID_ARG;
+        if (writer && (!t->d_work || !aligned16(t->d_work))) return LCT_ERR_INVALID_ARG;
+    }
+    if (t->ovf_cap > 0 && !t->d_ovf) return LCT_ERR_INVALID_ARG;
+    if (t->d_ovf && !aligned16(t->d_ovf)) return LCT_ERR_INVALID_ARG;
+    if (writer && t->n > 0) {
+        // the regions a writer fills must not overlap one another
+        const void *p[7] = {t->d_header, t->d_sf, t->d_slots, t->d_markers, t->d_blk_off, t->d_ovf, t->d_work};
+        const uint64_t len[7] = {s->header_bytes, s->sf_bytes, s->slot_bytes, s->marker_bytes,
+                                 s->blk_off_bytes, t->ovf_cap, s->work_bytes};
+        for (int i = 0; i < 7; ++i)
+            for (int k = i + 1; k < 7; ++k)
+                if (p[i] && p[k] && overlap(range_of(p[i], len[i]), range_of(p[k], len[k])))
+                    return LCT_ERR_INVALID_ARG;
+    }
+    return LCT_OK;
+}
+
+DevTensor dev_view(const lct_tensor *t, const lct_sizes &s)
+{
+    DevTensor d;
+    d.hdr = static_cast<lct_header *>(t->d_header);
+    d.sf = t->d_sf;
+    d.slots = t->d_slots;
+    d.markers = t->d_markers;
+    d.blk_off = t->d_blk_off;
+    d.ovf = t->d_ovf;
+    d.work = static_cast<unsigned long long *>(t->d_work);
+    d.ovf_cap = t->ovf_cap;
+    d.n = t->n;
+    d.nblocks = static_cast<uint32_t>(s.nblocks);
+    d.level = t->level;
+    return d;
+}
+
+DevCodebook dev_codebook(const lct_codebook &cb)
+{
+    DevCodebook d;
+    std::memcpy(d.len, cb.len, 256);
+    std::memcpy(d.code, cb.code, 256);
+    std::memcpy(d.dec, cb.dec, sizeof(d.dec));
+    d.esc_len = cb.esc_len;
+    d.esc_code = cb.esc_code;
+    d.pad = 0;
+    d.hash = cb.hash;
+    return d;
+}
+
+// Every region of a tensor, for overlap checks.
+void regions(const lct_tensor *t, const lct_sizes &s, Range out[7])
+{
+    out[0] = range_of(t->d_header, s.header_bytes);
+    out[1] = range_of(t->d_sf, s.sf_bytes);
+    out[2] = range_of(t->d_slots, s.slot_bytes);
+    out[3] = range_of(t->d_markers, s.marker_bytes);
+    out[4] = range_of(t->d_blk_off, s.blk_off_bytes);
+    out[5] = range_of(t->d_ovf, t->ovf_cap);
+    out[6] = range_of(t->d_work, s.work_bytes);
+}
+
+}  // namespace
+}  // namespace lct
+
+using namespace lct;
+
+extern "C" lct_status lct_compressed_size(uint64_t n, int level, const lct_tensor *t, void *stream,
+                                          lct_sizes *out)
+{
+    Geometry g;
+    if (!out || n > kMaxN || !level_geometry(level, &g)) return LCT_ERR_INVALID_ARG;
+    if (t && (t->n != n || t->level != level)) return LCT_ERR_INVALID_ARG;
+    lct_sizes s;
+    fill_sizes(n, g, &s);
+    if (t) {
+        if (!t->d_header || !aligned16(t->d_header)) return LCT_ERR_INVALID_ARG;
+        lct_header h;
+        cudaStream_t st = static_cast<cudaStream_t>(stream);
+        if (cudaMemcpyAsync(&h, t->d_header, sizeof(h), cudaMemcpyDeviceToHost, st) != cudaSuccess)
+            return LCT_ERR_CUDA;
+        if (cudaStreamSynchronize(st) != cudaSuccess) return LCT_ERR_CUDA;
+        s.ovf_used = h.ovf_used;
+        s.status = h.status;
+        s.delta = h.delta;
+        if (h.magic != LCT_MAGIC && s.status == 0) s.status = LCT_ERR_CORRUPT;
+    }
+    *out = s;
+    return LCT_OK;
+}
+
+extern "C" lct_status lct_encode(const uint16_t *d_x, const lct_codebook *cb, const lct_tensor *t,
+                                 void *stream)
+{
+    lct_sizes s;
+    lct_status rc = check_tensor(t, true, &s);
+    if (rc != LCT_OK) return rc;
+    if (!cb || !codebook_valid(*cb)) return LCT_ERR_INVALID_ARG;
+    if (t->n > 0 && (!d_x || !aligned16(d_x))) return LCT_ERR_INVALID_ARG;
+    Range r[7];
+    regions(t, s, r);
+    for (int i = 0; i < 7; ++i)
+        if (t->n > 0 && overlap(r[i], range_of(d_x, 2 * t->n))) return LCT_ERR_INVALID_ARG;
+    EncodeArgs a;
+    a.x = d_x;
+    a.t = dev_view(t, s);
+    a.cb = dev_codebook(*cb);
+    a.median_exp = cb->median_exp;
+    a.pad = 0;
+    a.wait_ns = kDefaultWaitNs;
+    return launch_encode(a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? LCT_OK : LCT_ERR_CUDA;
+}
+
+extern "C" lct_status lct_decode(const lct_tensor *t, const lct_codebook *cb, uint16_t *d_y, void *stream)
+{
+    lct_sizes s;
+    lct_status rc = check_tensor(t, false, &s);
+    if (rc != LCT_OK) return rc;
+    if (!cb || !codebook_valid(*cb)) return LCT_ERR_INVALID_ARG;
+    if (t->n > 0 && (!d_y || !aligned16(d_y))) return LCT_ERR_INVALID_ARG;
+    Range r[7];
+    regions(t, s, r);
+    for (int i = 0; i < 6; ++i)
+        if (t->n > 0 && overlap(r[i], range_of(d_y, 2 * t->n))) return LCT_ERR_INVALID_ARG;
+    DecodeArgs a;
+    a.t = dev_view(t, s);
+    a.y = d_y;
+    a.cb = dev_codebook(*cb);
+    return launch_decode(a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? LCT_OK : LCT_ERR_CUDA;
+}
+
+extern "C" lct_status lct_sgd_step_fused(const lct_tensor *W_in, const lct_codebook *cbW, const lct_tensor *M,
+                                         const lct_codebook *cbM, float eta, const lct_tensor *W_out,
+                                         void *stream)
+{
+    lct_sizes sw, sm, so;
+    lct_status rc;
+    if ((rc = check_tensor(W_in, false, &sw)) != LCT_OK) return rc;
+    if ((rc = check_tensor(M, false, &sm)) != LCT_OK) return rc;
+    if ((rc = check_tensor(W_out, true, &so)) != LCT_OK) return rc;
+    if (!cbW || !cbM || !codebook_valid(*cbW) || !codebook_valid(*cbM)) return LCT_ERR_INVALID_ARG;
+    if (W_in->n != M->n || W_in->n != W_out->n) return LCT_ERR_INVALID_ARG;
+    if (W_in->level != M->level || W_in->level != W_out->level) return LCT_ERR_UNSUPPORTED;
+    Range rw[7], rm[7], ro[7];
+    regions(W_in, sw, rw);
+    regions(M, sm, rm);
+    regions(W_out, so, ro);
+    if (W_out->n > 0) {
+        // W_out must not touch M at all.
+        for (int i = 0; i < 7; ++i)
+            for (int k = 0; k < 6; ++k)
+                if (overlap(ro[i], rm[k])) return LCT_ERR_INVALID_ARG;
+        // W_out's overflow and scratch must be apart from every input region;
+        // its other regions may coincide exactly with W_in's (in place) but
+        // not partly overlap them.
+        for (int k = 0; k < 6; ++k) {
+            if (overlap(ro[5], rw[k]) || overlap(ro[6], rw[k])) return LCT_ERR_INVALID_ARG;
+        }
+        for (int i = 0; i < 5; ++i)
+            for (int k = 0; k < 6; ++k) {
+                const bool same = i == k && ro[i].lo == rw[k].lo;
+                if (!same && overlap(ro[i], rw[k])) return LCT_ERR_INVALID_ARG;
+            }
+    }
+    SgdArgs a;
+    a.w_in = dev_view(W_in, sw);
+    a.m = dev_view(M, sm);
+    a.w_out = dev_view(W_out, so);
+    a.cbw = dev_codebook(*cbW);
+    a.cbm = dev_codebook(*cbM);
+    a.eta = eta;
+    a.pad = 0;
+    a.wait_ns = kDefaultWaitNs;
+    return launch_sgd(a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? LCT_OK : LCT_ERR_CUDA;
+}
+
+// ------------------------------------------------------------ test hook
+
+namespace lct {
+namespace dev {
+
+// Runs the look-back of block 1 over a status array whose block 0 never
+// publishes; the bounded wait must run out and latch LCT_ERR_TIMEOUT.
+__global__ void k_wait_probe(lct_header *hdr, unsigned long long *work, uint64_t wait_ns)
+{
+    if (threadIdx.x != 0) return;
+    work[0] = 0ull;
+    work[1] = 0ull;
+    __threadfence();
+    bool timed_out;
+    lookback(work, 1, 0, wait_ns, &timed_out);
+    if (timed_out) latch(hdr, LCT_ERR_TIMEOUT);
+}
+
+}  // namespace dev
+
+cudaError_t launch_wait_probe(lct_header *hdr, unsigned long long *work, uint64_t wait_ns, cudaStream_t s)
+{
+    dev::k_wait_probe<<<1, 32, 0, s>>>(hdr, work, wait_ns);
+    return cudaGetLastError();
+}
+
+}  // namespace lct
+
+extern "C" lct_status lct_debug_wait_timeout(void *d_header, void *d_work, uint64_t limit_ns, void *stream)
+{
+    if (!d_header || !d_work || !aligned16(d_header) || !aligned16(d_work)) return LCT_ERR_INVALID_ARG;
+    if (limit_ns == 0 || limit_ns > kDefaultWaitNs) return LCT_ERR_INVALID_ARG;
+    return launch_wait_probe(static_cast<lct_header *>(d_header), static_cast<unsigned long long *>(d_work),
+                             limit_ns, static_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? LCT_OK
+               : LCT_ERR_CUDA;
+}

@@ -1,0 +1,93 @@
+// Library-private declarations shared by the host entry points and the CUDA
+// kernels of liblct.
+#pragma once
+
+#include <cstdint>
+
+#include <cuda_runtime.h>
+
+#include "../../include/lct.h"
+
+namespace lct {
+
+constexpr int kStreams = LCT_STREAMS;
+constexpr uint64_t kMaxN = 1ull << 40;
+constexpr uint64_t kDefaultWaitNs = 1000000000ull;  // 1 s bound on any device wait
+
+struct Geometry {
+    uint32_t block;       // exponents per block
+    uint32_t slot_words;  // 32-bit words per stream slot
+};
+
+// [EXP] "Compressing is easy": 65,536-value blocks in CLEAN, 32,768 in MEDIUM
+// and HIGH.  Slot sizes: 800 bits in CLEAN (the 1.4382x bound of [EXP] "Here
+// is the idealized arithmetic"); 512 and 640 bits in MEDIUM and HIGH.
+inline bool level_geometry(int level, Geometry *g)
+{
+    switch (level) {
+    case LCT_LEVEL_CLEAN: *g = {65536u, 25u}; return true;
+    case LCT_LEVEL_MEDIUM: *g = {32768u, 16u}; return true;
+    case LCT_LEVEL_HIGH: *g = {32768u, 20u}; return true;
+    default: return false;
+    }
+}
+
+uint32_t codebook_hash(const lct_codebook &cb);
+bool codebook_valid(const lct_codebook &cb);
+
+// The codebook as kernels receive it (by value, in kernel parameters).
+struct DevCodebook {
+    uint8_t len[256];
+    uint8_t code[256];
+    uint16_t dec[256];
+    uint8_t esc_len;
+    uint8_t esc_code;
+    uint16_t pad;
+    uint32_t hash;
+};
+
+// Device view of one compressed tensor.
+struct DevTensor {
+    lct_header *hdr;
+    uint8_t *sf;
+    uint32_t *slots;
+    uint16_t *markers;
+    uint64_t *blk_off;
+    uint8_t *ovf;
+    unsigned long long *work;  // per-block scan status words
+    uint64_t ovf_cap;
+    uint64_t n;
+    uint32_t nblocks;
+    int32_t level;
+};
+
+struct EncodeArgs {
+    const uint16_t *x;
+    DevTensor t;
+    DevCodebook cb;
+    int32_t median_exp;
+    uint32_t pad;
+    uint64_t wait_ns;
+};
+
+struct DecodeArgs {
+    DevTensor t;
+    uint16_t *y;
+    DevCodebook cb;
+};
+
+struct SgdArgs {
+    DevTensor w_in, m, w_out;
+    DevCodebook cbw, cbm;
+    float eta;
+    uint32_t pad;
+    uint64_t wait_ns;
+};
+
+cudaError_t launch_encode(const EncodeArgs &a, cudaStream_t s);
+cudaError_t launch_decode(const DecodeArgs &a, cudaStream_t s);
+cudaError_t launch_sgd(const SgdArgs &a, cudaStream_t s);
+cudaError_t launch_wait_probe(lct_header *hdr, unsigned long long *work, uint64_t wait_ns,
+                              cudaStream_t s);
+
+}  // namespace lct

@@ -1,0 +1,155 @@
+"""C-ABI checks that need no GPU: the library loads and exports every entry
+point its headers declare, the host-side codebook builder reproduces the
+oracle's tables, region sizes follow the format, and host-detectable argument
+errors come back as status codes without touching the device."""
+import ctypes
+import glob
+import os
+import re
+
+import numpy as np
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+MODELS = [(0, 0.02, 0.0), (0, 1.0, 0.0), (0, 1e-3, 0.0), (0, 3e-30, 0.0), (0, 1e20, 0.0),
+          (1, 0.01, 0.0), (1, 3e-5, 0.0), (1, 7.0, 0.0), (2, 1e-3, 3.0), (2, 0.5, 1.5), (2, 1e-6, 0.7),
+          (2, 2.0, 12.0)]
+
+
+def declared_functions():
+    names = set()
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        text = open(h).read()
+        names |= set(re.findall(r"^lct_status\s+(lct_\w+)\s*\(", text, flags=re.M))
+    return names
+
+
+def test_library_exports_every_declared_entry_point(lct_lib):
+    names = declared_functions()
+    assert {"lct_codebook_build", "lct_encode", "lct_decode", "lct_sgd_step_fused",
+            "lct_compressed_size"} <= names
+    lib = lct_lib.library()
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+@pytest.mark.parametrize("model,scale,shape", MODELS)
+def test_codebook_matches_oracle(lct_lib, orc, model, scale, shape):
+    cb = lct_lib.lct_codebook_build(model, scale, shape)
+    ref = orc.codebook_build(model, scale, shape)
+    assert bytes(cb.len) == bytes(ref.len)
+    assert list(cb.code) == [int(c) for c in ref.code]
+    assert cb.esc_len == ref.esc_len and cb.esc_code == ref.esc_code
+    assert cb.nsym == ref.k and cb.median_exp == ref.median_exp
+    for v in range(256):
+        assert cb.dec[v] & 0x1FF == ref.lut_sym[v]
+        assert cb.dec[v] >> 12 == ref.lut_len[v]
+
+
+def test_codebook_rejects_bad_parameters(lct_lib):
+    lib = lct_lib.library()
+    cb = lct_lib.lct_codebook()
+    for args in [(0, 0.0, 0.0), (1, -1.0, 0.0), (2, 1.0, 0.0), (0, float("inf"), 0.0), (3, 1.0, 1.0),
+                 (2, 1.0, float("nan")), (0, float("nan"), 0.0)]:
+        assert lib.lct_codebook_build(args[0], args[1], args[2], ctypes.byref(cb)) == lct_lib.LCT_ERR_INVALID_ARG
+    assert lib.lct_codebook_build(0, 1.0, 0.0, None) == lct_lib.LCT_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("n", [0, 1, 255, 65536, 65537, 162_000_000, 1 << 26])
+@pytest.mark.parametrize("level", [0, 1, 2])
+def test_region_sizes(lct_lib, orc, n, level):
+    block, words = orc.geometry(level)
+    nb = -(-n // block)
+    s = lct_lib.lct_compressed_size(n, level)
+    assert (s.block, s.slot_words, s.nblocks) == (block, words, nb)
+    assert s.sf_bytes == n and s.slot_bytes == nb * words * 256 * 4
+    assert s.marker_bytes == nb * 512 and s.blk_off_bytes == 8 * (nb + 1)
+    assert s.fixed_bytes == 64 + s.sf_bytes + s.slot_bytes + s.marker_bytes + s.blk_off_bytes
+    assert s.worst_ovf_bytes == n and s.work_bytes == 8 * nb
+
+
+def test_clean_all_in_ratio(lct_lib):
+    """All-in ratio of a CLEAN tensor with no spill: 2n over the fixed bytes
+    (slots, markers and offsets included), just under the 1.4382x payload bound."""
+    n = 1 << 24
+    s = lct_lib.lct_compressed_size(n, 0)
+    assert abs(2 * n / s.fixed_bytes - 1.4301) < 5e-4
+
+
+def test_sizes_reject_bad_arguments(lct_lib):
+    lib = lct_lib.library()
+    out = lct_lib.lct_sizes()
+    assert lib.lct_compressed_size(10, 3, None, None, ctypes.byref(out)) == lct_lib.LCT_ERR_INVALID_ARG
+    assert lib.lct_compressed_size((1 << 40) + 1, 0, None, None, ctypes.byref(out)) == lct_lib.LCT_ERR_INVALID_ARG
+    assert lib.lct_compressed_size(10, 0, None, None, None) == lct_lib.LCT_ERR_INVALID_ARG
+
+
+def _fake_tensor(lct_lib, n=1000, level=0, base=0x10000000):
+    t = lct_lib.lct_tensor()
+    t.n, t.level = n, level
+    t.d_header, t.d_sf, t.d_slots = base, base + 0x1000, base + 0x100000
+    t.d_markers, t.d_blk_off, t.d_ovf = base + 0x200000, base + 0x300000, base + 0x400000
+    t.ovf_cap, t.d_work = n, base + 0x500000
+    return t
+
+
+def test_host_argument_errors_never_reach_the_device(lct_lib):
+    """Each call below fails a host check, so no CUDA call is made (this
+    machine has no GPU; reaching the device would give LCT_ERR_CUDA)."""
+    lib = lct_lib.library()
+    cb = lct_lib.lct_codebook_build(0, 0.02)
+    bad_cb = lct_lib.lct_codebook_build(0, 0.02)
+    bad_cb.len[120] = 9
+    x = 0x20000000
+    E = lct_lib.LCT_ERR_INVALID_ARG
+
+    def enc(t, c=cb, xp=x):
+        return lib.lct_encode(xp, ctypes.byref(c), ctypes.byref(t), None)
+
+    t = _fake_tensor(lct_lib)
+    assert enc(t, c=bad_cb) == E                        # malformed codebook
+    assert lib.lct_encode(x, None, ctypes.byref(t), None) == E
+    assert enc(t, xp=None) == E                         # NULL input
+    assert enc(t, xp=x + 2) == E                        # misaligned input
+    for field in ("d_header", "d_sf", "d_slots", "d_markers", "d_blk_off", "d_work"):
+        u = _fake_tensor(lct_lib)
+        setattr(u, field, None)
+        assert enc(u) == E, field
+        setattr(u, field, getattr(_fake_tensor(lct_lib), field) + 4)
+        assert enc(u) == E, field
+    u = _fake_tensor(lct_lib)
+    u.level = 7
+    assert enc(u) == E
+    u = _fake_tensor(lct_lib)
+    u.d_ovf = u.d_slots                                # overlapping regions
+    assert enc(u) == E
+    u = _fake_tensor(lct_lib)
+    assert enc(u, xp=u.d_sf) == E                      # input overlaps the output
+    # decode
+    y = 0x30000000
+    assert lib.lct_decode(ctypes.byref(t), ctypes.byref(bad_cb), y, None) == E
+    assert lib.lct_decode(ctypes.byref(t), ctypes.byref(cb), y + 8, None) == E
+    assert lib.lct_decode(ctypes.byref(t), ctypes.byref(cb), t.d_sf, None) == E
+    # sgd
+    w, m, o = _fake_tensor(lct_lib), _fake_tensor(lct_lib, base=0x40000000), _fake_tensor(lct_lib, base=0x50000000)
+
+    def sgd(w, m, o):
+        return lib.lct_sgd_step_fused(ctypes.byref(w), ctypes.byref(cb), ctypes.byref(m), ctypes.byref(cb),
+                                      ctypes.c_float(1e-3), ctypes.byref(o), None)
+
+    m2 = _fake_tensor(lct_lib, n=999, base=0x40000000)
+    assert sgd(w, m2, o) == E                           # n mismatch
+    m3 = _fake_tensor(lct_lib, level=1, base=0x40000000)
+    assert sgd(w, m3, o) == lct_lib.LCT_ERR_UNSUPPORTED  # level mismatch
+    o2 = _fake_tensor(lct_lib, base=0x50000000)
+    o2.d_ovf = w.d_ovf                                  # shares W_in's overflow
+    assert sgd(w, m, o2) == E
+    o3 = _fake_tensor(lct_lib, base=0x10000000)          # fully aliases W_in, overflow included
+    assert sgd(w, m, o3) == E
+    o4 = _fake_tensor(lct_lib, base=0x40000000)          # writes into M
+    assert sgd(w, m, o4) == E
+    # the debug hook checks its arguments too
+    assert lib.lct_debug_wait_timeout(None, 0x10000000, 1000, None) == E
+    assert lib.lct_debug_wait_timeout(0x10000000, 0x10000000 + 4, 1000, None) == E
+    assert lib.lct_debug_wait_timeout(0x10000000, 0x10000010, 0, None) == E

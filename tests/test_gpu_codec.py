@@ -1,0 +1,218 @@
+"""GPU parity of the encode/decode path against the CPU oracle, through the C
+ABI: shift, sign-fraction bytes, slot words, markers, block offsets, overflow
+bytes and decoded values must all be identical (0 ULP, bit for bit)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from lossless_bf16_tensor_gb300 import binding as B
+from lossless_bf16_tensor_gb300 import synth
+
+from gpu_helpers import (assert_same_format, codebooks, from_device, gpu_decode, gpu_encode, to_device,
+                         workload)
+
+pytestmark = pytest.mark.gpu
+
+
+def _roundtrip(x, model, scale, shape, level, ovf_cap=None):
+    cb, ocb = codebooks(model, scale, shape)
+    ct = gpu_encode(x, cb, level, ovf_cap=ovf_cap)
+    ref = oracle.encode(x, ocb, level, ovf_cap=ovf_cap)
+    got = ct.to_host()
+    assert got["status"] == ref.status
+    assert_same_format(got, ref)
+    if ref.status == oracle.OK:
+        y = gpu_decode(ct, cb)
+        assert np.array_equal(y, x)
+        assert ct.state().status == B.LCT_OK
+    return ct, ref, cb, ocb
+
+
+def test_one_clean_block_gaussian():
+    """65,536 values ~ N(0, 0.02), Gaussian codebook, CLEAN: one block."""
+    x, m, s, sh, lv = workload("gauss_block")
+    ct, ref, cb, _ = _roundtrip(x, m, s, sh, lv)
+    assert ref.delta == 0 and ref.ovf_used == 0
+    st = ct.state()
+    assert st.delta == 0 and st.ovf_used == 0
+
+
+@pytest.mark.parametrize("level", [0, 1, 2])
+@pytest.mark.parametrize("n", [1, 7, 8, 255, 256, 257, 4097, 32767, 32768, 32769, 65535, 65536, 65537,
+                               3 * 65536 + 1234])
+def test_ragged_sizes(level, n):
+    x = synth.laplace(n, 0.01, seed=n)
+    _roundtrip(x, 1, 0.01, 0.0, level)
+
+
+@pytest.mark.parametrize("level", [0, 1, 2])
+def test_every_bf16_pattern(level):
+    """Zeros, subnormals, infinities and every NaN payload survive exactly."""
+    x = synth.all_bf16_patterns()
+    for model, scale, shape in [(0, 0.02, 0.0), (2, 1e-3, 3.0), (1, 1e10, 0.0)]:
+        _roundtrip(x, model, scale, shape, level)
+
+
+@pytest.mark.parametrize("name,n", [("heavy_64m", 5 * 32768 + 17), ("gelu_act", 6 * 32768 - 5)])
+def test_spilling_workloads_small(name, n):
+    x, m, s, sh, lv = workload(name, n)
+    _, ref, _, _ = _roundtrip(x, m, s, sh, lv)
+    if name == "gelu_act":
+        assert ref.ovf_used > 0
+
+
+def test_forced_spill_every_stream():
+    """Every value escapes (exponents far from the codebook): each stream
+    spills, offsets run over every block."""
+    rng = np.random.default_rng(3)
+    e = rng.integers(1, 40, size=3 * 65536 + 99).astype(np.uint16)
+    x = (e << 7) | rng.integers(0, 128, size=e.size).astype(np.uint16)
+    x[::2] |= 0x8000
+    _, ref, _, _ = _roundtrip(x, 0, 1.0, 0.0, 0)
+    assert ref.ovf_used > x.size // 2
+
+
+def test_laplace_16m_full():
+    x, m, s, sh, lv = workload("laplace_16m")
+    _roundtrip(x, m, s, sh, lv)
+
+
+def test_heavy_tail_64m_full():
+    x, m, s, sh, lv = workload("heavy_64m")
+    _roundtrip(x, m, s, sh, lv)
+
+
+def test_gelu_activation_pow2_rounds():
+    """[8, 4096, 3072] GELU activations with 30% zeros, scaled by 2^k for
+    k = -4..4; the shift is re-estimated every round.  Full-size parity on
+    three rounds; on all nine, the shift moves by k and the markers and
+    overflow size do not move at all."""
+    x0, m, s, sh, lv = workload("gelu_act")
+    cb, ocb = codebooks(m, s, sh)
+    markers0 = d0 = used0 = None
+    for k in range(-4, 5):
+        xk = synth.scale_pow2(x0, k)
+        ct = gpu_encode(xk, cb, lv)
+        got = ct.to_host()
+        assert got["status"] == 0
+        if k in (-4, 0, 4):
+            assert_same_format(got, oracle.encode(xk, ocb, lv))
+        if markers0 is None:
+            markers0, d0, used0 = got["markers"].copy(), got["delta"] - k, got["ovf_used"]
+        assert got["delta"] == d0 + k
+        assert np.array_equal(got["markers"], markers0)
+        assert got["ovf_used"] == used0
+        assert np.array_equal(gpu_decode(ct, cb), xk)
+        del ct
+
+
+def test_decode_of_oracle_encoding():
+    """The GPU decoder reads streams written by the oracle (not by the GPU)."""
+    x, m, s, sh, lv = workload("heavy_64m", 4 * 32768 + 1000)
+    cb, ocb = codebooks(0, 1.0, 0.0)
+    ref = oracle.encode(x, ocb, 2, block=32768, slot_words=20)
+    ct = gpu_encode(np.zeros_like(x), cb, 2)           # a valid header for this n
+    torch.cuda.synchronize()
+    r = ct.regions
+    r["sf"].copy_(torch.from_numpy(ref.sf))
+    r["slots"].copy_(torch.from_numpy(ref.slots.view(np.uint8)))
+    r["markers"].copy_(torch.from_numpy(ref.markers.view(np.uint8)))
+    r["blk_off"].copy_(torch.from_numpy(ref.blk_off.view(np.uint8)))
+    r["ovf"][: ref.ovf_used].copy_(torch.from_numpy(ref.ovf[: ref.ovf_used]))
+    hdr = r["header"].cpu().numpy().copy()
+    hdr[20:24] = np.array([ref.delta], np.int32).view(np.uint8)
+    r["header"].copy_(torch.from_numpy(hdr))
+    assert np.array_equal(gpu_decode(ct, cb), x)
+
+
+def test_empty_tensor():
+    cb = B.lct_codebook_build(0, 0.02)
+    ct = B.CompressedTensor(0, 0)
+    B.lct_encode(torch.empty(0, dtype=torch.int16, device="cuda"), cb, ct)
+    y = torch.empty(0, dtype=torch.int16, device="cuda")
+    B.lct_decode(ct, cb, y)
+    st = ct.state()
+    assert st.status == 0 and st.ovf_used == 0
+
+
+def test_overflow_capacity_is_latched():
+    x, m, s, sh, lv = workload("gelu_act", 3 * 32768)
+    cb, ocb = codebooks(m, s, sh)
+    full = oracle.encode(x, ocb, lv)
+    cap = int(full.blk_off[1]) + 3
+    ct, ref, _, _ = _roundtrip(x, m, s, sh, lv, ovf_cap=cap)
+    assert ref.status == oracle.CAPACITY
+    st = ct.state()
+    assert st.status == B.LCT_ERR_OVERFLOW_CAPACITY and st.ovf_used == full.ovf_used
+    y = torch.empty(ct.n, dtype=torch.int16, device="cuda")
+    B.lct_decode(ct, cb, y)
+    assert ct.state().status == B.LCT_ERR_OVERFLOW_CAPACITY
+
+
+def _encoded(n=3 * 65536 + 5):
+    x = synth.laplace(n, 0.01, seed=9)
+    cb = B.lct_codebook_build(1, 0.01)
+    return x, cb, gpu_encode(x, cb, 0)
+
+
+def test_corrupt_marker_is_latched_not_faulted():
+    x, cb, ct = _encoded()
+    mk = ct.regions["markers"].view(torch.int16)
+    mk[300] = 1000                                 # beyond the stream's 256 symbols
+    gpu_decode(ct, cb)
+    assert ct.state().status == B.LCT_ERR_CORRUPT
+
+
+def test_corrupt_slots_are_latched_not_faulted():
+    """Garbage slot words decode without reading outside the slot image; an
+    all-ones slot (every window reads as the longest code) overruns and is
+    reported."""
+    x, cb, ct = _encoded()
+    g = torch.Generator(device="cpu").manual_seed(5)
+    ct.regions["slots"].copy_(torch.randint(0, 256, (ct.regions["slots"].numel(),), generator=g,
+                                            dtype=torch.uint8))
+    gpu_decode(ct, cb)
+    ct.state()
+    x, cb, ct = _encoded()
+    ct.regions["slots"].fill_(0xFF)
+    gpu_decode(ct, cb)
+    assert ct.state().status == B.LCT_ERR_CORRUPT
+
+
+def test_bad_magic_and_wrong_codebook():
+    x, cb, ct = _encoded()
+    other = B.lct_codebook_build(0, 0.02)
+    gpu_decode(ct, other)
+    assert ct.state().status == B.LCT_ERR_CORRUPT
+    x, cb, ct = _encoded()
+    ct.regions["header"][0] = 0
+    gpu_decode(ct, cb)
+    assert ct.state().status == B.LCT_ERR_CORRUPT
+
+
+def test_bounded_wait_runs_out():
+    """A block waiting for a predecessor that never publishes gives up after
+    the limit and latches LCT_ERR_TIMEOUT; the context stays usable."""
+    hdr = torch.zeros(64, dtype=torch.uint8, device="cuda")
+    work = torch.zeros(64, dtype=torch.uint8, device="cuda")
+    B.lct_debug_wait_timeout(hdr, work, 2_000_000)
+    torch.cuda.synchronize()
+    assert int(hdr[24:28].cpu().numpy().view(np.uint32)[0]) == B.LCT_ERR_TIMEOUT
+    x, cb, ct = _encoded(70000)
+    assert np.array_equal(gpu_decode(ct, cb), x)
+
+
+def test_async_on_side_stream():
+    """Calls run on the stream given (here a non-default one)."""
+    x = synth.laplace(2 * 65536 + 3, 0.01, seed=4)
+    cb = B.lct_codebook_build(1, 0.01)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        xd = to_device(x)
+        ct = B.CompressedTensor(x.size, 0)
+        y = torch.empty(x.size, dtype=torch.int16, device="cuda")
+        B.lct_encode(xd, cb, ct, stream=s)
+        B.lct_decode(ct, cb, y, stream=s)
+    s.synchronize()
+    assert np.array_equal(from_device(y), x)

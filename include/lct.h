@@ -198,6 +198,36 @@ lct_status lct_compressed_size(uint64_t n, int level, const lct_tensor *t, void 
 lct_status lct_encode(const uint16_t *d_x, const lct_codebook *cb, const lct_tensor *t,
                       void *stream);
 
+/* lct_encode for callers that cannot allocate device memory.  (The paper has
+ * no counterpart: this is a convenience of this library.)
+ *
+ * lct_encode needs `t->d_work`, a little device scratch (8 bytes per block)
+ * for the scan that places each block's overflow bytes.  Some callers cannot
+ * allocate it: a caching allocator or out-of-memory handler that compresses
+ * tensors to free space would have to re-enter the allocator, or fail for
+ * lack of memory, to get scratch; other code must avoid cudaMalloc/cudaFree
+ * because they can synchronise the device.  This variant allocates nothing:
+ * its scratch is a fixed array of LCT_STATIC_SCRATCH_BLOCKS 8-byte words
+ * (128 KiB) compiled into the library, which every GPU that loads the library
+ * holds until the process exits.  `t->d_work` is ignored and may be NULL;
+ * everything else is exactly as for lct_encode (same checks, same output,
+ * bit for bit).
+ *   - Tensors needing more than LCT_STATIC_SCRATCH_BLOCKS blocks (n above
+ *     2^30 values in CLEAN, 2^29 in MEDIUM and HIGH) are rejected with
+ *     LCT_ERR_UNSUPPORTED before anything is enqueued.
+ *   - The first call on a device looks up the array's device address (with
+ *     that device current) and keeps it; make that first call before any
+ *     stream capture.
+ *   - All calls share the one array.  Each call clears the words it uses
+ *     before using them, but calls whose GPU work overlaps -- on different
+ *     streams, or from different threads -- race on the array and may produce
+ *     wrong overflow offsets.  Serialise them.
+ * Errors: as lct_encode, plus LCT_ERR_UNSUPPORTED (too large) and
+ * LCT_ERR_CUDA (the device address could not be obtained). */
+#define LCT_STATIC_SCRATCH_BLOCKS 16384
+lct_status lct_encode_static_scratch(const uint16_t *d_x, const lct_codebook *cb, const lct_tensor *t,
+                                     void *stream);
+
 /* Reconstruct the n BF16 values of `t` into d_y (device, 16-byte aligned),
  * bit for bit ([EXP] "In bits": every value decodes exactly).  `cb` must be
  * the codebook the tensor was written with (checked on the device by hash).

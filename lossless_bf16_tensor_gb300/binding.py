@@ -32,6 +32,7 @@ STATUS_NAMES = {0: "LCT_OK", 1: "LCT_ERR_INVALID_ARG", 2: "LCT_ERR_UNSUPPORTED",
 LCT_MODEL_GAUSSIAN, LCT_MODEL_LAPLACE, LCT_MODEL_POWERLAW = 0, 1, 2
 LCT_LEVEL_CLEAN, LCT_LEVEL_MEDIUM, LCT_LEVEL_HIGH = 0, 1, 2
 LCT_HEADER_BYTES = 64
+LCT_STATIC_SCRATCH_BLOCKS = 16384
 LCT_MAGIC = 0x3154434C
 MODELS = {"gaussian": 0, "laplace": 1, "powerlaw": 2}
 LEVELS = {"CLEAN": 0, "MEDIUM": 1, "HIGH": 2}
@@ -80,8 +81,9 @@ _lib.lct_sgd_step_fused.argtypes = [ctypes.POINTER(lct_tensor), ctypes.POINTER(l
                                     ctypes.POINTER(lct_tensor), ctypes.POINTER(lct_codebook), ctypes.c_float,
                                     ctypes.POINTER(lct_tensor), _P]
 _lib.lct_debug_wait_timeout.argtypes = [_P, _P, ctypes.c_uint64, _P]
+_lib.lct_encode_static_scratch.argtypes = [_P, ctypes.POINTER(lct_codebook), ctypes.POINTER(lct_tensor), _P]
 for _fn in ("lct_codebook_build", "lct_compressed_size", "lct_encode", "lct_decode", "lct_sgd_step_fused",
-            "lct_debug_wait_timeout"):
+            "lct_debug_wait_timeout", "lct_encode_static_scratch"):
     getattr(_lib, _fn).restype = ctypes.c_int
 
 
@@ -136,6 +138,15 @@ def _dev_ptr(x: torch.Tensor, n: int) -> int:
 def lct_encode(x: torch.Tensor, cb: lct_codebook, t: "CompressedTensor", stream=None) -> None:
     ptr = _dev_ptr(x, t.n) if t.n else None
     _check(_lib.lct_encode(ptr, ctypes.byref(cb), ctypes.byref(t.desc), _stream(stream)), "lct_encode")
+
+
+def lct_encode_static_scratch(x: torch.Tensor, cb: lct_codebook, t: "CompressedTensor", stream=None) -> None:
+    """lct_encode without caller-provided scratch: for callers that cannot
+    allocate device memory (e.g. an allocator compressing tensors to free
+    space); the library's fixed scratch array is used instead of t's."""
+    ptr = _dev_ptr(x, t.n) if t.n else None
+    _check(_lib.lct_encode_static_scratch(ptr, ctypes.byref(cb), ctypes.byref(t.desc), _stream(stream)),
+           "lct_encode_static_scratch")
 
 
 def lct_decode(t: "CompressedTensor", cb: lct_codebook, y: torch.Tensor, stream=None) -> None:

@@ -181,6 +181,7 @@ extern "C" lct_status lct_decode(const lct_tensor *t, const lct_codebook *cb, ui
     a.t = dev_view(t, s);
     a.y = d_y;
     a.cb = dev_codebook(*cb);
+    a.wait_ns = kDefaultWaitNs;
     return launch_decode(a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? LCT_OK : LCT_ERR_CUDA;
 }
 
@@ -224,7 +225,7 @@ extern "C" lct_status lct_sgd_step_fused(const lct_tensor *W_in, const lct_codeb
     a.cbw = dev_codebook(*cbW);
     a.cbm = dev_codebook(*cbM);
     a.eta = eta;
-    a.pad = 0;
+    a.in_place = W_out->d_sf == W_in->d_sf ? 1u : 0u;
     a.wait_ns = kDefaultWaitNs;
     return launch_sgd(a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? LCT_OK : LCT_ERR_CUDA;
 }

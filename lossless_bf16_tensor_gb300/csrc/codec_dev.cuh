@@ -1,6 +1,7 @@
 // Device building blocks of the LCT codec for sm_103a: byte split and join,
-// the per-stream coder and decoder, block-wide scans and the bounded
-// decoupled look-back that places each block's overflow bytes.
+// per-stream coding and decoding, block-wide scans, TMA bulk copies with
+// bounded mbarrier waits, and the bounded decoupled look-back that places
+// each block's overflow bytes.
 //
 // Sources: [EXP] "LCT paper -- Lossless Huffman coding of BF16 training
 // tensors -- What does it mean?", paragraphs "In bits" (byte split, 8-bit
@@ -30,67 +31,28 @@ struct Geo<LCT_LEVEL_HIGH> {
     static constexpr int B = 32768, W = 20, NJ = 128;
 };
 
-// Exponents of a block are staged in shared memory as rows of 256 (one symbol
-// of every stream); a row is padded to 260 bytes so that a warp walking one
-// stream down the rows hits 32 different banks.
+// Staged exponent rows hold one symbol of every stream; a row is padded to
+// 260 bytes so that a warp walking one stream down the rows hits 32 banks.
 constexpr int kRow = 260;
+constexpr unsigned kFull = 0xFFFFFFFFu;
 
-// Shared-memory carve-up; every region starts on a 128-byte boundary so that
-// 16-byte vector accesses to the regions after the staging rows stay aligned.
-template <int LEVEL>
-struct Smem {
-    static constexpr int kExpBytes = ((Geo<LEVEL>::NJ + 1) * kRow + 127) / 128 * 128;  // + guard row
-    static constexpr int kSlotBytes = (Geo<LEVEL>::W + 1) * kStreams * 4;              // + zero row
-    static_assert(kExpBytes % 128 == 0 && kSlotBytes % 128 == 0, "regions must stay 16-byte aligned");
-};
+__device__ __forceinline__ void latch(lct_header *h, uint32_t code) { atomicCAS(&h->status, 0u, code); }
 
-__device__ __forceinline__ void latch(lct_header *h, uint32_t code)
+__device__ __forceinline__ uint64_t global_ns()
 {
-    atomicCAS(&h->status, 0u, code);
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
 }
 
 // ------------------------------------------------------------ byte split
 
-// Eight BF16 values (one uint4, little endian) -> 8 sign-fraction bytes and
-// 8 exponent bytes, in element order.  High byte of a BF16 = sign | e[7:1],
-// low byte = e[0] | fraction.
-__device__ __forceinline__ void split8(const uint4 v, uint2 &sf, uint2 &ex)
-{
-    uint32_t hb = __byte_perm(v.x, v.y, 0x7531), lb = __byte_perm(v.x, v.y, 0x6420);
-    ex.x = ((hb << 1) & 0xFEFEFEFEu) | ((lb >> 7) & 0x01010101u);
-    sf.x = (hb & 0x80808080u) | (lb & 0x7F7F7F7Fu);
-    hb = __byte_perm(v.z, v.w, 0x7531);
-    lb = __byte_perm(v.z, v.w, 0x6420);
-    ex.y = ((hb << 1) & 0xFEFEFEFEu) | ((lb >> 7) & 0x01010101u);
-    sf.y = (hb & 0x80808080u) | (lb & 0x7F7F7F7Fu);
-}
+__device__ __forceinline__ uint8_t exp_of(uint32_t h) { return (uint8_t)((h >> 7) & 0xFF); }
+__device__ __forceinline__ uint8_t sf_of(uint32_t h) { return (uint8_t)(((h >> 8) & 0x80) | (h & 0x7F)); }
 
-__device__ __forceinline__ uint4 join8(const uint2 sf, const uint2 ex)
-{
-    uint4 v;
-    uint32_t hb = (sf.x & 0x80808080u) | ((ex.x >> 1) & 0x7F7F7F7Fu);
-    uint32_t lb = ((ex.x << 7) & 0x80808080u) | (sf.x & 0x7F7F7F7Fu);
-    v.x = __byte_perm(lb, hb, 0x5140);
-    v.y = __byte_perm(lb, hb, 0x7362);
-    hb = (sf.y & 0x80808080u) | ((ex.y >> 1) & 0x7F7F7F7Fu);
-    lb = ((ex.y << 7) & 0x80808080u) | (sf.y & 0x7F7F7F7Fu);
-    v.z = __byte_perm(lb, hb, 0x5140);
-    v.w = __byte_perm(lb, hb, 0x7362);
-    return v;
-}
-
-__device__ __forceinline__ uint8_t exp_of(uint16_t h) { return (uint8_t)((h >> 7) & 0xFF); }
-__device__ __forceinline__ uint8_t sf_of(uint16_t h) { return (uint8_t)(((h >> 8) & 0x80) | (h & 0x7F)); }
-__device__ __forceinline__ uint16_t join1(uint8_t sf, uint8_t e)
-{
-    return (uint16_t)(((uint32_t)(sf & 0x80) << 8) | ((uint32_t)e << 7) | (sf & 0x7F));
-}
-
-// Staged exponents of in-block group g (8 values, row g/32, column 8*(g%32)).
-__device__ __forceinline__ uint8_t *stage_at(uint8_t *e_s, uint32_t i)
-{
-    return e_s + (i >> 8) * kRow + (i & 255);
-}
+// BF16 from a sign-fraction byte and an exponent already shifted to bits
+// 7..14: sf * 0x101 puts the sign at bit 15 and keeps the fraction in bits 0..6.
+__device__ __forceinline__ uint32_t join_e7(uint32_t sf, uint32_t e7) { return ((sf * 0x101u) & 0x807Fu) | e7; }
 
 // --------------------------------------------------------- code tables
 
@@ -111,84 +73,124 @@ __device__ __forceinline__ uint2 enc_entry(const DevCodebook &cb, int delta, int
     return make_uint2(code << (32u - len), len);
 }
 
-// Decode table for shift delta, by 8-bit window: bits 0..7 exponent (coded
-// symbols), 8..15 bits consumed, 16..23 literal offset, bit 24 escape.
+// Decode table for shift delta, indexed by the next 8 bits of the stream:
+//   bits  7..14  the exponent, for a symbol with its own code (0 for escape)
+//   bits 16..23  bits consumed (code length, or escape length + 8)
+//   bits 24..31  for the escape: its length (the literal follows it);
+//                otherwise 32, which shifts the literal out entirely
 __device__ __forceinline__ uint32_t dec_entry(const DevCodebook &cb, int delta, int v)
 {
     const uint32_t d = cb.dec[v], sym = d & 0x1FF, l = d >> 12;
-    if (sym == 256) return (1u << 24) | (l << 16) | ((l + 8u) << 8);
-    return (l << 8) | ((sym + (uint32_t)delta) & 0xFFu);
+    if (sym == 256) return (l << 24) | ((l + 8u) << 16);
+    return (32u << 24) | (l << 16) | (((sym + (uint32_t)delta) & 0xFFu) << 7);
 }
 
-// ------------------------------------------------------ stream coding
+// ------------------------------------------------------ stream decoding
 
-// Code stream j: its symbols are column j of the staged rows.  Codes are
-// appended most significant bit first while they fit the W-word slot; the
-// first code that does not fit ends the slot (the marker).  Writes every slot
-// word (unused bits zero) at slot_col[w * 256].  Returns the marker.
-template <int W, int NJ>
-__device__ __forceinline__ uint32_t encode_stream(const uint8_t *__restrict__ col, uint32_t nj,
-                                                  const uint2 *__restrict__ tbl,
-                                                  uint32_t *__restrict__ slot_col)
-{
-    uint32_t hi = 0, nbits = 0, wi = 0, rem = 32u * W, marker = nj;
-    const uint32_t count = NJ > 0 ? (uint32_t)NJ : nj;
-#pragma unroll 8
-    for (uint32_t k = 0; k < count; ++k) {
-        const uint2 ent = tbl[col[k * kRow]];
-        if (ent.y > rem) {
-            marker = k;
-            break;
-        }
-        rem -= ent.y;
-        const uint32_t merged = hi | (ent.x >> nbits);
-        nbits += ent.y;
-        if (nbits >= 32u) {
-            slot_col[wi * kStreams] = merged;
-            ++wi;
-            hi = ent.x << (32u - (nbits - ent.y));
-            nbits -= 32u;
-        } else {
-            hi = merged;
-        }
-    }
-    if (wi < (uint32_t)W) {
-        slot_col[wi * kStreams] = hi;
-        for (uint32_t w = wi + 1; w < (uint32_t)W; ++w) slot_col[w * kStreams] = 0u;
-    }
-    return marker;
-}
+// Reads one stream's slot, most significant bit first.  `buf` holds the next
+// `nb` bits at its top; `nxt` is the next slot word, already loaded.  The
+// slot image has a zero guard row after its W rows and reads past the slot
+// stay on that row, so a corrupt stream never reads outside the image.
+struct BitReader {
+    uint64_t buf;
+    uint32_t nb, wi, nxt;
+};
 
-// Decode `count` symbols of one stream from its slot image (W words plus a
-// zero guard word) into column j of the staged rows.  Returns the bits
-// consumed; more than 32*W means the slot was corrupt (reads stay in the
-// image because the word index is clamped).
 template <int W>
-__device__ __forceinline__ uint32_t decode_stream(const uint32_t *__restrict__ slot_col, uint32_t count,
-                                                  const uint32_t *__restrict__ lut,
-                                                  uint8_t *__restrict__ col)
+__device__ __forceinline__ void br_init(BitReader &r, const uint32_t *col)
 {
-    uint32_t p = 0;
-#pragma unroll 4
-    for (uint32_t k = 0; k < count; ++k) {
-        const uint32_t w = min(p >> 5, (uint32_t)(W - 1));
-        const uint32_t hiw = slot_col[w * kStreams], low = slot_col[(w + 1) * kStreams];
-        const uint32_t win = __funnelshift_l(low, hiw, p);
-        const uint32_t ent = lut[win >> 24];
-        const uint32_t lit = (win << ((ent >> 16) & 0xFFu)) >> 24;
-        col[k * kRow] = (uint8_t)((ent & (1u << 24)) ? lit : ent);
-        p += (ent >> 8) & 0xFFu;
+    r.buf = ((uint64_t)col[0] << 32) | col[kStreams];
+    r.nb = 64;
+    r.wi = 2;
+    r.nxt = col[2 * kStreams];
+}
+
+// Keep at least 32 bits ahead: two symbols (at most 16 bits each) can then be
+// taken without another refill.
+template <int W>
+__device__ __forceinline__ void br_refill(BitReader &r, const uint32_t *col)
+{
+    if (r.nb < 32) {
+        r.buf |= (uint64_t)r.nxt << (32 - r.nb);
+        r.nb += 32;
+        ++r.wi;
+        r.nxt = col[min(r.wi, (uint32_t)W) * kStreams];
     }
-    return p;
+}
+
+// One symbol: returns the exponent shifted to bits 7..14.
+__device__ __forceinline__ uint32_t br_symbol(BitReader &r, const uint32_t *lut)
+{
+    const uint32_t top = (uint32_t)(r.buf >> 32);
+    const uint32_t ent = lut[top >> 24];
+    const uint32_t lit = __funnelshift_lc(0u, top, ent >> 24);
+    const uint32_t adv = (ent >> 16) & 0xFFu;
+    r.buf <<= adv;
+    r.nb -= adv;
+    return ((lit >> 17) | ent) & 0x7F80u;
+}
+
+// Bits taken from the slot so far (more than 32*W means a corrupt stream).
+__device__ __forceinline__ uint32_t br_consumed(const BitReader &r) { return 32u * r.wi - r.nb; }
+
+// ------------------------------------------------------- stream coding
+
+// Appends codes most significant bit first into one stream's W-word slot
+// image (word w at col[w * 256]) until the first code that does not fit; that
+// symbol's index is the marker.
+struct BitWriter {
+    uint32_t hi, nbits, wi, rem, marker;
+    bool alive;
+};
+
+template <int W>
+__device__ __forceinline__ void bw_init(BitWriter &w, uint32_t nj)
+{
+    w.hi = 0;
+    w.nbits = 0;
+    w.wi = 0;
+    w.rem = 32u * W;
+    w.marker = nj;
+    w.alive = true;
+}
+
+__device__ __forceinline__ void bw_put(BitWriter &w, const uint2 ent, uint32_t k, uint32_t *col)
+{
+    if (!w.alive) return;
+    if (ent.y > w.rem) {
+        w.alive = false;
+        w.marker = k;
+        return;
+    }
+    w.rem -= ent.y;
+    const uint32_t merged = w.hi | (ent.x >> w.nbits);
+    const uint32_t n2 = w.nbits + ent.y;
+    if (n2 >= 32u) {
+        col[w.wi * kStreams] = merged;
+        ++w.wi;
+        w.hi = ent.x << (32u - w.nbits);
+        w.nbits = n2 - 32u;
+    } else {
+        w.hi = merged;
+        w.nbits = n2;
+    }
+}
+
+// Write the partly filled word and zero the rest of the slot.
+template <int W>
+__device__ __forceinline__ void bw_finish(const BitWriter &w, uint32_t *col)
+{
+    if (w.wi < (uint32_t)W) {
+        col[w.wi * kStreams] = w.hi;
+        for (uint32_t i = w.wi + 1; i < (uint32_t)W; ++i) col[i * kStreams] = 0u;
+    }
 }
 
 // ------------------------------------------------------------- scans
 
-// Exclusive scan of one value per thread over `nthreads` consecutive threads
-// starting at warp `first_warp` (nthreads a multiple of 32, at most 1024).
-// `warp_tot` holds one word per warp.  Returns the exclusive prefix; *total
-// gets the sum.  Must be called by all threads of the group; contains
-// __syncthreads() so the whole CTA must call it.
+// Exclusive scan of one value per thread over `group_warps` warps starting at
+// warp `first_warp`; *total gets the group's sum.  Contains __syncthreads(),
+// so every thread of the CTA must call it.
 __device__ __forceinline__ uint32_t group_exclusive_scan(uint32_t v, uint32_t *warp_tot, int group_warps,
                                                          int first_warp, uint32_t *total)
 {
@@ -196,7 +198,7 @@ __device__ __forceinline__ uint32_t group_exclusive_scan(uint32_t v, uint32_t *w
     uint32_t inc = v;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-        const uint32_t t = __shfl_up_sync(0xFFFFFFFFu, inc, o);
+        const uint32_t t = __shfl_up_sync(kFull, inc, o);
         if (lane >= o) inc += t;
     }
     if (lane == 31) warp_tot[warp] = inc;
@@ -211,6 +213,84 @@ __device__ __forceinline__ uint32_t group_exclusive_scan(uint32_t v, uint32_t *w
     __syncthreads();
     return before + inc - v;
 }
+
+// ------------------------------------------- TMA bulk copies, mbarriers
+
+__device__ __forceinline__ uint32_t smem_addr(const void *p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count)
+{
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count) : "memory");
+}
+
+// Make initialised mbarriers visible to the async (TMA) proxy.
+__device__ __forceinline__ void fence_mbar_init()
+{
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint64_t *bar, uint32_t bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try(uint64_t *bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_addr(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Wait for phase `parity` of `bar` to complete, giving up after limit_ns of
+// %globaltimer.  Returns false if it gave up.
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, uint64_t limit_ns)
+{
+    if (mbar_try(bar, parity)) return true;
+    const uint64_t t0 = global_ns();
+    for (uint32_t i = 1;; ++i) {
+        if (mbar_try(bar, parity)) return true;
+        if ((i & 15u) == 0 && global_ns() - t0 > limit_ns) return false;
+    }
+}
+
+// Global -> shared bulk copy (TMA, no tensor map); completes on `bar`.  Both
+// addresses 16-byte aligned, `bytes` a multiple of 16.
+__device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t bytes, uint64_t *bar)
+{
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                     smem_addr(dst)),
+                 "l"(src), "r"(bytes), "r"(smem_addr(bar))
+                 : "memory");
+}
+
+// Shared -> global bulk copy, tracked by bulk groups.
+__device__ __forceinline__ void bulk_store(void *dst, const void *src, uint32_t bytes)
+{
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst), "r"(smem_addr(src)),
+                 "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
+// Make this thread's generic-proxy shared-memory writes visible to the async
+// proxy (before a bulk store reads them).
+__device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
+// Programmatic dependent launch: let the next kernel in the stream start its
+// independent work, and wait for the previous kernel's results.
+__device__ __forceinline__ void pdl_launch_dependents()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
 // ------------------------------------------------ decoupled look-back
 
@@ -230,29 +310,59 @@ __device__ __forceinline__ void st_release(unsigned long long *p, unsigned long 
     asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
 }
 
-__device__ __forceinline__ uint64_t global_ns()
+// One full warp of block b: publish the block's overflow byte count, then
+// read the status words of the 32 nearest predecessors at once, add their
+// counts up to the nearest published inclusive prefix, and move 32 further
+// back while none is found.  Publishes the inclusive prefix and returns the
+// exclusive one (same value in every lane).  Every wait is bounded by wait_ns
+// of %globaltimer and an iteration cap; on expiry *timed_out is set and the
+// prefix found so far is used, so later blocks are never stuck.
+static __device__ __noinline__ unsigned long long warp_lookback(unsigned long long *status, uint32_t b,
+                                                                unsigned long long total, uint64_t wait_ns,
+                                                                bool *timed_out)
 {
-    uint64_t t;
-    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-    return t;
+    const int lane = threadIdx.x & 31;
+    *timed_out = false;
+    if (b == 0) {
+        if (lane == 0) st_release(&status[0], kFlagInc | total);
+        return 0;
+    }
+    if (lane == 0) st_release(&status[b], kFlagAgg | total);
+    unsigned long long excl = 0;
+    int64_t nearest = (int64_t)b - 1;
+    const uint64_t t0 = global_ns();
+    uint32_t spins = 0;
+    for (;;) {
+        const int64_t idx = nearest - lane;
+        const unsigned long long v = idx >= 0 ? ld_acquire(&status[idx]) : kFlagInc;
+        const uint32_t flag = (uint32_t)(v >> 62);
+        const uint32_t inc = __ballot_sync(kFull, flag == 2u);
+        const uint32_t not_ready = __ballot_sync(kFull, flag == 0u);
+        const uint32_t upto = inc ? ((inc & (0u - inc)) << 1) - 1u : kFull;  // lanes up to the nearest inclusive
+        if (not_ready & upto) {
+            ++spins;
+            if (spins > (1u << 24) || ((spins & 63u) == 0 && global_ns() - t0 > wait_ns)) {
+                *timed_out = true;
+                break;
+            }
+            __nanosleep(32);
+            continue;
+        }
+        unsigned long long mine = ((upto >> lane) & 1u) ? (v & kValMask) : 0ull;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) mine += __shfl_xor_sync(kFull, mine, o);
+        excl += mine;
+        if (inc) break;
+        nearest -= 32;
+    }
+    if (lane == 0) st_release(&status[b], kFlagInc | ((excl + total) & kValMask));
+    return excl;
 }
 
-// Programmatic dependent launch: let the next kernel in the stream start its
-// independent prologue, and wait for the previous kernel's results.
-__device__ __forceinline__ void pdl_launch_dependents()
-{
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-}
-__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
-
-// One thread of block b: publish the block's overflow byte count, add up the
-// predecessors' counts (stopping at the first inclusive prefix), publish the
-// inclusive prefix and return the exclusive one.  Every wait is bounded by
-// wait_ns of %globaltimer and an iteration cap; on expiry *timed_out is set
-// and the prefix found so far is used, so later blocks are never stuck.
+// The same protocol run by a single thread (used by the wait-timeout test hook).
 static __device__ __noinline__ unsigned long long lookback(unsigned long long *status, uint32_t b,
-                                                     unsigned long long total, uint64_t wait_ns,
-                                                     bool *timed_out)
+                                                           unsigned long long total, uint64_t wait_ns,
+                                                           bool *timed_out)
 {
     *timed_out = false;
     if (b == 0) {
@@ -282,6 +392,23 @@ static __device__ __noinline__ unsigned long long lookback(unsigned long long *s
     }
     st_release(&status[b], kFlagInc | ((excl + total) & kValMask));
     return excl;
+}
+
+// Launch a kernel as a programmatic dependent of the previous work in `s`.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*k)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s, Args &&...args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, k, static_cast<Args &&>(args)...);
 }
 
 }  // namespace dev

@@ -5,46 +5,77 @@
 // [EXP] "Compressing is easy": each of the 256 streams decodes independently
 // from its fixed-length slot up to its spill marker, then takes its spilled
 // exponents from the uncompressed overflow region.
+//
+// Thread j owns stream j.  The block's slot image is fetched once with a TMA
+// bulk copy; the sign-fraction bytes stream through a ring of row chunks that
+// TMA keeps filled ahead of the decoders; every row the 256 threads decode
+// together is written out as 512 contiguous bytes.
 #include "codec_dev.cuh"
 
 namespace lct {
 namespace dev {
 
+constexpr int kDecRows = 16;  // rows per sign-fraction chunk
+constexpr int kDecRing = 4;   // chunks in flight
+
 template <int LEVEL>
-__global__ void __launch_bounds__(256, 2) k_decode(const __grid_constant__ DecodeArgs a)
+struct DecodeSmem {
+    static constexpr int W = Geo<LEVEL>::W;
+    static constexpr int kSlot = (W + 1) * kStreams * 4;  // slot image + zero guard row
+    static constexpr int kRing = kDecRing * kDecRows * kStreams;
+    static constexpr int kLut = 256 * 4;
+    static constexpr int kBytes = kSlot + kRing + kLut;
+};
+
+template <int LEVEL>
+__global__ void __launch_bounds__(256, 4) k_decode(const __grid_constant__ DecodeArgs a)
 {
     using G = Geo<LEVEL>;
-    extern __shared__ __align__(16) uint8_t smem[];
-    uint8_t *e_s = smem;
-    uint32_t *slot_s = reinterpret_cast<uint32_t *>(smem + Smem<LEVEL>::kExpBytes);
-    uint32_t *lut = reinterpret_cast<uint32_t *>(smem + Smem<LEVEL>::kExpBytes + Smem<LEVEL>::kSlotBytes);
+    using L = DecodeSmem<LEVEL>;
+    constexpr int W = G::W, R = kDecRows, S = kDecRing;
+    extern __shared__ __align__(128) uint8_t smem[];
+    uint32_t *slot_s = reinterpret_cast<uint32_t *>(smem);
+    uint8_t *sf_s = smem + L::kSlot;
+    uint32_t *lut = reinterpret_cast<uint32_t *>(smem + L::kSlot + L::kRing);
+    __shared__ __align__(8) uint64_t bar_slot, bar_sf[S];
     __shared__ uint32_t warp_tot[8];
+    __shared__ uint32_t s_timeout;
 
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int tid = threadIdx.x;
+    const uint32_t j = tid;
     const uint32_t b = blockIdx.x;
     const uint64_t base = (uint64_t)b * G::B;
     const uint32_t nb = (uint32_t)min((uint64_t)G::B, a.t.n - base);
-    lct_header *hdr = a.t.hdr;
+    const uint32_t nrows = (nb + 255) >> 8, nbulk = (nb >> 8) / R, nchunks = (nrows + R - 1) / R;
+    const uint64_t limit = a.wait_ns;
 
-    // The header must describe this tensor and this codebook.
+    if (tid == 0) {
+        mbar_init(&bar_slot, 1);
+        for (int s = 0; s < S; ++s) mbar_init(&bar_sf[s], 1);
+        fence_mbar_init();
+        s_timeout = 0;
+    }
+    // Everything below reads what earlier work in the stream wrote.
+    pdl_wait();
+    lct_header *hdr = a.t.hdr;
     const bool hdr_ok = hdr->magic == LCT_MAGIC && hdr->n == a.t.n && hdr->level == LEVEL &&
                         hdr->cb_hash == a.cb.hash;
     if (!hdr_ok) {
         if (tid == 0) latch(hdr, LCT_ERR_CORRUPT);
-        return;
+        return;  // no copy has been issued yet
     }
-    const int delta = hdr->delta;
-    lut[tid] = dec_entry(a.cb, delta, tid);
+    lut[tid] = dec_entry(a.cb, hdr->delta, tid);
+    slot_s[W * kStreams + tid] = 0u;
+    __syncthreads();  // barriers initialised
+    if (tid == 0) {
+        mbar_expect_tx(&bar_slot, W * kStreams * 4);
+        bulk_load(slot_s, a.t.slots + (uint64_t)b * W * kStreams, W * kStreams * 4, &bar_slot);
+        for (uint32_t c = 0; c < (uint32_t)S && c < nbulk; ++c) {
+            mbar_expect_tx(&bar_sf[c], R * kStreams);
+            bulk_load(sf_s + c * R * kStreams, a.t.sf + base + (uint64_t)c * R * kStreams, R * kStreams, &bar_sf[c]);
+        }
+    }
 
-    // slot image of this block plus one zero guard row
-    {
-        const uint4 *src = reinterpret_cast<const uint4 *>(a.t.slots + (uint64_t)b * G::W * kStreams);
-        uint4 *dst = reinterpret_cast<uint4 *>(slot_s);
-#pragma unroll 5
-        for (int w = tid; w < G::W * kStreams / 4; w += 256) dst[w] = __ldcs(src + w);
-        slot_s[G::W * kStreams + tid] = 0u;
-    }
-    const uint32_t j = tid;
     const uint32_t nj = nb > j ? (nb - j + 255) / 256 : 0;
     uint32_t marker = a.t.markers[(uint64_t)b * kStreams + j];
     bool bad = marker > nj;
@@ -52,50 +83,72 @@ __global__ void __launch_bounds__(256, 2) k_decode(const __grid_constant__ Decod
     const uint32_t spill = nj - marker;
     uint32_t total;
     const uint32_t pre = group_exclusive_scan(spill, warp_tot, 8, 0, &total);  // syncs
-
     const uint64_t off0 = a.t.blk_off[b], off1 = a.t.blk_off[b + 1];
     const bool ovf_ok = off1 <= a.t.ovf_cap && off0 <= off1 && off1 - off0 == total;
+    // index of this stream's spilled symbol k in the overflow region is
+    // ovf_at + k (k >= marker)
+    const uint64_t ovf_at = off0 + pre - marker;
 
-    const uint32_t bits = decode_stream<G::W>(slot_s + j, marker, lut, e_s + j);
-    bad |= bits > 32u * G::W;
-    if (bad) latch(hdr, LCT_ERR_CORRUPT);
-    if (tid == 0 && !ovf_ok)
-        latch(hdr, off1 > a.t.ovf_cap && off0 <= off1 ? LCT_ERR_OVERFLOW_CAPACITY : LCT_ERR_CORRUPT);
+    if (!mbar_wait(&bar_slot, 0, limit)) s_timeout = 1;
+    BitReader rd;
+    const uint32_t *col = slot_s + j;
+    br_init<W>(rd, col);
+    uint16_t *yj = a.y + base + j;
 
-    // spilled exponents: one warp per stream at a time
-    if (total > 0 && ovf_ok) {
-        const uint8_t *in = a.t.ovf + off0;
-        for (int i = 0; i < 32; ++i) {
-            const uint32_t sm = __shfl_sync(0xFFFFFFFFu, marker, i);
-            const uint32_t sp = __shfl_sync(0xFFFFFFFFu, spill, i);
-            const uint32_t so = __shfl_sync(0xFFFFFFFFu, pre, i);
-            const uint32_t sj = (uint32_t)(warp * 32 + i);
-            for (uint32_t l = lane; l < sp; l += 32) e_s[(sm + l) * kRow + sj] = __ldg(in + so + l);
+    for (uint32_t c = 0; c < nchunks; ++c) {
+        const bool bulk = c < nbulk;
+        const uint32_t slot = c % S;
+        if (bulk && !mbar_wait(&bar_sf[slot], (c / S) & 1u, s_timeout ? 1000000ull : limit)) s_timeout = 1;
+        const uint8_t *sfc = sf_s + slot * R * kStreams + j;
+#pragma unroll
+        for (int r = 0; r < R; r += 2) {
+            br_refill<W>(rd, col);
+#pragma unroll
+            for (int q = 0; q < 2; ++q) {
+                const uint32_t k = c * R + r + q;
+                if (bulk || k < nj) {
+                    uint32_t e7;
+                    if (k < marker)
+                        e7 = br_symbol(rd, lut);
+                    else
+                        e7 = ovf_ok ? (uint32_t)__ldg(a.t.ovf + ovf_at + k) << 7 : 0u;
+                    const uint32_t sf = bulk ? sfc[(r + q) * kStreams] : a.t.sf[base + (uint64_t)k * kStreams + j];
+                    yj[(uint64_t)k * kStreams] = (uint16_t)join_e7(sf, e7);
+                }
+            }
+        }
+        __syncthreads();  // every thread is done with this chunk's ring slot
+        if (tid == 0 && c + S < nbulk) {
+            mbar_expect_tx(&bar_sf[slot], R * kStreams);
+            bulk_load(sf_s + slot * R * kStreams, a.t.sf + base + (uint64_t)(c + S) * R * kStreams, R * kStreams,
+                      &bar_sf[slot]);
         }
     }
-    __syncthreads();
-
-    // reassemble: sign-fraction bytes + exponents -> BF16, 8 values per step
-    const uint2 *sfv = reinterpret_cast<const uint2 *>(a.t.sf + base);
-    uint4 *yv = reinterpret_cast<uint4 *>(a.y + base);
-    const uint32_t ng = nb >> 3;
-#pragma unroll 4
-    for (uint32_t g = tid; g < ng; g += 256) {
-        const uint2 sf = __ldcs(sfv + g);
-        const uint32_t *ep = reinterpret_cast<const uint32_t *>(stage_at(e_s, g << 3));
-        __stcs(yv + g, join8(sf, make_uint2(ep[0], ep[1])));
+    pdl_launch_dependents();
+    if (tid == 0 && s_timeout) {
+        // a wait gave up: let every copy still in flight land before the CTA
+        // (and its shared memory) goes away
+        mbar_wait(&bar_slot, 0, limit);
+        for (uint32_t s = 0; s < (uint32_t)S && s < nbulk; ++s) {
+            const uint32_t last = s + (nbulk - 1 - s) / S * S;
+            mbar_wait(&bar_sf[s], (last / S) & 1u, limit);
+        }
     }
-    for (uint32_t i = (ng << 3) + tid; i < nb; i += 256) a.y[base + i] = join1(a.t.sf[base + i], *stage_at(e_s, i));
+    bad |= br_consumed(rd) > 32u * W;
+    if (bad) latch(hdr, LCT_ERR_CORRUPT);
+    if (tid == 0) {
+        if (!ovf_ok) latch(hdr, off1 > a.t.ovf_cap && off0 <= off1 ? LCT_ERR_OVERFLOW_CAPACITY : LCT_ERR_CORRUPT);
+        if (s_timeout) latch(hdr, LCT_ERR_TIMEOUT);
+    }
 }
 
 template <int LEVEL>
 cudaError_t launch_level(const DecodeArgs &a, cudaStream_t s)
 {
-    constexpr int smem = Smem<LEVEL>::kExpBytes + Smem<LEVEL>::kSlotBytes + 256 * 4;
+    constexpr int smem = DecodeSmem<LEVEL>::kBytes;
     cudaError_t err = cudaFuncSetAttribute(k_decode<LEVEL>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (err != cudaSuccess) return err;
-    k_decode<LEVEL><<<a.t.nblocks, 256, smem, s>>>(a);
-    return cudaGetLastError();
+    return launch_pdl(k_decode<LEVEL>, dim3(a.t.nblocks), dim3(256), smem, s, a);
 }
 
 }  // namespace dev

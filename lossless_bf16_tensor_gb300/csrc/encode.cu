@@ -6,19 +6,39 @@
 // [EXP] "Compressing is easy": blocks of 65,536 (CLEAN) or 32,768 values,
 // 256 streams per block dealt round-robin, fixed-length slots, uncompressed
 // overflow with a per-stream spill marker.
+//
+// Thread j of a block's CTA owns stream j.  The BF16 input streams through a
+// ring of row chunks filled by TMA bulk copies; each row's 256 values are
+// split, their sign-fraction bytes written straight out, and their exponents
+// appended to the streams' slot images in shared memory.  The last 64 rows
+// of exponents stay in shared memory for the spill; older spilled exponents
+// (a stream that spills more than 64 symbols) are read back from the input.
 #include "codec_dev.cuh"
 
 namespace lct {
 namespace dev {
 
+constexpr int kEncRows = 16;   // rows per input chunk
+constexpr int kEncRing = 3;    // chunks in flight
+constexpr int kSpillRows = 64; // exponent rows kept for the spill
+
+template <int LEVEL>
+struct EncodeSmem {
+    static constexpr int W = Geo<LEVEL>::W;
+    static constexpr int kIn = kEncRing * kEncRows * kStreams * 2;
+    static constexpr int kSlot = W * kStreams * 4;
+    static constexpr int kTbl = 256 * 8;
+    static constexpr int kSpill = (kSpillRows * kRow + 127) / 128 * 128;
+    static constexpr int kBytes = kIn + kSlot + kTbl + kSpill;
+};
+
 // Prologue (one launch per encode): CTA 0 estimates the shift and writes the
 // tensor header; every CTA zeroes its share of the look-back status words.
-// The block encoder is launched as a programmatic dependent and overlaps its
-// load/split phase with this kernel.
 __global__ void __launch_bounds__(256) k_encode_prologue(const uint16_t *__restrict__ x, DevTensor t,
                                                           int32_t median_exp, uint32_t cb_hash)
 {
-    pdl_launch_dependents();
+    pdl_wait();                // earlier work in the stream (e.g. what produced x) is done
+    pdl_launch_dependents();   // the block encoder may start its input loads now
     for (uint64_t i = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x; i < t.nblocks;
          i += (uint64_t)gridDim.x * blockDim.x)
         t.work[i] = 0ull;
@@ -26,25 +46,34 @@ __global__ void __launch_bounds__(256) k_encode_prologue(const uint16_t *__restr
 
     // Shift: m = min(n, 4096) samples at floor(k*n/m); histogram of their
     // exponents in the normal range 1..254; lower median.
+    constexpr int kPer = LCT_SHIFT_SAMPLES / 256;
     __shared__ uint32_t hist[256];
     __shared__ uint32_t wsum[8];
+    __shared__ int32_t median;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     hist[tid] = 0;
+    if (tid == 0) median = -1;
     __syncthreads();
     const uint64_t n = t.n;
     const uint32_t m = n < (uint64_t)LCT_SHIFT_SAMPLES ? (uint32_t)n : (uint32_t)LCT_SHIFT_SAMPLES;
-    for (uint32_t k = tid; k < m; k += 256) {
-        const uint8_t e = exp_of(x[((uint64_t)k * n) / m]);
-        if (e >= 1 && e <= 254) atomicAdd(&hist[e], 1u);
+    uint16_t v[kPer];
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) {  // all loads in flight at once
+        const uint32_t k = tid + 256u * i;
+        v[i] = k < m ? __ldg(x + ((uint64_t)k * n) / m) : 0;
+    }
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) {
+        const uint32_t e = exp_of(v[i]);
+        if (tid + 256u * i < m && e >= 1 && e <= 254) atomicAdd(&hist[e], 1u);
     }
     __syncthreads();
-    // inclusive scan of the 256 bins (one per thread)
     const uint32_t c = hist[tid];
     uint32_t inc = c;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-        const uint32_t v = __shfl_up_sync(0xFFFFFFFFu, inc, o);
-        if (lane >= o) inc += v;
+        const uint32_t u = __shfl_up_sync(kFull, inc, o);
+        if (lane >= o) inc += u;
     }
     if (lane == 31) wsum[warp] = inc;
     __syncthreads();
@@ -54,9 +83,6 @@ __global__ void __launch_bounds__(256) k_encode_prologue(const uint16_t *__restr
         kept += wsum[w];
     }
     inc += before;
-    __shared__ int32_t median;
-    if (tid == 0) median = -1;
-    __syncthreads();
     if (kept > 0) {
         const uint32_t rank = (kept - 1) / 2;  // lower median, 0-based
         if (inc > rank && inc - c <= rank) median = tid;
@@ -81,119 +107,143 @@ __global__ void __launch_bounds__(256) k_encode_prologue(const uint16_t *__restr
     }
 }
 
-// One CTA per block, one thread per stream.
 template <int LEVEL>
-__global__ void __launch_bounds__(256, 2) k_encode(const __grid_constant__ EncodeArgs a)
+__global__ void __launch_bounds__(256, 3) k_encode(const __grid_constant__ EncodeArgs a)
 {
     using G = Geo<LEVEL>;
-    extern __shared__ __align__(16) uint8_t smem[];
-    uint8_t *e_s = smem;
-    uint32_t *slot_s = reinterpret_cast<uint32_t *>(smem + Smem<LEVEL>::kExpBytes);
-    uint2 *tbl = reinterpret_cast<uint2 *>(smem + Smem<LEVEL>::kExpBytes + Smem<LEVEL>::kSlotBytes);
+    using L = EncodeSmem<LEVEL>;
+    constexpr int W = G::W, R = kEncRows, S = kEncRing, SP = kSpillRows;
+    extern __shared__ __align__(128) uint8_t smem[];
+    uint16_t *x_s = reinterpret_cast<uint16_t *>(smem);
+    uint32_t *slot_s = reinterpret_cast<uint32_t *>(smem + L::kIn);
+    uint2 *tbl = reinterpret_cast<uint2 *>(smem + L::kIn + L::kSlot);
+    uint8_t *ring = smem + L::kIn + L::kSlot + L::kTbl;
+    __shared__ __align__(8) uint64_t bar[S];
     __shared__ uint32_t warp_tot[8];
     __shared__ unsigned long long s_excl;
+    __shared__ uint32_t s_timeout;
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const uint32_t j = tid;
     const uint32_t b = blockIdx.x;
     const uint64_t base = (uint64_t)b * G::B;
     const uint32_t nb = (uint32_t)min((uint64_t)G::B, a.t.n - base);
+    const uint32_t nrows = (nb + 255) >> 8, nbulk = (nb >> 8) / R, nchunks = (nrows + R - 1) / R;
+    const uint64_t limit = a.wait_ns;
 
-    // ---- split: sign-fraction bytes straight out, exponents to shared rows
-    {
-        const uint4 *xv = reinterpret_cast<const uint4 *>(a.x + base);
-        uint2 *sfv = reinterpret_cast<uint2 *>(a.t.sf + base);
-        const uint32_t ng = nb >> 3;
-#pragma unroll 4
-        for (uint32_t g = tid; g < ng; g += 256) {
-            const uint4 v = __ldcs(xv + g);
-            uint2 sf, ex;
-            split8(v, sf, ex);
-            __stcs(sfv + g, sf);
-            uint32_t *dst = reinterpret_cast<uint32_t *>(stage_at(e_s, g << 3));
-            dst[0] = ex.x;
-            dst[1] = ex.y;
-        }
-        for (uint32_t i = (ng << 3) + tid; i < nb; i += 256) {
-            const uint16_t h = a.x[base + i];
-            a.t.sf[base + i] = sf_of(h);
-            *stage_at(e_s, i) = exp_of(h);
-        }
-    }
-
-    // ---- the shift and the cleared look-back words come from the prologue
-    pdl_wait();
-    const int delta = a.t.hdr->delta;
-    tbl[tid] = enc_entry(a.cb, delta, tid);
-    __syncthreads();
-
-    // ---- code stream `tid` into its slot
-    const uint32_t j = tid;
-    const uint32_t nj = nb > j ? (nb - j + 255) / 256 : 0;
-    uint32_t marker;
-    if (nb == (uint32_t)G::B)
-        marker = encode_stream<G::W, G::NJ>(e_s + j, nj, tbl, slot_s + j);
-    else
-        marker = encode_stream<G::W, 0>(e_s + j, nj, tbl, slot_s + j);
-    const uint32_t spill = nj - marker;
-    uint32_t total;
-    const uint32_t pre = group_exclusive_scan(spill, warp_tot, 8, 0, &total);  // syncs
-
-    // ---- slots and markers out (coalesced)
-    {
-        const uint4 *src = reinterpret_cast<const uint4 *>(slot_s);
-        uint4 *dst = reinterpret_cast<uint4 *>(a.t.slots + (uint64_t)b * G::W * kStreams);
-#pragma unroll 5
-        for (int w = tid; w < G::W * kStreams / 4; w += 256) __stcs(dst + w, src[w]);
-        a.t.markers[(uint64_t)b * kStreams + j] = (uint16_t)marker;
-    }
-
-    // ---- overflow offset of this block (single-pass look-back)
     if (tid == 0) {
-        bool timed_out;
-        const unsigned long long excl = lookback(a.t.work, b, total, a.wait_ns, &timed_out);
-        if (timed_out) latch(a.t.hdr, LCT_ERR_TIMEOUT);
-        a.t.blk_off[b] = excl;
-        if (b == a.t.nblocks - 1) {
-            a.t.blk_off[b + 1] = excl + total;
-            a.t.hdr->ovf_used = excl + total;
+        for (int s = 0; s < S; ++s) mbar_init(&bar[s], 1);
+        fence_mbar_init();
+        s_timeout = 0;
+        // The input was written before the prologue ran, so it can be read
+        // before waiting for the prologue.
+        for (uint32_t c = 0; c < (uint32_t)S && c < nbulk; ++c) {
+            mbar_expect_tx(&bar[c], R * kStreams * 2);
+            bulk_load(x_s + c * R * kStreams, a.x + base + (uint64_t)c * R * kStreams, R * kStreams * 2, &bar[c]);
         }
-        if (excl + total > a.t.ovf_cap) latch(a.t.hdr, LCT_ERR_OVERFLOW_CAPACITY);
-        s_excl = excl;
+    }
+    // the shift and the cleared look-back words come from the prologue
+    pdl_wait();
+    tbl[tid] = enc_entry(a.cb, a.t.hdr->delta, tid);
+    __syncthreads();
+
+    const uint32_t nj = nb > j ? (nb - j + 255) / 256 : 0;
+    BitWriter bw;
+    bw_init<W>(bw, nj);
+    uint32_t *col = slot_s + j;
+    uint8_t *sfj = a.t.sf + base + j;
+    uint8_t *ringj = ring + j;
+
+    for (uint32_t c = 0; c < nchunks; ++c) {
+        const bool bulk = c < nbulk;
+        const uint32_t slot = c % S;
+        if (bulk && !mbar_wait(&bar[slot], (c / S) & 1u, s_timeout ? 1000000ull : limit)) s_timeout = 1;
+        const uint16_t *xc = x_s + slot * R * kStreams + j;
+#pragma unroll 4
+        for (int r = 0; r < R; ++r) {
+            const uint32_t k = c * R + r;
+            if (bulk || k < nj) {
+                const uint32_t h = bulk ? xc[r * kStreams] : a.x[base + (uint64_t)k * kStreams + j];
+                const uint32_t e = exp_of(h);
+                sfj[(uint64_t)k * kStreams] = sf_of(h);
+                ringj[(k & (SP - 1)) * kRow] = (uint8_t)e;
+                bw_put(bw, tbl[e], k, col);
+            }
+        }
+        __syncthreads();  // every thread is done with this chunk's ring slot
+        if (tid == 0 && c + S < nbulk) {
+            mbar_expect_tx(&bar[slot], R * kStreams * 2);
+            bulk_load(x_s + slot * R * kStreams, a.x + base + (uint64_t)(c + S) * R * kStreams, R * kStreams * 2,
+                      &bar[slot]);
+        }
+    }
+    bw_finish<W>(bw, col);
+    const uint32_t marker = bw.marker, spill = nj - marker;
+    uint32_t total;
+    const uint32_t pre = group_exclusive_scan(spill, warp_tot, 8, 0, &total);  // syncs: slot image complete
+
+    if (tid == 0) {
+        fence_proxy_async();
+        bulk_store(a.t.slots + (uint64_t)b * W * kStreams, slot_s, W * kStreams * 4);
+        bulk_commit();
+    }
+    a.t.markers[(uint64_t)b * kStreams + j] = (uint16_t)marker;
+
+    // overflow offset of this block (single-pass decoupled look-back)
+    if (warp == 0) {
+        bool timed_out;
+        const unsigned long long excl = warp_lookback(a.t.work, b, total, limit, &timed_out);
+        if (lane == 0) {
+            if (timed_out) latch(a.t.hdr, LCT_ERR_TIMEOUT);
+            a.t.blk_off[b] = excl;
+            if (b == a.t.nblocks - 1) {
+                a.t.blk_off[b + 1] = excl + total;
+                a.t.hdr->ovf_used = excl + total;
+            }
+            if (excl + total > a.t.ovf_cap) latch(a.t.hdr, LCT_ERR_OVERFLOW_CAPACITY);
+            s_excl = excl;
+        }
     }
     __syncthreads();
 
-    // ---- spilled exponents, raw, in (stream, symbol) order: one warp per
-    //      stream at a time, lanes over the stream's spilled symbols
+    // spilled exponents, raw, in (stream, symbol) order: one warp per stream
+    // at a time, lanes over the stream's spilled symbols
     const unsigned long long excl = s_excl;
     if (total > 0 && excl + total <= a.t.ovf_cap) {
         uint8_t *out = a.t.ovf + excl;
+        const uint32_t kept_from = nrows > (uint32_t)SP ? nrows - SP : 0u;  // rows still in the ring
         for (int i = 0; i < 32; ++i) {
-            const uint32_t sm = __shfl_sync(0xFFFFFFFFu, marker, i);
-            const uint32_t sp = __shfl_sync(0xFFFFFFFFu, spill, i);
-            const uint32_t so = __shfl_sync(0xFFFFFFFFu, pre, i);
+            const uint32_t sm = __shfl_sync(kFull, marker, i);
+            const uint32_t sp = __shfl_sync(kFull, spill, i);
+            const uint32_t so = __shfl_sync(kFull, pre, i);
             const uint32_t sj = (uint32_t)(warp * 32 + i);
-            for (uint32_t l = lane; l < sp; l += 32) out[so + l] = e_s[(sm + l) * kRow + sj];
+            for (uint32_t l = lane; l < sp; l += 32) {
+                const uint32_t k = sm + l;
+                out[so + l] = k >= kept_from ? ring[(k & (SP - 1)) * kRow + sj]
+                                             : exp_of(a.x[base + (uint64_t)k * kStreams + sj]);
+            }
         }
+    }
+    pdl_launch_dependents();
+    if (tid == 0) {
+        if (s_timeout) {
+            latch(a.t.hdr, LCT_ERR_TIMEOUT);
+            for (uint32_t s = 0; s < (uint32_t)S && s < nbulk; ++s) {
+                const uint32_t last = s + (nbulk - 1 - s) / S * S;
+                mbar_wait(&bar[s], (last / S) & 1u, limit);
+            }
+        }
+        bulk_wait_all();  // the slot image store has read shared memory
     }
 }
 
 template <int LEVEL>
 cudaError_t launch_level(const EncodeArgs &a, cudaStream_t s)
 {
-    constexpr int smem = Smem<LEVEL>::kExpBytes + Smem<LEVEL>::kSlotBytes + 256 * 8;
+    constexpr int smem = EncodeSmem<LEVEL>::kBytes;
     cudaError_t err = cudaFuncSetAttribute(k_encode<LEVEL>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (err != cudaSuccess) return err;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(a.t.nblocks);
-    cfg.blockDim = dim3(256);
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = s;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, k_encode<LEVEL>, a);
+    return launch_pdl(k_encode<LEVEL>, dim3(a.t.nblocks), dim3(256), smem, s, a);
 }
 
 }  // namespace dev
@@ -201,8 +251,8 @@ cudaError_t launch_level(const EncodeArgs &a, cudaStream_t s)
 cudaError_t launch_encode(const EncodeArgs &a, cudaStream_t s)
 {
     const uint32_t zero_ctas = 1 + a.t.nblocks / 8192;
-    dev::k_encode_prologue<<<zero_ctas < 64 ? zero_ctas : 64, 256, 0, s>>>(a.x, a.t, a.median_exp, a.cb.hash);
-    cudaError_t err = cudaGetLastError();
+    cudaError_t err = dev::launch_pdl(dev::k_encode_prologue, dim3(zero_ctas < 64 ? zero_ctas : 64), dim3(256), 0, s,
+                                      a.x, a.t, a.median_exp, a.cb.hash);
     if (err != cudaSuccess || a.t.nblocks == 0) return err;
     switch (a.t.level) {
     case LCT_LEVEL_CLEAN: return dev::launch_level<LCT_LEVEL_CLEAN>(a, s);

@@ -74,13 +74,14 @@ struct DecodeArgs {
     DevTensor t;
     uint16_t *y;
     DevCodebook cb;
+    uint64_t wait_ns;
 };
 
 struct SgdArgs {
     DevTensor w_in, m, w_out;
     DevCodebook cbw, cbm;
     float eta;
-    uint32_t pad;
+    uint32_t in_place;  // W_out's sign-fraction bytes are W_in's
     uint64_t wait_ns;
 };
 

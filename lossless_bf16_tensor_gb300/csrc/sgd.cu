@@ -4,10 +4,22 @@
 // updating, and re-encoding (three round trips), one kernel reads the
 // compressed inputs, does the arithmetic, and writes the new sign-fraction
 // bytes and the re-coded exponents in a single pass over each block.
+//
+// Thread j of a block's CTA owns stream j of W, of M and of the new W: per
+// row it decodes one symbol of W and of M, updates the value, writes the new
+// sign-fraction byte and appends the new exponent to its slot.  The slot
+// images of W and M come in by TMA bulk copy, the sign-fraction bytes stream
+// through a ring of row chunks.  New exponents are kept for the last 64 rows
+// (all rows when W is updated in place); an out-of-place step that spills
+// more than that re-decodes the older rows of that stream at the end.
 #include "codec_dev.cuh"
 
 namespace lct {
 namespace dev {
+
+constexpr int kSgdRows = 8;   // rows per sign-fraction chunk
+constexpr int kSgdRing = 3;   // chunks in flight
+constexpr int kSgdSpill = 64; // new-exponent rows kept (out of place)
 
 // float32 -> BF16, round to nearest even; subnormals kept; NaN -> 0x7FC0.
 __device__ __forceinline__ uint32_t bf16_rne(float r)
@@ -17,28 +29,31 @@ __device__ __forceinline__ uint32_t bf16_rne(float r)
     return (u + 0x7FFFu + ((u >> 16) & 1u)) >> 16;
 }
 
-// Two BF16 (one word) of W and M -> two updated BF16 (one word).
-__device__ __forceinline__ uint32_t sgd2(uint32_t w2, uint32_t m2, float eta)
+// One value: fl32(w - fl32(eta*m)) (two roundings, never contracted), to BF16.
+__device__ __forceinline__ uint32_t sgd1(uint32_t w, uint32_t m, float eta)
 {
-    const float w0 = __uint_as_float(w2 << 16), w1 = __uint_as_float(w2 & 0xFFFF0000u);
-    const float m0 = __uint_as_float(m2 << 16), m1 = __uint_as_float(m2 & 0xFFFF0000u);
-    const uint32_t r0 = bf16_rne(__fsub_rn(w0, __fmul_rn(eta, m0)));
-    const uint32_t r1 = bf16_rne(__fsub_rn(w1, __fmul_rn(eta, m1)));
-    return r0 | (r1 << 16);
+    return bf16_rne(__fsub_rn(__uint_as_float(w << 16), __fmul_rn(eta, __uint_as_float(m << 16))));
 }
 
-__device__ __forceinline__ uint16_t sgd1(uint16_t w, uint16_t m, float eta)
-{
-    const float wf = __uint_as_float((uint32_t)w << 16), mf = __uint_as_float((uint32_t)m << 16);
-    return (uint16_t)bf16_rne(__fsub_rn(wf, __fmul_rn(eta, mf)));
-}
+template <int LEVEL, bool INPLACE>
+struct SgdSmem {
+    static constexpr int W = Geo<LEVEL>::W, NJ = Geo<LEVEL>::NJ;
+    static constexpr int kSpillRows = INPLACE ? NJ : kSgdSpill;
+    static constexpr int kSlotIn = (W + 1) * kStreams * 4;  // + zero guard row
+    static constexpr int kSlotOut = W * kStreams * 4;
+    static constexpr int kRing = kSgdRing * kSgdRows * kStreams;  // per input
+    static constexpr int kLuts = 2 * 256 * 4 + 256 * 8;
+    static constexpr int kSpill = (kSpillRows * kRow + 127) / 128 * 128;
+    static constexpr int kBytes = 2 * kSlotIn + kSlotOut + 2 * kRing + kLuts + kSpill;
+};
 
 // Prologue: the new W's header (shift and codebook carried over, status
-// cleared, but inheriting an error already latched in W or M) and cleared
-// look-back words.
+// cleared but inheriting an error already latched in W or M, or CORRUPT if
+// either header is not valid) and cleared look-back words.
 __global__ void __launch_bounds__(256) k_sgd_prologue(DevTensor w_in, DevTensor m, DevTensor w_out,
                                                        uint32_t hash_w, uint32_t hash_m)
 {
+    pdl_wait();
     pdl_launch_dependents();
     for (uint64_t i = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x; i < w_out.nblocks;
          i += (uint64_t)gridDim.x * blockDim.x)
@@ -64,178 +79,251 @@ __global__ void __launch_bounds__(256) k_sgd_prologue(DevTensor w_in, DevTensor 
     }
 }
 
-// One CTA (512 threads) per block: threads 0..255 decode W's streams while
-// 256..511 decode M's; all 512 update the values; threads 0..255 re-code.
-template <int LEVEL>
-__global__ void __launch_bounds__(512, 1) k_sgd(const __grid_constant__ SgdArgs a)
+// Per-stream view of one compressed input (W or M) inside the kernel.
+struct InStream {
+    BitReader rd;
+    const uint32_t *col;     // slot image column in shared memory
+    const uint32_t *lut;     // decode table in shared memory
+    uint32_t marker;
+    uint64_t ovf_at;         // overflow index of symbol k is ovf_at + k
+    const uint8_t *ovf;
+    bool ovf_ok;
+};
+
+template <int W>
+__device__ __forceinline__ uint32_t in_symbol(InStream &s, uint32_t k)
+{
+    if (k < s.marker) return br_symbol(s.rd, s.lut);
+    return s.ovf_ok ? (uint32_t)__ldg(s.ovf + s.ovf_at + k) << 7 : 0u;
+}
+
+template <int LEVEL, bool INPLACE>
+__global__ void __launch_bounds__(256, 2) k_sgd(const __grid_constant__ SgdArgs a)
 {
     using G = Geo<LEVEL>;
-    constexpr int EB = Smem<LEVEL>::kExpBytes, SB = Smem<LEVEL>::kSlotBytes;
-    extern __shared__ __align__(16) uint8_t smem[];
-    uint8_t *eW = smem;
-    uint8_t *eM = smem + EB;
-    uint32_t *slotW = reinterpret_cast<uint32_t *>(smem + 2 * EB);
-    uint32_t *slotM = reinterpret_cast<uint32_t *>(smem + 2 * EB + SB);
-    uint32_t *lutW = reinterpret_cast<uint32_t *>(smem + 2 * EB + 2 * SB);
+    using L = SgdSmem<LEVEL, INPLACE>;
+    constexpr int W = G::W, R = kSgdRows, S = kSgdRing, SP = L::kSpillRows;
+    extern __shared__ __align__(128) uint8_t smem[];
+    uint32_t *slotW = reinterpret_cast<uint32_t *>(smem);
+    uint32_t *slotM = reinterpret_cast<uint32_t *>(smem + L::kSlotIn);
+    uint32_t *slotO = reinterpret_cast<uint32_t *>(smem + 2 * L::kSlotIn);
+    uint8_t *sfW_s = smem + 2 * L::kSlotIn + L::kSlotOut;
+    uint8_t *sfM_s = sfW_s + L::kRing;
+    uint32_t *lutW = reinterpret_cast<uint32_t *>(sfM_s + L::kRing);
     uint32_t *lutM = lutW + 256;
     uint2 *tbl = reinterpret_cast<uint2 *>(lutM + 256);
-    __shared__ uint32_t warp_tot[16];
-    __shared__ uint32_t s_err;
+    uint8_t *ring = reinterpret_cast<uint8_t *>(tbl + 256);
+    __shared__ __align__(8) uint64_t bar_slot, bar_sf[S];
+    __shared__ uint32_t warp_tot[8];
     __shared__ unsigned long long s_excl;
+    __shared__ uint32_t s_flags;  // bit 0: a wait gave up, bit 1: corrupt input
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int half = tid >> 8;  // 0: W, 1: M
-    const uint32_t j = tid & 255;
+    const uint32_t j = tid;
     const uint32_t b = blockIdx.x;
     const uint64_t base = (uint64_t)b * G::B;
     const uint32_t nb = (uint32_t)min((uint64_t)G::B, a.w_in.n - base);
-    const DevTensor &src = half ? a.m : a.w_in;
-    const DevCodebook &cb = half ? a.cbm : a.cbw;
-    uint8_t *e_s = half ? eM : eW;
-    uint32_t *slot_s = half ? slotM : slotW;
-    uint32_t *lut = half ? lutM : lutW;
+    const uint32_t nrows = (nb + 255) >> 8, nbulk = (nb >> 8) / R, nchunks = (nrows + R - 1) / R;
+    const uint64_t limit = a.wait_ns;
 
-    if (tid == 0) s_err = 0;
-    const lct_header *hs = src.hdr;
-    const bool hdr_ok = hs->magic == LCT_MAGIC && hs->n == src.n && hs->level == LEVEL && hs->cb_hash == cb.hash;
-    const int delta = hs->delta;
-    const int delta_w = a.w_in.hdr->delta;
-    lut[j] = dec_entry(cb, delta, (int)j);
-    if (half == 0) tbl[j] = enc_entry(a.cbw, delta_w, (int)j);
-    {
-        const uint4 *sv = reinterpret_cast<const uint4 *>(src.slots + (uint64_t)b * G::W * kStreams);
-        uint4 *dv = reinterpret_cast<uint4 *>(slot_s);
-#pragma unroll 5
-        for (int w = j; w < G::W * kStreams / 4; w += 256) dv[w] = __ldcs(sv + w);
-        slot_s[G::W * kStreams + j] = 0u;
-    }
-    const uint32_t nj = nb > j ? (nb - j + 255) / 256 : 0;
-    uint32_t marker = src.markers[(uint64_t)b * kStreams + j];
-    bool bad = !hdr_ok || marker > nj;
-    marker = min(marker, nj);
-    uint32_t spill = nj - marker;
-    uint32_t total;
-    uint32_t pre = group_exclusive_scan(spill, warp_tot, 8, half * 8, &total);  // syncs
-    const uint64_t off0 = src.blk_off[b], off1 = src.blk_off[b + 1];
-    const bool ovf_ok = off1 <= src.ovf_cap && off0 <= off1 && off1 - off0 == total;
-    bad |= !ovf_ok;
-
-    // ---- decode W (half 0) and M (half 1) side by side
-    const uint32_t bits = decode_stream<G::W>(slot_s + j, marker, lut, e_s + j);
-    bad |= bits > 32u * G::W;
-    if (bad) atomicCAS(&s_err, 0u, (uint32_t)LCT_ERR_CORRUPT);
-    if (total > 0 && ovf_ok) {
-        const uint8_t *in = src.ovf + off0;
-        for (int i = 0; i < 32; ++i) {
-            const uint32_t sm = __shfl_sync(0xFFFFFFFFu, marker, i);
-            const uint32_t sp = __shfl_sync(0xFFFFFFFFu, spill, i);
-            const uint32_t so = __shfl_sync(0xFFFFFFFFu, pre, i);
-            const uint32_t sj = (uint32_t)((warp & 7) * 32 + i);
-            for (uint32_t l = lane; l < sp; l += 32) e_s[(sm + l) * kRow + sj] = __ldg(in + so + l);
-        }
-    }
-    __syncthreads();
-
-    // ---- update, 8 values per step: new sign-fraction bytes out, new
-    //      exponents back into W's staging rows
-    {
-        const uint2 *sfw = reinterpret_cast<const uint2 *>(a.w_in.sf + base);
-        const uint2 *sfm = reinterpret_cast<const uint2 *>(a.m.sf + base);
-        uint2 *sfo = reinterpret_cast<uint2 *>(a.w_out.sf + base);
-        const uint32_t ng = nb >> 3;
-        const float eta = a.eta;
-#pragma unroll 2
-        for (uint32_t g = tid; g < ng; g += 512) {
-            const uint2 sw = __ldcs(sfw + g), sm = __ldcs(sfm + g);
-            uint32_t *ew = reinterpret_cast<uint32_t *>(stage_at(eW, g << 3));
-            const uint32_t *em = reinterpret_cast<const uint32_t *>(stage_at(eM, g << 3));
-            const uint4 vw = join8(sw, make_uint2(ew[0], ew[1]));
-            const uint4 vm = join8(sm, make_uint2(em[0], em[1]));
-            uint4 r;
-            r.x = sgd2(vw.x, vm.x, eta);
-            r.y = sgd2(vw.y, vm.y, eta);
-            r.z = sgd2(vw.z, vm.z, eta);
-            r.w = sgd2(vw.w, vm.w, eta);
-            uint2 sf, ex;
-            split8(r, sf, ex);
-            __stcs(sfo + g, sf);
-            ew[0] = ex.x;
-            ew[1] = ex.y;
-        }
-        for (uint32_t i = (ng << 3) + tid; i < nb; i += 512) {
-            const uint16_t w = join1(a.w_in.sf[base + i], *stage_at(eW, i));
-            const uint16_t m = join1(a.m.sf[base + i], *stage_at(eM, i));
-            const uint16_t r = sgd1(w, m, eta);
-            a.w_out.sf[base + i] = sf_of(r);
-            *stage_at(eW, i) = exp_of(r);
-        }
-    }
-    __syncthreads();
-
-    // ---- re-code W with its codebook and its stored shift
-    uint32_t new_marker = 0, new_spill = 0;
-    if (half == 0) {
-        if (nb == (uint32_t)G::B)
-            new_marker = encode_stream<G::W, G::NJ>(eW + j, nj, tbl, slotW + j);
-        else
-            new_marker = encode_stream<G::W, 0>(eW + j, nj, tbl, slotW + j);
-        new_spill = nj - new_marker;
-    }
-    uint32_t new_total;
-    const uint32_t new_pre = group_exclusive_scan(new_spill, warp_tot, 8, 0, &new_total);  // syncs
-    {
-        const uint4 *sv = reinterpret_cast<const uint4 *>(slotW);
-        uint4 *dv = reinterpret_cast<uint4 *>(a.w_out.slots + (uint64_t)b * G::W * kStreams);
-        for (int w = tid; w < G::W * kStreams / 4; w += 512) __stcs(dv + w, sv[w]);
-        if (half == 0) a.w_out.markers[(uint64_t)b * kStreams + j] = (uint16_t)new_marker;
-    }
-
-    // ---- the prologue has cleared W_out's header and look-back words
-    pdl_wait();
     if (tid == 0) {
-        if (s_err) latch(a.w_out.hdr, s_err);
-        bool timed_out;
-        const unsigned long long excl = lookback(a.w_out.work, b, new_total, a.wait_ns, &timed_out);
-        if (timed_out) latch(a.w_out.hdr, LCT_ERR_TIMEOUT);
-        a.w_out.blk_off[b] = excl;
-        if (b == a.w_out.nblocks - 1) {
-            a.w_out.blk_off[b + 1] = excl + new_total;
-            a.w_out.hdr->ovf_used = excl + new_total;
+        mbar_init(&bar_slot, 1);
+        for (int s = 0; s < S; ++s) mbar_init(&bar_sf[s], 1);
+        fence_mbar_init();
+        s_flags = 0;
+    }
+    // inputs, the new header and the cleared look-back words are all ready
+    pdl_wait();
+    const lct_header *hw = a.w_in.hdr, *hm = a.m.hdr;
+    bool bad = !(hw->magic == LCT_MAGIC && hw->n == a.w_in.n && hw->level == LEVEL && hw->cb_hash == a.cbw.hash) ||
+               !(hm->magic == LCT_MAGIC && hm->n == a.m.n && hm->level == LEVEL && hm->cb_hash == a.cbm.hash);
+    const int delta_w = a.w_out.hdr->delta;  // the prologue copied W's shift
+    const int delta_m = hm->delta;
+    lutW[tid] = dec_entry(a.cbw, delta_w, tid);
+    lutM[tid] = dec_entry(a.cbm, delta_m, tid);
+    tbl[tid] = enc_entry(a.cbw, delta_w, tid);
+    slotW[W * kStreams + tid] = 0u;
+    slotM[W * kStreams + tid] = 0u;
+    __syncthreads();  // barriers initialised
+    if (tid == 0) {
+        mbar_expect_tx(&bar_slot, 2 * W * kStreams * 4);
+        bulk_load(slotW, a.w_in.slots + (uint64_t)b * W * kStreams, W * kStreams * 4, &bar_slot);
+        bulk_load(slotM, a.m.slots + (uint64_t)b * W * kStreams, W * kStreams * 4, &bar_slot);
+        for (uint32_t c = 0; c < (uint32_t)S && c < nbulk; ++c) {
+            mbar_expect_tx(&bar_sf[c], 2 * R * kStreams);
+            bulk_load(sfW_s + c * R * kStreams, a.w_in.sf + base + (uint64_t)c * R * kStreams, R * kStreams, &bar_sf[c]);
+            bulk_load(sfM_s + c * R * kStreams, a.m.sf + base + (uint64_t)c * R * kStreams, R * kStreams, &bar_sf[c]);
         }
-        if (excl + new_total > a.w_out.ovf_cap) latch(a.w_out.hdr, LCT_ERR_OVERFLOW_CAPACITY);
-        s_excl = excl;
+    }
+
+    // input markers, spill prefixes and overflow ranges
+    const uint32_t nj = nb > j ? (nb - j + 255) / 256 : 0;
+    InStream sw, sm;
+    sw.col = slotW + j;
+    sm.col = slotM + j;
+    sw.lut = lutW;
+    sm.lut = lutM;
+    sw.ovf = a.w_in.ovf;
+    sm.ovf = a.m.ovf;
+    uint32_t mk_w = a.w_in.markers[(uint64_t)b * kStreams + j], mk_m = a.m.markers[(uint64_t)b * kStreams + j];
+    bad |= mk_w > nj || mk_m > nj;
+    sw.marker = min(mk_w, nj);
+    sm.marker = min(mk_m, nj);
+    {
+        uint32_t tot_w, tot_m;
+        const uint32_t pre_w = group_exclusive_scan(nj - sw.marker, warp_tot, 8, 0, &tot_w);
+        const uint32_t pre_m = group_exclusive_scan(nj - sm.marker, warp_tot, 8, 0, &tot_m);
+        const uint64_t w0 = a.w_in.blk_off[b], w1 = a.w_in.blk_off[b + 1];
+        const uint64_t m0 = a.m.blk_off[b], m1 = a.m.blk_off[b + 1];
+        sw.ovf_ok = w1 <= a.w_in.ovf_cap && w0 <= w1 && w1 - w0 == tot_w;
+        sm.ovf_ok = m1 <= a.m.ovf_cap && m0 <= m1 && m1 - m0 == tot_m;
+        sw.ovf_at = w0 + pre_w - sw.marker;
+        sm.ovf_at = m0 + pre_m - sm.marker;
+        bad |= !sw.ovf_ok || !sm.ovf_ok;
+    }
+
+    if (!mbar_wait(&bar_slot, 0, limit)) s_flags = 1;
+    br_init<W>(sw.rd, sw.col);
+    br_init<W>(sm.rd, sm.col);
+    BitWriter bw;
+    bw_init<W>(bw, nj);
+    uint32_t *colO = slotO + j;
+    uint8_t *sfo = a.w_out.sf + base + j;
+    uint8_t *ringj = ring + j;
+    const float eta = a.eta;
+
+    for (uint32_t c = 0; c < nchunks; ++c) {
+        const bool bulk = c < nbulk;
+        const uint32_t slot = c % S;
+        if (bulk && !mbar_wait(&bar_sf[slot], (c / S) & 1u, (s_flags & 1u) ? 1000000ull : limit)) s_flags = 1;
+        const uint8_t *sfwc = sfW_s + slot * R * kStreams + j;
+        const uint8_t *sfmc = sfM_s + slot * R * kStreams + j;
+#pragma unroll
+        for (int r = 0; r < R; r += 2) {
+            br_refill<W>(sw.rd, sw.col);
+            br_refill<W>(sm.rd, sm.col);
+#pragma unroll
+            for (int q = 0; q < 2; ++q) {
+                const uint32_t k = c * R + r + q;
+                if (bulk || k < nj) {
+                    const uint32_t ew7 = in_symbol<W>(sw, k), em7 = in_symbol<W>(sm, k);
+                    uint32_t fw, fm;
+                    if (bulk) {
+                        fw = sfwc[(r + q) * kStreams];
+                        fm = sfmc[(r + q) * kStreams];
+                    } else {
+                        fw = a.w_in.sf[base + (uint64_t)k * kStreams + j];
+                        fm = a.m.sf[base + (uint64_t)k * kStreams + j];
+                    }
+                    const uint32_t h = sgd1(join_e7(fw, ew7), join_e7(fm, em7), eta);
+                    const uint32_t e = exp_of(h);
+                    sfo[(uint64_t)k * kStreams] = sf_of(h);
+                    ringj[(k % SP) * kRow] = (uint8_t)e;
+                    bw_put(bw, tbl[e], k, colO);
+                }
+            }
+        }
+        __syncthreads();  // every thread is done with this chunk's ring slot
+        if (tid == 0 && c + S < nbulk) {
+            mbar_expect_tx(&bar_sf[slot], 2 * R * kStreams);
+            bulk_load(sfW_s + slot * R * kStreams, a.w_in.sf + base + (uint64_t)(c + S) * R * kStreams, R * kStreams,
+                      &bar_sf[slot]);
+            bulk_load(sfM_s + slot * R * kStreams, a.m.sf + base + (uint64_t)(c + S) * R * kStreams, R * kStreams,
+                      &bar_sf[slot]);
+        }
+    }
+    bad |= br_consumed(sw.rd) > 32u * W || br_consumed(sm.rd) > 32u * W;
+    if (bad) atomicOr(&s_flags, 2u);
+    bw_finish<W>(bw, colO);
+    const uint32_t marker = bw.marker, spill = nj - marker;
+    uint32_t total;
+    const uint32_t pre = group_exclusive_scan(spill, warp_tot, 8, 0, &total);  // syncs: slot image complete
+
+    if (tid == 0) {
+        fence_proxy_async();
+        bulk_store(a.w_out.slots + (uint64_t)b * W * kStreams, slotO, W * kStreams * 4);
+        bulk_commit();
+    }
+    a.w_out.markers[(uint64_t)b * kStreams + j] = (uint16_t)marker;
+
+    if (warp == 0) {
+        bool timed_out;
+        const unsigned long long excl = warp_lookback(a.w_out.work, b, total, limit, &timed_out);
+        if (lane == 0) {
+            if (s_flags & 2u) latch(a.w_out.hdr, LCT_ERR_CORRUPT);
+            if (timed_out || (s_flags & 1u)) latch(a.w_out.hdr, LCT_ERR_TIMEOUT);
+            a.w_out.blk_off[b] = excl;
+            if (b == a.w_out.nblocks - 1) {
+                a.w_out.blk_off[b + 1] = excl + total;
+                a.w_out.hdr->ovf_used = excl + total;
+            }
+            if (excl + total > a.w_out.ovf_cap) latch(a.w_out.hdr, LCT_ERR_OVERFLOW_CAPACITY);
+            s_excl = excl;
+        }
     }
     __syncthreads();
+
     const unsigned long long excl = s_excl;
-    if (half == 0 && new_total > 0 && excl + new_total <= a.w_out.ovf_cap) {
+    if (total > 0 && excl + total <= a.w_out.ovf_cap) {
         uint8_t *out = a.w_out.ovf + excl;
+        const uint32_t kept_from = nrows > (uint32_t)SP ? nrows - SP : 0u;
+        // rows still kept in shared memory: one warp per stream at a time
         for (int i = 0; i < 32; ++i) {
-            const uint32_t sm = __shfl_sync(0xFFFFFFFFu, new_marker, i);
-            const uint32_t sp = __shfl_sync(0xFFFFFFFFu, new_spill, i);
-            const uint32_t so = __shfl_sync(0xFFFFFFFFu, new_pre, i);
+            const uint32_t smk = __shfl_sync(kFull, marker, i);
+            const uint32_t ssp = __shfl_sync(kFull, spill, i);
+            const uint32_t spr = __shfl_sync(kFull, pre, i);
             const uint32_t sj = (uint32_t)(warp * 32 + i);
-            for (uint32_t l = lane; l < sp; l += 32) out[so + l] = eW[(sm + l) * kRow + sj];
+            for (uint32_t l = lane; l < ssp; l += 32) {
+                const uint32_t k = smk + l;
+                if (k >= kept_from) out[spr + l] = ring[(k % SP) * kRow + sj];
+            }
         }
+        if (!INPLACE && marker < kept_from) {
+            // This stream spilled past the kept rows: decode its W and M again
+            // from the slot images (still in shared memory) and recompute the
+            // older spilled exponents.  W's sign-fraction bytes are intact
+            // because the step is out of place.
+            InStream rw = sw, rm = sm;
+            br_init<W>(rw.rd, rw.col);
+            br_init<W>(rm.rd, rm.col);
+            for (uint32_t k = 0; k < kept_from; k += 2) {
+                br_refill<W>(rw.rd, rw.col);
+                br_refill<W>(rm.rd, rm.col);
+                for (uint32_t q = 0; q < 2 && k + q < kept_from; ++q) {
+                    const uint32_t kk = k + q;
+                    const uint32_t ew7 = in_symbol<W>(rw, kk), em7 = in_symbol<W>(rm, kk);
+                    const uint64_t at = base + (uint64_t)kk * kStreams + j;
+                    const uint32_t h = sgd1(join_e7(a.w_in.sf[at], ew7), join_e7(a.m.sf[at], em7), eta);
+                    if (kk >= marker) out[pre + (kk - marker)] = exp_of(h);
+                }
+            }
+        }
+    }
+    pdl_launch_dependents();
+    if (tid == 0) {
+        if (s_flags & 1u) {
+            for (uint32_t s = 0; s < (uint32_t)S && s < nbulk; ++s) {
+                const uint32_t last = s + (nbulk - 1 - s) / S * S;
+                mbar_wait(&bar_sf[s], (last / S) & 1u, limit);
+            }
+        }
+        bulk_wait_all();  // the slot image store has read shared memory
     }
 }
 
-template <int LEVEL>
+template <int LEVEL, bool INPLACE>
 cudaError_t launch_level(const SgdArgs &a, cudaStream_t s)
 {
-    constexpr int smem = 2 * Smem<LEVEL>::kExpBytes + 2 * Smem<LEVEL>::kSlotBytes + 2 * 256 * 4 + 256 * 8;
-    cudaError_t err = cudaFuncSetAttribute(k_sgd<LEVEL>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    constexpr int smem = SgdSmem<LEVEL, INPLACE>::kBytes;
+    cudaError_t err = cudaFuncSetAttribute(k_sgd<LEVEL, INPLACE>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (err != cudaSuccess) return err;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(a.w_out.nblocks);
-    cfg.blockDim = dim3(512);
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = s;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, k_sgd<LEVEL>, a);
+    return launch_pdl(k_sgd<LEVEL, INPLACE>, dim3(a.w_out.nblocks), dim3(256), smem, s, a);
+}
+
+template <int LEVEL>
+cudaError_t launch_sgd_level(const SgdArgs &a, cudaStream_t s)
+{
+    return a.in_place ? launch_level<LEVEL, true>(a, s) : launch_level<LEVEL, false>(a, s);
 }
 
 }  // namespace dev
@@ -243,13 +331,13 @@ cudaError_t launch_level(const SgdArgs &a, cudaStream_t s)
 cudaError_t launch_sgd(const SgdArgs &a, cudaStream_t s)
 {
     const uint32_t zero_ctas = 1 + a.w_out.nblocks / 8192;
-    dev::k_sgd_prologue<<<zero_ctas < 64 ? zero_ctas : 64, 256, 0, s>>>(a.w_in, a.m, a.w_out, a.cbw.hash, a.cbm.hash);
-    cudaError_t err = cudaGetLastError();
+    cudaError_t err = dev::launch_pdl(dev::k_sgd_prologue, dim3(zero_ctas < 64 ? zero_ctas : 64), dim3(256), 0, s,
+                                      a.w_in, a.m, a.w_out, a.cbw.hash, a.cbm.hash);
     if (err != cudaSuccess || a.w_out.nblocks == 0) return err;
     switch (a.w_out.level) {
-    case LCT_LEVEL_CLEAN: return dev::launch_level<LCT_LEVEL_CLEAN>(a, s);
-    case LCT_LEVEL_MEDIUM: return dev::launch_level<LCT_LEVEL_MEDIUM>(a, s);
-    default: return dev::launch_level<LCT_LEVEL_HIGH>(a, s);
+    case LCT_LEVEL_CLEAN: return dev::launch_sgd_level<LCT_LEVEL_CLEAN>(a, s);
+    case LCT_LEVEL_MEDIUM: return dev::launch_sgd_level<LCT_LEVEL_MEDIUM>(a, s);
+    default: return dev::launch_sgd_level<LCT_LEVEL_HIGH>(a, s);
     }
 }
 

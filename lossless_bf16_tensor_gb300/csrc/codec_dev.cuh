@@ -50,10 +50,6 @@ __device__ __forceinline__ uint64_t global_ns()
 __device__ __forceinline__ uint8_t exp_of(uint32_t h) { return (uint8_t)((h >> 7) & 0xFF); }
 __device__ __forceinline__ uint8_t sf_of(uint32_t h) { return (uint8_t)(((h >> 8) & 0x80) | (h & 0x7F)); }
 
-// BF16 from a sign-fraction byte and an exponent already shifted to bits
-// 7..14: sf * 0x101 puts the sign at bit 15 and keeps the fraction in bits 0..6.
-__device__ __forceinline__ uint32_t join_e7(uint32_t sf, uint32_t e7) { return ((sf * 0x101u) & 0x807Fu) | e7; }
-
 // --------------------------------------------------------- code tables
 
 // Encode table for shift delta: entry e = {code left-aligned in 32 bits, bit
@@ -76,75 +72,73 @@ __device__ __forceinline__ uint2 enc_entry(const DevCodebook &cb, int delta, int
 // Decode table for shift delta, indexed by the next 8 bits of the stream:
 //   bits  7..14  the exponent, for a symbol with its own code (0 for escape)
 //   bits 16..23  bits consumed (code length, or escape length + 8)
-//   bits 24..31  for the escape: its length (the literal follows it);
-//                otherwise 32, which shifts the literal out entirely
+//   bits 24..27  escape length (escape only)
+//   bit  31      escape: the exponent is the 8-bit literal after the prefix
+// Bits 0..15 of an entry are therefore the exponent already in place in a
+// BF16 word (bits 7..14), ready to be OR-ed with the sign and fraction.
+constexpr uint32_t kEsc = 0x80000000u;
+
 __device__ __forceinline__ uint32_t dec_entry(const DevCodebook &cb, int delta, int v)
 {
     const uint32_t d = cb.dec[v], sym = d & 0x1FF, l = d >> 12;
-    if (sym == 256) return (l << 24) | ((l + 8u) << 16);
-    return (32u << 24) | (l << 16) | (((sym + (uint32_t)delta) & 0xFFu) << 7);
+    if (sym == 256) return kEsc | (l << 24) | ((l + 8u) << 16);
+    return (l << 16) | (((sym + (uint32_t)delta) & 0xFFu) << 7);
 }
 
 // ------------------------------------------------------ stream decoding
 
-// Reads one stream's slot, most significant bit first.  `buf` holds the next
-// `nb` bits at its top; `nxt` is the next slot word, already loaded.  The
-// slot image has a zero guard row after its W rows and reads past the slot
-// stay on that row, so a corrupt stream never reads outside the image.
-struct BitReader {
-    uint64_t buf;
-    uint32_t nb, wi, nxt;
+// Reads one stream's slot, most significant bit first: `cur` is the word
+// holding the next bit, `nxt` the word after it, `off` the bits of `cur`
+// already taken, `wi` the index of the next word to load.  The slot image has
+// a zero guard row after its W rows and loads past the slot stay on that row,
+// so a corrupt stream never reads outside the image.
+struct Reader {
+    uint32_t cur, nxt, off, wi;
 };
 
 template <int W>
-__device__ __forceinline__ void br_init(BitReader &r, const uint32_t *col)
+__device__ __forceinline__ void rd_init(Reader &r, const uint32_t *col)
 {
-    r.buf = ((uint64_t)col[0] << 32) | col[kStreams];
-    r.nb = 64;
+    r.cur = col[0];
+    r.nxt = col[kStreams];
+    r.off = 0;
     r.wi = 2;
-    r.nxt = col[2 * kStreams];
 }
 
-// Keep at least 32 bits ahead: two symbols (at most 16 bits each) can then be
-// taken without another refill.
+// One symbol; returns its table entry with the exponent in bits 7..14 (the
+// literal already merged for an escape).
 template <int W>
-__device__ __forceinline__ void br_refill(BitReader &r, const uint32_t *col)
+__device__ __forceinline__ uint32_t rd_take(Reader &r, const uint32_t *col, const uint32_t *lut)
 {
-    if (r.nb < 32) {
-        r.buf |= (uint64_t)r.nxt << (32 - r.nb);
-        r.nb += 32;
-        ++r.wi;
+    const uint32_t win = __funnelshift_l(r.nxt, r.cur, r.off);  // the next 32 bits
+    uint32_t ent = lut[win >> 24];
+    if (ent & kEsc) ent |= ((win << ((ent >> 24) & 15u)) >> 17) & 0x7F80u;
+    r.off += (ent >> 16) & 0xFFu;
+    if (r.off >= 32u) {
+        r.cur = r.nxt;
         r.nxt = col[min(r.wi, (uint32_t)W) * kStreams];
+        ++r.wi;
+        r.off -= 32u;
     }
-}
-
-// One symbol: returns the exponent shifted to bits 7..14.
-__device__ __forceinline__ uint32_t br_symbol(BitReader &r, const uint32_t *lut)
-{
-    const uint32_t top = (uint32_t)(r.buf >> 32);
-    const uint32_t ent = lut[top >> 24];
-    const uint32_t lit = __funnelshift_lc(0u, top, ent >> 24);
-    const uint32_t adv = (ent >> 16) & 0xFFu;
-    r.buf <<= adv;
-    r.nb -= adv;
-    return ((lit >> 17) | ent) & 0x7F80u;
+    return ent;
 }
 
 // Bits taken from the slot so far (more than 32*W means a corrupt stream).
-__device__ __forceinline__ uint32_t br_consumed(const BitReader &r) { return 32u * r.wi - r.nb; }
+__device__ __forceinline__ uint32_t rd_consumed(const Reader &r) { return 32u * (r.wi - 2u) + r.off; }
 
 // ------------------------------------------------------- stream coding
 
 // Appends codes most significant bit first into one stream's W-word slot
 // image (word w at col[w * 256]) until the first code that does not fit; that
-// symbol's index is the marker.
-struct BitWriter {
+// symbol's index is the marker.  `rem` is kept exact only on the checked path
+// (wr_fix_rem restores it after unchecked appends).
+struct Writer {
     uint32_t hi, nbits, wi, rem, marker;
     bool alive;
 };
 
 template <int W>
-__device__ __forceinline__ void bw_init(BitWriter &w, uint32_t nj)
+__device__ __forceinline__ void wr_init(Writer &w, uint32_t nj)
 {
     w.hi = 0;
     w.nbits = 0;
@@ -154,36 +148,76 @@ __device__ __forceinline__ void bw_init(BitWriter &w, uint32_t nj)
     w.alive = true;
 }
 
-__device__ __forceinline__ void bw_put(BitWriter &w, const uint2 ent, uint32_t k, uint32_t *col)
+// Append without the fit check (the caller knows at least 16 bits remain).
+__device__ __forceinline__ void wr_put(Writer &w, const uint2 ent, uint32_t *col)
 {
-    if (!w.alive) return;
-    if (ent.y > w.rem) {
-        w.alive = false;
-        w.marker = k;
-        return;
-    }
-    w.rem -= ent.y;
     const uint32_t merged = w.hi | (ent.x >> w.nbits);
     const uint32_t n2 = w.nbits + ent.y;
     if (n2 >= 32u) {
         col[w.wi * kStreams] = merged;
         ++w.wi;
         w.hi = ent.x << (32u - w.nbits);
-        w.nbits = n2 - 32u;
     } else {
         w.hi = merged;
-        w.nbits = n2;
     }
+    w.nbits = n2 & 31u;
+}
+
+template <int W>
+__device__ __forceinline__ void wr_fix_rem(Writer &w)
+{
+    w.rem = 32u * W - 32u * w.wi - w.nbits;
+}
+
+// Append with the fit check; returns true when symbol k spilled (it, and
+// every later symbol of the stream, goes to the overflow region).
+__device__ __forceinline__ bool wr_put_checked(Writer &w, const uint2 ent, uint32_t k, uint32_t *col)
+{
+    if (w.alive && ent.y <= w.rem) {
+        w.rem -= ent.y;
+        wr_put(w, ent, col);
+        return false;
+    }
+    if (w.alive) {
+        w.alive = false;
+        w.marker = k;
+    }
+    return true;
 }
 
 // Write the partly filled word and zero the rest of the slot.
 template <int W>
-__device__ __forceinline__ void bw_finish(const BitWriter &w, uint32_t *col)
+__device__ __forceinline__ void wr_finish(const Writer &w, uint32_t *col)
 {
     if (w.wi < (uint32_t)W) {
         col[w.wi * kStreams] = w.hi;
         for (uint32_t i = w.wi + 1; i < (uint32_t)W; ++i) col[i * kStreams] = 0u;
     }
+}
+
+// ------------------------------------------------------- value pairs
+// Thread t owns the neighbouring streams 2t and 2t+1, so each row gives it two
+// neighbouring values: one 32-bit word of BF16, one 16-bit pair of bytes.
+
+// Two BF16 -> their two sign-fraction bytes (low byte: the first value).
+__device__ __forceinline__ uint32_t sf_pair(uint32_t x2)
+{
+    const uint32_t hb = __byte_perm(x2, 0u, 0x4431), lb = __byte_perm(x2, 0u, 0x4420);
+    return (hb & 0x8080u) | (lb & 0x7F7Fu);
+}
+
+// Two sign-fraction bytes + two decode-table entries -> two BF16.
+__device__ __forceinline__ uint32_t join_pair(uint32_t sf2, uint32_t ent0, uint32_t ent1)
+{
+    const uint32_t s = __byte_perm(sf2, 0u, 0x1100);       // sf0 sf0 sf1 sf1
+    const uint32_t e = __byte_perm(ent0, ent1, 0x5410);    // low halves: exponents in place
+    return (s & 0x807F807Fu) | e;
+}
+
+// One sign-fraction byte + one decode-table entry -> one BF16.
+__device__ __forceinline__ uint32_t join_one(uint32_t sf, uint32_t ent)
+{
+    return ((sf * 0x101u) & 0x807Fu) | (ent & 0x7F80u);
 }
 
 // ------------------------------------------------------------- scans

@@ -5,34 +5,44 @@
 // compressed inputs, does the arithmetic, and writes the new sign-fraction
 // bytes and the re-coded exponents in a single pass over each block.
 //
-// Thread j of a block's CTA owns stream j of W, of M and of the new W: per
-// row it decodes one symbol of W and of M, updates the value, writes the new
-// sign-fraction byte and appends the new exponent to its slot.  The slot
-// images of W and M come in by TMA bulk copy, the sign-fraction bytes stream
-// through a ring of row chunks.  New exponents are kept for the last 64 rows
-// (all rows when W is updated in place); an out-of-place step that spills
-// more than that re-decodes the older rows of that stream at the end.
+// Thread t of a block's CTA owns the neighbouring streams 2t and 2t+1 of W, of
+// M and of the new W: per row it decodes two symbols of W and two of M,
+// updates the two values, writes their sign-fraction bytes and appends their
+// exponents to the new slots.  The slot images of W and M come in by TMA bulk
+// copy; the sign-fraction bytes stream through a ring of row chunks.  A chunk
+// in which no stream of a warp reaches a spill marker and every new slot has
+// room takes a fast path with no per-value checks.  Spilled new exponents are
+// kept for 64 rows (every row when W is updated in place); an out-of-place
+// step whose stream spills more than that re-decodes the older rows of that
+// stream at the end.
 #include "codec_dev.cuh"
 
 namespace lct {
 namespace dev {
 
-constexpr int kSgdRows = 8;   // rows per sign-fraction chunk
-constexpr int kSgdRing = 3;   // chunks in flight
-constexpr int kSgdSpill = 64; // new-exponent rows kept (out of place)
+constexpr int kSgdThreads = 128;
+constexpr int kSgdRows = 8;    // rows per sign-fraction chunk
+constexpr int kSgdRing = 3;    // chunks in flight
+constexpr int kSgdSpill = 64;  // spilled new-exponent rows kept (out of place)
 
-// float32 -> BF16, round to nearest even; subnormals kept; NaN -> 0x7FC0.
-__device__ __forceinline__ uint32_t bf16_rne(float r)
+// Two float32 -> two BF16 (low half: r0), round to nearest even, subnormals
+// kept.  The conversion writes NaN as 0x7FFF; this library's NaN is 0x7FC0.
+__device__ __forceinline__ uint32_t bf16x2_rne(float r0, float r1)
 {
-    const uint32_t u = __float_as_uint(r);
-    if ((u & 0x7FFFFFFFu) > 0x7F800000u) return 0x7FC0u;
-    return (u + 0x7FFFu + ((u >> 16) & 1u)) >> 16;
+    uint32_t h;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(h) : "f"(r1), "f"(r0));
+    if ((h & 0xFFFFu) == 0x7FFFu) h ^= 0x003Fu;
+    if ((h >> 16) == 0x7FFFu) h ^= 0x003F0000u;
+    return h;
 }
 
-// One value: fl32(w - fl32(eta*m)) (two roundings, never contracted), to BF16.
-__device__ __forceinline__ uint32_t sgd1(uint32_t w, uint32_t m, float eta)
+// Two values of W and two of M (BF16 pairs) -> the two updated BF16:
+// fl32(w - fl32(eta*m)), product and difference rounded separately.
+__device__ __forceinline__ uint32_t sgd_pair(uint32_t w2, uint32_t m2, float eta)
 {
-    return bf16_rne(__fsub_rn(__uint_as_float(w << 16), __fmul_rn(eta, __uint_as_float(m << 16))));
+    const float r0 = __fsub_rn(__uint_as_float(w2 << 16), __fmul_rn(eta, __uint_as_float(m2 << 16)));
+    const float r1 = __fsub_rn(__uint_as_float(w2 & 0xFFFF0000u), __fmul_rn(eta, __uint_as_float(m2 & 0xFFFF0000u)));
+    return bf16x2_rne(r0, r1);
 }
 
 template <int LEVEL, bool INPLACE>
@@ -79,30 +89,30 @@ __global__ void __launch_bounds__(256) k_sgd_prologue(DevTensor w_in, DevTensor 
     }
 }
 
-// Per-stream view of one compressed input (W or M) inside the kernel.
+// One stream of one compressed input (W or M) inside the kernel.
 struct InStream {
-    BitReader rd;
-    const uint32_t *col;     // slot image column in shared memory
-    const uint32_t *lut;     // decode table in shared memory
+    Reader rd;
+    const uint32_t *col;  // slot image column in shared memory
     uint32_t marker;
-    uint64_t ovf_at;         // overflow index of symbol k is ovf_at + k
-    const uint8_t *ovf;
-    bool ovf_ok;
+    uint64_t ovf_at;      // overflow index of spilled symbol k is ovf_at + k
 };
 
+// Symbol k of an input stream as a decode-table entry (exponent in bits 7..14).
 template <int W>
-__device__ __forceinline__ uint32_t in_symbol(InStream &s, uint32_t k)
+__device__ __forceinline__ uint32_t in_take(InStream &s, uint32_t k, const uint32_t *lut, const uint8_t *ovf,
+                                            bool ovf_ok)
 {
-    if (k < s.marker) return br_symbol(s.rd, s.lut);
-    return s.ovf_ok ? (uint32_t)__ldg(s.ovf + s.ovf_at + k) << 7 : 0u;
+    if (k < s.marker) return rd_take<W>(s.rd, s.col, lut);
+    return ovf_ok ? (uint32_t)__ldg(ovf + s.ovf_at + k) << 7 : 0u;
 }
 
 template <int LEVEL, bool INPLACE>
-__global__ void __launch_bounds__(256, 2) k_sgd(const __grid_constant__ SgdArgs a)
+__global__ void __launch_bounds__(kSgdThreads, 2) k_sgd(const __grid_constant__ SgdArgs a)
 {
     using G = Geo<LEVEL>;
     using L = SgdSmem<LEVEL, INPLACE>;
     constexpr int W = G::W, R = kSgdRows, S = kSgdRing, SP = L::kSpillRows;
+    constexpr int NW = kSgdThreads / 32, HALF = kStreams / 2;
     extern __shared__ __align__(128) uint8_t smem[];
     uint32_t *slotW = reinterpret_cast<uint32_t *>(smem);
     uint32_t *slotM = reinterpret_cast<uint32_t *>(smem + L::kSlotIn);
@@ -114,19 +124,19 @@ __global__ void __launch_bounds__(256, 2) k_sgd(const __grid_constant__ SgdArgs 
     uint2 *tbl = reinterpret_cast<uint2 *>(lutM + 256);
     uint8_t *ring = reinterpret_cast<uint8_t *>(tbl + 256);
     __shared__ __align__(8) uint64_t bar_slot, bar_sf[S];
-    __shared__ uint32_t warp_tot[8];
+    __shared__ uint32_t warp_tot[NW];
     __shared__ unsigned long long s_excl;
     __shared__ uint32_t s_flags;  // bit 0: a wait gave up, bit 1: corrupt input
 
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const uint32_t j = tid;
+    const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+    const uint32_t j0 = 2 * t, j1 = 2 * t + 1;
     const uint32_t b = blockIdx.x;
     const uint64_t base = (uint64_t)b * G::B;
     const uint32_t nb = (uint32_t)min((uint64_t)G::B, a.w_in.n - base);
     const uint32_t nrows = (nb + 255) >> 8, nbulk = (nb >> 8) / R, nchunks = (nrows + R - 1) / R;
     const uint64_t limit = a.wait_ns;
 
-    if (tid == 0) {
+    if (t == 0) {
         mbar_init(&bar_slot, 1);
         for (int s = 0; s < S; ++s) mbar_init(&bar_sf[s], 1);
         fence_mbar_init();
@@ -139,13 +149,15 @@ __global__ void __launch_bounds__(256, 2) k_sgd(const __grid_constant__ SgdArgs 
                !(hm->magic == LCT_MAGIC && hm->n == a.m.n && hm->level == LEVEL && hm->cb_hash == a.cbm.hash);
     const int delta_w = a.w_out.hdr->delta;  // the prologue copied W's shift
     const int delta_m = hm->delta;
-    lutW[tid] = dec_entry(a.cbw, delta_w, tid);
-    lutM[tid] = dec_entry(a.cbm, delta_m, tid);
-    tbl[tid] = enc_entry(a.cbw, delta_w, tid);
-    slotW[W * kStreams + tid] = 0u;
-    slotM[W * kStreams + tid] = 0u;
+    for (int v = t; v < 256; v += kSgdThreads) {
+        lutW[v] = dec_entry(a.cbw, delta_w, v);
+        lutM[v] = dec_entry(a.cbm, delta_m, v);
+        tbl[v] = enc_entry(a.cbw, delta_w, v);
+    }
+    reinterpret_cast<uint2 *>(slotW + W * kStreams)[t] = make_uint2(0u, 0u);
+    reinterpret_cast<uint2 *>(slotM + W * kStreams)[t] = make_uint2(0u, 0u);
     __syncthreads();  // barriers initialised
-    if (tid == 0) {
+    if (t == 0) {
         mbar_expect_tx(&bar_slot, 2 * W * kStreams * 4);
         bulk_load(slotW, a.w_in.slots + (uint64_t)b * W * kStreams, W * kStreams * 4, &bar_slot);
         bulk_load(slotM, a.m.slots + (uint64_t)b * W * kStreams, W * kStreams * 4, &bar_slot);
@@ -157,74 +169,109 @@ __global__ void __launch_bounds__(256, 2) k_sgd(const __grid_constant__ SgdArgs 
     }
 
     // input markers, spill prefixes and overflow ranges
-    const uint32_t nj = nb > j ? (nb - j + 255) / 256 : 0;
-    InStream sw, sm;
-    sw.col = slotW + j;
-    sm.col = slotM + j;
-    sw.lut = lutW;
-    sm.lut = lutM;
-    sw.ovf = a.w_in.ovf;
-    sm.ovf = a.m.ovf;
-    uint32_t mk_w = a.w_in.markers[(uint64_t)b * kStreams + j], mk_m = a.m.markers[(uint64_t)b * kStreams + j];
-    bad |= mk_w > nj || mk_m > nj;
-    sw.marker = min(mk_w, nj);
-    sm.marker = min(mk_m, nj);
+    const uint32_t nj0 = nb > j0 ? (nb - j0 + 255) / 256 : 0, nj1 = nb > j1 ? (nb - j1 + 255) / 256 : 0;
+    InStream w0, w1, m0, m1;
+    w0.col = slotW + j0;
+    w1.col = slotW + j1;
+    m0.col = slotM + j0;
+    m1.col = slotM + j1;
+    {
+        const uint32_t mw = reinterpret_cast<const uint32_t *>(a.w_in.markers + (uint64_t)b * kStreams)[t];
+        const uint32_t mm = reinterpret_cast<const uint32_t *>(a.m.markers + (uint64_t)b * kStreams)[t];
+        bad |= (mw & 0xFFFFu) > nj0 || (mw >> 16) > nj1 || (mm & 0xFFFFu) > nj0 || (mm >> 16) > nj1;
+        w0.marker = min(mw & 0xFFFFu, nj0);
+        w1.marker = min(mw >> 16, nj1);
+        m0.marker = min(mm & 0xFFFFu, nj0);
+        m1.marker = min(mm >> 16, nj1);
+    }
+    bool ovf_ok_w, ovf_ok_m;
     {
         uint32_t tot_w, tot_m;
-        const uint32_t pre_w = group_exclusive_scan(nj - sw.marker, warp_tot, 8, 0, &tot_w);
-        const uint32_t pre_m = group_exclusive_scan(nj - sm.marker, warp_tot, 8, 0, &tot_m);
-        const uint64_t w0 = a.w_in.blk_off[b], w1 = a.w_in.blk_off[b + 1];
-        const uint64_t m0 = a.m.blk_off[b], m1 = a.m.blk_off[b + 1];
-        sw.ovf_ok = w1 <= a.w_in.ovf_cap && w0 <= w1 && w1 - w0 == tot_w;
-        sm.ovf_ok = m1 <= a.m.ovf_cap && m0 <= m1 && m1 - m0 == tot_m;
-        sw.ovf_at = w0 + pre_w - sw.marker;
-        sm.ovf_at = m0 + pre_m - sm.marker;
-        bad |= !sw.ovf_ok || !sm.ovf_ok;
+        const uint32_t spw0 = nj0 - w0.marker, spm0 = nj0 - m0.marker;
+        const uint32_t pre_w = group_exclusive_scan(spw0 + nj1 - w1.marker, warp_tot, NW, 0, &tot_w);
+        const uint32_t pre_m = group_exclusive_scan(spm0 + nj1 - m1.marker, warp_tot, NW, 0, &tot_m);
+        const uint64_t a0 = a.w_in.blk_off[b], a1 = a.w_in.blk_off[b + 1];
+        const uint64_t c0 = a.m.blk_off[b], c1 = a.m.blk_off[b + 1];
+        ovf_ok_w = a1 <= a.w_in.ovf_cap && a0 <= a1 && a1 - a0 == tot_w;
+        ovf_ok_m = c1 <= a.m.ovf_cap && c0 <= c1 && c1 - c0 == tot_m;
+        w0.ovf_at = a0 + pre_w - w0.marker;
+        w1.ovf_at = a0 + pre_w + spw0 - w1.marker;
+        m0.ovf_at = c0 + pre_m - m0.marker;
+        m1.ovf_at = c0 + pre_m + spm0 - m1.marker;
+        bad |= !ovf_ok_w || !ovf_ok_m;
     }
+    const uint8_t *ovf_w = a.w_in.ovf, *ovf_m = a.m.ovf;
 
     if (!mbar_wait(&bar_slot, 0, limit)) s_flags = 1;
-    br_init<W>(sw.rd, sw.col);
-    br_init<W>(sm.rd, sm.col);
-    BitWriter bw;
-    bw_init<W>(bw, nj);
-    uint32_t *colO = slotO + j;
-    uint8_t *sfo = a.w_out.sf + base + j;
-    uint8_t *ringj = ring + j;
+    rd_init<W>(w0.rd, w0.col);
+    rd_init<W>(w1.rd, w1.col);
+    rd_init<W>(m0.rd, m0.col);
+    rd_init<W>(m1.rd, m1.col);
+    Writer o0, o1;
+    wr_init<W>(o0, nj0);
+    wr_init<W>(o1, nj1);
+    uint32_t *colO0 = slotO + j0, *colO1 = slotO + j1;
+    uint16_t *sft = reinterpret_cast<uint16_t *>(a.w_out.sf + base) + t;
     const float eta = a.eta;
 
     for (uint32_t c = 0; c < nchunks; ++c) {
         const bool bulk = c < nbulk;
         const uint32_t slot = c % S;
         if (bulk && !mbar_wait(&bar_sf[slot], (c / S) & 1u, (s_flags & 1u) ? 1000000ull : limit)) s_flags = 1;
-        const uint8_t *sfwc = sfW_s + slot * R * kStreams + j;
-        const uint8_t *sfmc = sfM_s + slot * R * kStreams + j;
+        const uint16_t *sfwc = reinterpret_cast<const uint16_t *>(sfW_s + slot * R * kStreams) + t;
+        const uint16_t *sfmc = reinterpret_cast<const uint16_t *>(sfM_s + slot * R * kStreams) + t;
+        uint16_t *sfo = sft + (uint64_t)c * R * HALF;
+        const uint32_t kend = (c + 1) * R;
+        const bool fast = bulk && __all_sync(kFull, w0.marker >= kend && w1.marker >= kend && m0.marker >= kend &&
+                                                        m1.marker >= kend && o0.alive && o1.alive &&
+                                                        o0.rem >= 16u * R && o1.rem >= 16u * R);
+        if (fast) {
 #pragma unroll
-        for (int r = 0; r < R; r += 2) {
-            br_refill<W>(sw.rd, sw.col);
-            br_refill<W>(sm.rd, sm.col);
-#pragma unroll
-            for (int q = 0; q < 2; ++q) {
-                const uint32_t k = c * R + r + q;
-                if (bulk || k < nj) {
-                    const uint32_t ew7 = in_symbol<W>(sw, k), em7 = in_symbol<W>(sm, k);
-                    uint32_t fw, fm;
-                    if (bulk) {
-                        fw = sfwc[(r + q) * kStreams];
-                        fm = sfmc[(r + q) * kStreams];
-                    } else {
-                        fw = a.w_in.sf[base + (uint64_t)k * kStreams + j];
-                        fm = a.m.sf[base + (uint64_t)k * kStreams + j];
-                    }
-                    const uint32_t h = sgd1(join_e7(fw, ew7), join_e7(fm, em7), eta);
-                    const uint32_t e = exp_of(h);
-                    sfo[(uint64_t)k * kStreams] = sf_of(h);
-                    ringj[(k % SP) * kRow] = (uint8_t)e;
-                    bw_put(bw, tbl[e], k, colO);
+            for (int r = 0; r < R; ++r) {
+                const uint32_t ew0 = rd_take<W>(w0.rd, w0.col, lutW), ew1 = rd_take<W>(w1.rd, w1.col, lutW);
+                const uint32_t em0 = rd_take<W>(m0.rd, m0.col, lutM), em1 = rd_take<W>(m1.rd, m1.col, lutM);
+                const uint32_t h2 = sgd_pair(join_pair(sfwc[r * HALF], ew0, ew1), join_pair(sfmc[r * HALF], em0, em1),
+                                             eta);
+                sfo[r * HALF] = (uint16_t)sf_pair(h2);
+                wr_put(o0, tbl[(h2 >> 7) & 0xFFu], colO0);
+                wr_put(o1, tbl[(h2 >> 23) & 0xFFu], colO1);
+            }
+            wr_fix_rem<W>(o0);
+            wr_fix_rem<W>(o1);
+        } else {
+            for (int r = 0; r < R; ++r) {
+                const uint32_t k = c * R + r;
+                if (k >= nj0) break;  // nj1 <= nj0
+                const bool v1 = k < nj1;
+                const uint32_t ew0 = in_take<W>(w0, k, lutW, ovf_w, ovf_ok_w);
+                const uint32_t em0 = in_take<W>(m0, k, lutM, ovf_m, ovf_ok_m);
+                const uint32_t ew1 = v1 ? in_take<W>(w1, k, lutW, ovf_w, ovf_ok_w) : 0u;
+                const uint32_t em1 = v1 ? in_take<W>(m1, k, lutM, ovf_m, ovf_ok_m) : 0u;
+                const uint64_t at = base + (uint64_t)k * kStreams + j0;
+                uint32_t fw, fm;
+                if (bulk) {
+                    fw = sfwc[r * HALF];
+                    fm = sfmc[r * HALF];
+                } else if (v1) {
+                    fw = *reinterpret_cast<const uint16_t *>(a.w_in.sf + at);
+                    fm = *reinterpret_cast<const uint16_t *>(a.m.sf + at);
+                } else {
+                    fw = a.w_in.sf[at];
+                    fm = a.m.sf[at];
                 }
+                const uint32_t h2 = sgd_pair(join_pair(fw, ew0, ew1), join_pair(fm, em0, em1), eta);
+                const uint32_t sf2 = sf_pair(h2);
+                if (v1)
+                    sfo[r * HALF] = (uint16_t)sf2;
+                else
+                    a.w_out.sf[at] = (uint8_t)sf2;
+                const uint32_t e0 = (h2 >> 7) & 0xFFu, e1 = (h2 >> 23) & 0xFFu;
+                if (wr_put_checked(o0, tbl[e0], k, colO0)) ring[(k % SP) * kRow + j0] = (uint8_t)e0;
+                if (v1 && wr_put_checked(o1, tbl[e1], k, colO1)) ring[(k % SP) * kRow + j1] = (uint8_t)e1;
             }
         }
         __syncthreads();  // every thread is done with this chunk's ring slot
-        if (tid == 0 && c + S < nbulk) {
+        if (t == 0 && c + S < nbulk) {
             mbar_expect_tx(&bar_sf[slot], 2 * R * kStreams);
             bulk_load(sfW_s + slot * R * kStreams, a.w_in.sf + base + (uint64_t)(c + S) * R * kStreams, R * kStreams,
                       &bar_sf[slot]);
@@ -232,19 +279,22 @@ __global__ void __launch_bounds__(256, 2) k_sgd(const __grid_constant__ SgdArgs 
                       &bar_sf[slot]);
         }
     }
-    bad |= br_consumed(sw.rd) > 32u * W || br_consumed(sm.rd) > 32u * W;
+    bad |= rd_consumed(w0.rd) > 32u * W || rd_consumed(w1.rd) > 32u * W || rd_consumed(m0.rd) > 32u * W ||
+           rd_consumed(m1.rd) > 32u * W;
     if (bad) atomicOr(&s_flags, 2u);
-    bw_finish<W>(bw, colO);
-    const uint32_t marker = bw.marker, spill = nj - marker;
+    wr_finish<W>(o0, colO0);
+    wr_finish<W>(o1, colO1);
+    const uint32_t mk0 = o0.marker, mk1 = o1.marker, sp0 = nj0 - mk0, sp1 = nj1 - mk1;
     uint32_t total;
-    const uint32_t pre = group_exclusive_scan(spill, warp_tot, 8, 0, &total);  // syncs: slot image complete
+    const uint32_t pre0 = group_exclusive_scan(sp0 + sp1, warp_tot, NW, 0, &total);  // syncs: slot image complete
+    const uint32_t pre1 = pre0 + sp0;
 
-    if (tid == 0) {
+    if (t == 0) {
         fence_proxy_async();
         bulk_store(a.w_out.slots + (uint64_t)b * W * kStreams, slotO, W * kStreams * 4);
         bulk_commit();
     }
-    a.w_out.markers[(uint64_t)b * kStreams + j] = (uint16_t)marker;
+    reinterpret_cast<uint32_t *>(a.w_out.markers + (uint64_t)b * kStreams)[t] = mk0 | (mk1 << 16);
 
     if (warp == 0) {
         bool timed_out;
@@ -266,41 +316,45 @@ __global__ void __launch_bounds__(256, 2) k_sgd(const __grid_constant__ SgdArgs 
     const unsigned long long excl = s_excl;
     if (total > 0 && excl + total <= a.w_out.ovf_cap) {
         uint8_t *out = a.w_out.ovf + excl;
-        const uint32_t kept_from = nrows > (uint32_t)SP ? nrows - SP : 0u;
-        // rows still kept in shared memory: one warp per stream at a time
-        for (int i = 0; i < 32; ++i) {
-            const uint32_t smk = __shfl_sync(kFull, marker, i);
-            const uint32_t ssp = __shfl_sync(kFull, spill, i);
-            const uint32_t spr = __shfl_sync(kFull, pre, i);
-            const uint32_t sj = (uint32_t)(warp * 32 + i);
+        // spilled rows still kept in shared memory: one warp per stream at a time
+        for (int i = 0; i < 64; ++i) {
+            const int src = i >> 1;
+            const uint32_t smk = __shfl_sync(kFull, (i & 1) ? mk1 : mk0, src);
+            const uint32_t ssp = __shfl_sync(kFull, (i & 1) ? sp1 : sp0, src);
+            const uint32_t spr = __shfl_sync(kFull, (i & 1) ? pre1 : pre0, src);
+            const uint32_t sj = (uint32_t)(warp * 64 + i);
+            const uint32_t nj = smk + ssp;
+            const uint32_t kept_from = nj > (uint32_t)SP ? nj - SP : 0u;
             for (uint32_t l = lane; l < ssp; l += 32) {
                 const uint32_t k = smk + l;
                 if (k >= kept_from) out[spr + l] = ring[(k % SP) * kRow + sj];
             }
         }
-        if (!INPLACE && marker < kept_from) {
-            // This stream spilled past the kept rows: decode its W and M again
+        if (!INPLACE) {
+            // A stream that spilled past the kept rows: decode its W and M again
             // from the slot images (still in shared memory) and recompute the
             // older spilled exponents.  W's sign-fraction bytes are intact
             // because the step is out of place.
-            InStream rw = sw, rm = sm;
-            br_init<W>(rw.rd, rw.col);
-            br_init<W>(rm.rd, rm.col);
-            for (uint32_t k = 0; k < kept_from; k += 2) {
-                br_refill<W>(rw.rd, rw.col);
-                br_refill<W>(rm.rd, rm.col);
-                for (uint32_t q = 0; q < 2 && k + q < kept_from; ++q) {
-                    const uint32_t kk = k + q;
-                    const uint32_t ew7 = in_symbol<W>(rw, kk), em7 = in_symbol<W>(rm, kk);
-                    const uint64_t at = base + (uint64_t)kk * kStreams + j;
-                    const uint32_t h = sgd1(join_e7(a.w_in.sf[at], ew7), join_e7(a.m.sf[at], em7), eta);
-                    if (kk >= marker) out[pre + (kk - marker)] = exp_of(h);
+            for (int q = 0; q < 2; ++q) {
+                const uint32_t nj = q ? nj1 : nj0, marker = q ? mk1 : mk0, pre = q ? pre1 : pre0;
+                const uint32_t kept_from = nj > (uint32_t)SP ? nj - SP : 0u;
+                if (marker >= kept_from) continue;
+                const uint32_t j = q ? j1 : j0;
+                InStream rw = q ? w1 : w0, rm = q ? m1 : m0;
+                rd_init<W>(rw.rd, rw.col);
+                rd_init<W>(rm.rd, rm.col);
+                for (uint32_t k = 0; k < kept_from; ++k) {
+                    const uint32_t ew = in_take<W>(rw, k, lutW, ovf_w, ovf_ok_w);
+                    const uint32_t em = in_take<W>(rm, k, lutM, ovf_m, ovf_ok_m);
+                    const uint64_t at = base + (uint64_t)k * kStreams + j;
+                    const uint32_t h = sgd_pair(join_one(a.w_in.sf[at], ew), join_one(a.m.sf[at], em), eta);
+                    if (k >= marker) out[pre + (k - marker)] = exp_of(h);
                 }
             }
         }
     }
     pdl_launch_dependents();
-    if (tid == 0) {
+    if (t == 0) {
         if (s_flags & 1u) {
             for (uint32_t s = 0; s < (uint32_t)S && s < nbulk; ++s) {
                 const uint32_t last = s + (nbulk - 1 - s) / S * S;
@@ -317,7 +371,7 @@ cudaError_t launch_level(const SgdArgs &a, cudaStream_t s)
     constexpr int smem = SgdSmem<LEVEL, INPLACE>::kBytes;
     cudaError_t err = cudaFuncSetAttribute(k_sgd<LEVEL, INPLACE>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (err != cudaSuccess) return err;
-    return launch_pdl(k_sgd<LEVEL, INPLACE>, dim3(a.w_out.nblocks), dim3(256), smem, s, a);
+    return launch_pdl(k_sgd<LEVEL, INPLACE>, dim3(a.w_out.nblocks), dim3(kSgdThreads), smem, s, a);
 }
 
 template <int LEVEL>

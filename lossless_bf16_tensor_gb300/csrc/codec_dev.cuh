@@ -214,10 +214,11 @@ __device__ __forceinline__ uint32_t join_pair(uint32_t sf2, uint32_t ent0, uint3
     return (s & 0x807F807Fu) | e;
 }
 
-// One sign-fraction byte + one decode-table entry -> one BF16.
+// One sign-fraction byte + one decode-table entry -> one BF16 in bits 0..15
+// (bits 16 and up carry the entry's other fields and are to be ignored).
 __device__ __forceinline__ uint32_t join_one(uint32_t sf, uint32_t ent)
 {
-    return ((sf * 0x101u) & 0x807Fu) | (ent & 0x7F80u);
+    return ((sf * 0x101u) & 0x807Fu) | ent;
 }
 
 // ------------------------------------------------------------- scans

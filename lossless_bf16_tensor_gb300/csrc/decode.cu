@@ -6,18 +6,17 @@
 // from its fixed-length slot up to its spill marker, then takes its spilled
 // exponents from the uncompressed overflow region.
 //
-// Thread t owns the neighbouring streams 2t and 2t+1 (two independent decode
-// chains; 16-bit sign-fraction loads and 32-bit BF16 stores).  The block's
-// slot image arrives by one TMA bulk copy; the sign-fraction bytes stream
-// through a ring of row chunks that TMA keeps filled ahead of the decoders.
-// A chunk in which no stream of a warp reaches its spill marker takes a fast
-// path with no per-value checks.
+// Thread j owns stream j.  The block's slot image arrives by one TMA bulk
+// copy; the sign-fraction bytes stream through a ring of row chunks that TMA
+// keeps filled ahead of the decoders; each row the 256 threads decode together
+// is written as 512 contiguous bytes.  A chunk in which no stream of a warp
+// reaches its spill marker takes a fast path with no per-value checks.
 #include "codec_dev.cuh"
 
 namespace lct {
 namespace dev {
 
-constexpr int kDecThreads = 128;
+constexpr int kDecThreads = 256;
 constexpr int kDecRows = 16;  // rows per sign-fraction chunk
 constexpr int kDecRing = 4;   // chunks in flight
 
@@ -31,7 +30,7 @@ struct DecodeSmem {
 };
 
 template <int LEVEL>
-__global__ void __launch_bounds__(kDecThreads, 5) k_decode(const __grid_constant__ DecodeArgs a)
+__global__ void __launch_bounds__(kDecThreads, 4) k_decode(const __grid_constant__ DecodeArgs a)
 {
     using G = Geo<LEVEL>;
     using L = DecodeSmem<LEVEL>;
@@ -44,15 +43,14 @@ __global__ void __launch_bounds__(kDecThreads, 5) k_decode(const __grid_constant
     __shared__ uint32_t warp_tot[kDecThreads / 32];
     __shared__ uint32_t s_timeout;
 
-    const int t = threadIdx.x;
-    const uint32_t j0 = 2 * t, j1 = 2 * t + 1;
+    const int j = threadIdx.x;
     const uint32_t b = blockIdx.x;
     const uint64_t base = (uint64_t)b * G::B;
     const uint32_t nb = (uint32_t)min((uint64_t)G::B, a.t.n - base);
     const uint32_t nrows = (nb + 255) >> 8, nbulk = (nb >> 8) / R, nchunks = (nrows + R - 1) / R;
     const uint64_t limit = a.wait_ns;
 
-    if (t == 0) {
+    if (j == 0) {
         mbar_init(&bar_slot, 1);
         for (int s = 0; s < S; ++s) mbar_init(&bar_sf[s], 1);
         fence_mbar_init();
@@ -64,15 +62,13 @@ __global__ void __launch_bounds__(kDecThreads, 5) k_decode(const __grid_constant
     const bool hdr_ok = hdr->magic == LCT_MAGIC && hdr->n == a.t.n && hdr->level == LEVEL &&
                         hdr->cb_hash == a.cb.hash;
     if (!hdr_ok) {
-        if (t == 0) latch(hdr, LCT_ERR_CORRUPT);
+        if (j == 0) latch(hdr, LCT_ERR_CORRUPT);
         return;  // no copy has been issued yet
     }
-    const int delta = hdr->delta;
-    lut[t] = dec_entry(a.cb, delta, t);
-    lut[t + 128] = dec_entry(a.cb, delta, t + 128);
-    reinterpret_cast<uint2 *>(slot_s + W * kStreams)[t] = make_uint2(0u, 0u);
+    lut[j] = dec_entry(a.cb, hdr->delta, j);
+    slot_s[W * kStreams + j] = 0u;
     __syncthreads();  // barriers initialised
-    if (t == 0) {
+    if (j == 0) {
         mbar_expect_tx(&bar_slot, W * kStreams * 4);
         bulk_load(slot_s, a.t.slots + (uint64_t)b * W * kStreams, W * kStreams * 4, &bar_slot);
         for (uint32_t c = 0; c < (uint32_t)S && c < nbulk; ++c) {
@@ -81,79 +77,56 @@ __global__ void __launch_bounds__(kDecThreads, 5) k_decode(const __grid_constant
         }
     }
 
-    const uint32_t nj0 = nb > j0 ? (nb - j0 + 255) / 256 : 0, nj1 = nb > j1 ? (nb - j1 + 255) / 256 : 0;
-    const uint32_t mk = reinterpret_cast<const uint32_t *>(a.t.markers + (uint64_t)b * kStreams)[t];
-    uint32_t mk0 = mk & 0xFFFFu, mk1 = mk >> 16;
-    bool bad = mk0 > nj0 || mk1 > nj1;
-    mk0 = min(mk0, nj0);
-    mk1 = min(mk1, nj1);
-    const uint32_t sp0 = nj0 - mk0;
+    const uint32_t nj = nb > (uint32_t)j ? (nb - j + 255) / 256 : 0;
+    uint32_t marker = a.t.markers[(uint64_t)b * kStreams + j];
+    bool bad = marker > nj;
+    marker = min(marker, nj);
     uint32_t total;
-    const uint32_t pre0 = group_exclusive_scan(sp0 + (nj1 - mk1), warp_tot, kDecThreads / 32, 0, &total);
+    const uint32_t pre = group_exclusive_scan(nj - marker, warp_tot, kDecThreads / 32, 0, &total);
     const uint64_t off0 = a.t.blk_off[b], off1 = a.t.blk_off[b + 1];
     const bool ovf_ok = off1 <= a.t.ovf_cap && off0 <= off1 && off1 - off0 == total;
-    // overflow index of spilled symbol k of each stream (k >= its marker)
-    const uint64_t at0 = off0 + pre0 - mk0, at1 = off0 + pre0 + sp0 - mk1;
+    const uint64_t ovf_at = off0 + pre - marker;  // overflow index of spilled symbol k is ovf_at + k
 
     if (!mbar_wait(&bar_slot, 0, limit)) s_timeout = 1;
-    const uint32_t *col0 = slot_s + j0, *col1 = slot_s + j1;
-    Reader r0, r1;
-    rd_init<W>(r0, col0);
-    rd_init<W>(r1, col1);
-    uint32_t *yt = reinterpret_cast<uint32_t *>(a.y + base) + t;
+    const uint32_t *col = slot_s + j;
+    Reader rd;
+    rd_init<W>(rd, col);
+    uint16_t *yj = a.y + base + j;
 
     for (uint32_t c = 0; c < nchunks; ++c) {
         const bool bulk = c < nbulk;
         const uint32_t slot = c % S;
         if (bulk && !mbar_wait(&bar_sf[slot], (c / S) & 1u, s_timeout ? 1000000ull : limit)) s_timeout = 1;
-        const uint16_t *sfc = reinterpret_cast<const uint16_t *>(sf_s + slot * R * kStreams) + t;
-        uint32_t *yc = yt + (uint64_t)c * R * (kStreams / 2);
-        const uint32_t kend = (c + 1) * R;
-        if (bulk && __all_sync(kFull, mk0 >= kend && mk1 >= kend)) {
+        const uint8_t *sfc = sf_s + slot * R * kStreams + j;
+        uint16_t *yc = yj + (uint64_t)c * R * kStreams;
+        if (bulk && __all_sync(kFull, marker >= (c + 1) * R)) {
 #pragma unroll
             for (int r = 0; r < R; ++r) {
-                const uint32_t e0 = rd_take<W>(r0, col0, lut);
-                const uint32_t e1 = rd_take<W>(r1, col1, lut);
-                yc[r * (kStreams / 2)] = join_pair(sfc[r * (kStreams / 2)], e0, e1);
+                const uint32_t e = rd_take<W>(rd, col, lut);
+                yc[r * kStreams] = (uint16_t)join_one(sfc[r * kStreams], e);
             }
         } else {
             for (int r = 0; r < R; ++r) {
                 const uint32_t k = c * R + r;
-                if (k >= nj0) break;  // nj1 <= nj0: nothing left in this chunk
-                const bool v1 = k < nj1;
-                uint32_t e0, e1 = 0;
-                if (k < mk0)
-                    e0 = rd_take<W>(r0, col0, lut);
+                if (k >= nj) break;
+                uint32_t e;
+                if (k < marker)
+                    e = rd_take<W>(rd, col, lut);
                 else
-                    e0 = ovf_ok ? (uint32_t)__ldg(a.t.ovf + at0 + k) << 7 : 0u;
-                if (v1) {
-                    if (k < mk1)
-                        e1 = rd_take<W>(r1, col1, lut);
-                    else
-                        e1 = ovf_ok ? (uint32_t)__ldg(a.t.ovf + at1 + k) << 7 : 0u;
-                }
-                const uint64_t at = base + (uint64_t)k * kStreams + j0;
-                uint32_t sf2;
-                if (bulk)
-                    sf2 = sfc[r * (kStreams / 2)];
-                else
-                    sf2 = v1 ? (uint32_t)*reinterpret_cast<const uint16_t *>(a.t.sf + at) : (uint32_t)a.t.sf[at];
-                const uint32_t h2 = join_pair(sf2, e0, e1);
-                if (v1)
-                    yc[r * (kStreams / 2)] = h2;
-                else
-                    a.y[at] = (uint16_t)h2;
+                    e = ovf_ok ? (uint32_t)__ldg(a.t.ovf + ovf_at + k) << 7 : 0u;
+                const uint32_t sf = bulk ? sfc[r * kStreams] : a.t.sf[base + (uint64_t)k * kStreams + j];
+                yc[r * kStreams] = (uint16_t)join_one(sf, e);
             }
         }
         __syncthreads();  // every thread is done with this chunk's ring slot
-        if (t == 0 && c + S < nbulk) {
+        if (j == 0 && c + S < nbulk) {
             mbar_expect_tx(&bar_sf[slot], R * kStreams);
             bulk_load(sf_s + slot * R * kStreams, a.t.sf + base + (uint64_t)(c + S) * R * kStreams, R * kStreams,
                       &bar_sf[slot]);
         }
     }
     pdl_launch_dependents();
-    if (t == 0 && s_timeout) {
+    if (j == 0 && s_timeout) {
         // a wait gave up: let every copy still in flight land before the CTA
         // (and its shared memory) goes away
         mbar_wait(&bar_slot, 0, limit);
@@ -162,9 +135,9 @@ __global__ void __launch_bounds__(kDecThreads, 5) k_decode(const __grid_constant
             mbar_wait(&bar_sf[s], (last / S) & 1u, limit);
         }
     }
-    bad |= rd_consumed(r0) > 32u * W || rd_consumed(r1) > 32u * W;
+    bad |= rd_consumed(rd) > 32u * W;
     if (bad) latch(hdr, LCT_ERR_CORRUPT);
-    if (t == 0) {
+    if (j == 0) {
         if (!ovf_ok) latch(hdr, off1 > a.t.ovf_cap && off0 <= off1 ? LCT_ERR_OVERFLOW_CAPACITY : LCT_ERR_CORRUPT);
         if (s_timeout) latch(hdr, LCT_ERR_TIMEOUT);
     }

@@ -7,23 +7,23 @@
 // 256 streams per block dealt round-robin, fixed-length slots, uncompressed
 // overflow with a per-stream spill marker.
 //
-// Thread t of a block's CTA owns the neighbouring streams 2t and 2t+1.  The
-// BF16 input streams through a ring of row chunks filled by TMA bulk copies;
-// each row's values are split, their sign-fraction bytes written straight
-// out, and their exponents appended to the streams' slot images in shared
-// memory.  A chunk in which every stream of a warp has room for 16 more bits
-// per row takes a fast path with no fit checks.  Spilled exponents are kept in
-// a 64-row ring; a stream that spills more than that has its older spilled
-// exponents read back from the input.
+// Thread j of a block's CTA owns stream j.  The BF16 input streams through a
+// ring of row chunks filled by TMA bulk copies; each row's values are split,
+// their sign-fraction bytes written straight out, and their exponents
+// appended to the streams' slot images in shared memory.  A chunk in which
+// every stream of a warp has room for 16 more bits per row takes a fast path
+// with no fit checks.  Spilled exponents are kept in a 32-row ring; a stream
+// that spills more than that has its older spilled exponents read back from
+// the input.
 #include "codec_dev.cuh"
 
 namespace lct {
 namespace dev {
 
-constexpr int kEncThreads = 128;
-constexpr int kEncRows = 16;    // rows per input chunk
-constexpr int kEncRing = 3;     // chunks in flight
-constexpr int kSpillRows = 64;  // spilled-exponent rows kept
+constexpr int kEncThreads = 256;
+constexpr int kEncRows = 8;     // rows per input chunk
+constexpr int kEncRing = 4;     // chunks in flight
+constexpr int kSpillRows = 32;  // spilled-exponent rows kept
 
 template <int LEVEL>
 struct EncodeSmem {
@@ -111,7 +111,7 @@ __global__ void __launch_bounds__(256) k_encode_prologue(const uint16_t *__restr
 }
 
 template <int LEVEL>
-__global__ void __launch_bounds__(kEncThreads, 3) k_encode(const __grid_constant__ EncodeArgs a)
+__global__ void __launch_bounds__(kEncThreads, 4) k_encode(const __grid_constant__ EncodeArgs a)
 {
     using G = Geo<LEVEL>;
     using L = EncodeSmem<LEVEL>;
@@ -127,15 +127,14 @@ __global__ void __launch_bounds__(kEncThreads, 3) k_encode(const __grid_constant
     __shared__ unsigned long long s_excl;
     __shared__ uint32_t s_timeout;
 
-    const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
-    const uint32_t j0 = 2 * t, j1 = 2 * t + 1;
+    const int j = threadIdx.x, lane = j & 31, warp = j >> 5;
     const uint32_t b = blockIdx.x;
     const uint64_t base = (uint64_t)b * G::B;
     const uint32_t nb = (uint32_t)min((uint64_t)G::B, a.t.n - base);
     const uint32_t nrows = (nb + 255) >> 8, nbulk = (nb >> 8) / R, nchunks = (nrows + R - 1) / R;
     const uint64_t limit = a.wait_ns;
 
-    if (t == 0) {
+    if (j == 0) {
         for (int s = 0; s < S; ++s) mbar_init(&bar[s], 1);
         fence_mbar_init();
         s_timeout = 0;
@@ -148,75 +147,58 @@ __global__ void __launch_bounds__(kEncThreads, 3) k_encode(const __grid_constant
     }
     // the shift and the cleared look-back words come from the prologue
     pdl_wait();
-    const int delta = a.t.hdr->delta;
-    tbl[t] = enc_entry(a.cb, delta, t);
-    tbl[t + 128] = enc_entry(a.cb, delta, t + 128);
+    tbl[j] = enc_entry(a.cb, a.t.hdr->delta, j);
     __syncthreads();
 
-    const uint32_t nj0 = nb > j0 ? (nb - j0 + 255) / 256 : 0, nj1 = nb > j1 ? (nb - j1 + 255) / 256 : 0;
-    Writer w0, w1;
-    wr_init<W>(w0, nj0);
-    wr_init<W>(w1, nj1);
-    uint32_t *col0 = slot_s + j0, *col1 = slot_s + j1;
-    uint16_t *sft = reinterpret_cast<uint16_t *>(a.t.sf + base) + t;
+    const uint32_t nj = nb > (uint32_t)j ? (nb - j + 255) / 256 : 0;
+    Writer wr;
+    wr_init<W>(wr, nj);
+    uint32_t *col = slot_s + j;
+    uint8_t *sfj = a.t.sf + base + j;
+    uint8_t *ringj = ring + j;
 
     for (uint32_t c = 0; c < nchunks; ++c) {
         const bool bulk = c < nbulk;
         const uint32_t slot = c % S;
         if (bulk && !mbar_wait(&bar[slot], (c / S) & 1u, s_timeout ? 1000000ull : limit)) s_timeout = 1;
-        const uint32_t *xc = reinterpret_cast<const uint32_t *>(x_s + slot * R * kStreams) + t;
-        uint16_t *sfc = sft + (uint64_t)c * R * (kStreams / 2);
-        if (bulk && __all_sync(kFull, w0.alive && w1.alive && w0.rem >= 16u * R && w1.rem >= 16u * R)) {
+        const uint16_t *xc = x_s + slot * R * kStreams + j;
+        uint8_t *sfc = sfj + (uint64_t)c * R * kStreams;
+        if (bulk && __all_sync(kFull, wr.alive && wr.rem >= 16u * R)) {
 #pragma unroll
             for (int r = 0; r < R; ++r) {
-                const uint32_t x2 = xc[r * (kStreams / 2)];
-                sfc[r * (kStreams / 2)] = (uint16_t)sf_pair(x2);
-                wr_put(w0, tbl[(x2 >> 7) & 0xFFu], col0);
-                wr_put(w1, tbl[(x2 >> 23) & 0xFFu], col1);
+                const uint32_t h = xc[r * kStreams];
+                sfc[r * kStreams] = sf_of(h);
+                wr_put(wr, tbl[exp_of(h)], col);
             }
-            wr_fix_rem<W>(w0);
-            wr_fix_rem<W>(w1);
+            wr_fix_rem<W>(wr);
         } else {
             for (int r = 0; r < R; ++r) {
                 const uint32_t k = c * R + r;
-                if (k >= nj0) break;  // nj1 <= nj0
-                const bool v1 = k < nj1;
-                const uint64_t at = base + (uint64_t)k * kStreams + j0;
-                uint32_t x2;
-                if (bulk)
-                    x2 = xc[r * (kStreams / 2)];
-                else
-                    x2 = v1 ? *reinterpret_cast<const uint32_t *>(a.x + at) : (uint32_t)a.x[at];
-                const uint32_t sf2 = sf_pair(x2);
-                if (v1)
-                    sfc[r * (kStreams / 2)] = (uint16_t)sf2;
-                else
-                    a.t.sf[at] = (uint8_t)sf2;
-                const uint32_t e0 = (x2 >> 7) & 0xFFu, e1 = (x2 >> 23) & 0xFFu;
-                if (wr_put_checked(w0, tbl[e0], k, col0)) ring[(k & (SP - 1)) * kRow + j0] = (uint8_t)e0;
-                if (v1 && wr_put_checked(w1, tbl[e1], k, col1)) ring[(k & (SP - 1)) * kRow + j1] = (uint8_t)e1;
+                if (k >= nj) break;
+                const uint32_t h = bulk ? xc[r * kStreams] : a.x[base + (uint64_t)k * kStreams + j];
+                const uint32_t e = exp_of(h);
+                sfc[r * kStreams] = sf_of(h);
+                if (wr_put_checked(wr, tbl[e], k, col)) ringj[(k & (SP - 1)) * kRow] = (uint8_t)e;
             }
         }
         __syncthreads();  // every thread is done with this chunk's ring slot
-        if (t == 0 && c + S < nbulk) {
+        if (j == 0 && c + S < nbulk) {
             mbar_expect_tx(&bar[slot], R * kStreams * 2);
             bulk_load(x_s + slot * R * kStreams, a.x + base + (uint64_t)(c + S) * R * kStreams, R * kStreams * 2,
                       &bar[slot]);
         }
     }
-    wr_finish<W>(w0, col0);
-    wr_finish<W>(w1, col1);
-    const uint32_t mk0 = w0.marker, mk1 = w1.marker, sp0 = nj0 - mk0, sp1 = nj1 - mk1;
+    wr_finish<W>(wr, col);
+    const uint32_t marker = wr.marker, spill = nj - marker;
     uint32_t total;
-    const uint32_t pre0 = group_exclusive_scan(sp0 + sp1, warp_tot, NW, 0, &total);  // syncs: slot image complete
-    const uint32_t pre1 = pre0 + sp0;
+    const uint32_t pre = group_exclusive_scan(spill, warp_tot, NW, 0, &total);  // syncs: slot image complete
 
-    if (t == 0) {
+    if (j == 0) {
         fence_proxy_async();
         bulk_store(a.t.slots + (uint64_t)b * W * kStreams, slot_s, W * kStreams * 4);
         bulk_commit();
     }
-    reinterpret_cast<uint32_t *>(a.t.markers + (uint64_t)b * kStreams)[t] = mk0 | (mk1 << 16);
+    a.t.markers[(uint64_t)b * kStreams + j] = (uint16_t)marker;
 
     // overflow offset of this block (single-pass decoupled look-back)
     if (warp == 0) {
@@ -240,14 +222,13 @@ __global__ void __launch_bounds__(kEncThreads, 3) k_encode(const __grid_constant
     const unsigned long long excl = s_excl;
     if (total > 0 && excl + total <= a.t.ovf_cap) {
         uint8_t *out = a.t.ovf + excl;
-        for (int i = 0; i < 64; ++i) {
-            const int src = i >> 1;
-            const uint32_t sm = __shfl_sync(kFull, (i & 1) ? mk1 : mk0, src);
-            const uint32_t sp = __shfl_sync(kFull, (i & 1) ? sp1 : sp0, src);
-            const uint32_t so = __shfl_sync(kFull, (i & 1) ? pre1 : pre0, src);
-            const uint32_t sj = (uint32_t)(warp * 64 + i);
-            const uint32_t nj = sm + sp;
-            const uint32_t kept_from = nj > (uint32_t)SP ? nj - SP : 0u;  // older spills were overwritten
+        for (int i = 0; i < 32; ++i) {
+            const uint32_t sm = __shfl_sync(kFull, marker, i);
+            const uint32_t sp = __shfl_sync(kFull, spill, i);
+            const uint32_t so = __shfl_sync(kFull, pre, i);
+            const uint32_t sj = (uint32_t)(warp * 32 + i);
+            const uint32_t nj_i = sm + sp;
+            const uint32_t kept_from = nj_i > (uint32_t)SP ? nj_i - SP : 0u;  // older spills were overwritten
             for (uint32_t l = lane; l < sp; l += 32) {
                 const uint32_t k = sm + l;
                 out[so + l] = k >= kept_from ? ring[(k & (SP - 1)) * kRow + sj]
@@ -256,7 +237,7 @@ __global__ void __launch_bounds__(kEncThreads, 3) k_encode(const __grid_constant
         }
     }
     pdl_launch_dependents();
-    if (t == 0) {
+    if (j == 0) {
         if (s_timeout) {
             latch(a.t.hdr, LCT_ERR_TIMEOUT);
             for (uint32_t s = 0; s < (uint32_t)S && s < nbulk; ++s) {

@@ -71,69 +71,47 @@ __device__ __forceinline__ uint2 enc_entry(const DevCodebook &cb, int delta, int
 
 // Decode table for shift delta, indexed by the next 8 bits of the stream:
 //   bits  7..14  the exponent, for a symbol with its own code (0 for escape)
-//   bits 16..23  bits consumed (code length, or escape length + 8)
-//   bits 24..27  escape length (escape only)
-//   bit  31      escape: the exponent is the 8-bit literal after the prefix
-// Bits 0..15 of an entry are therefore the exponent already in place in a
-// BF16 word (bits 7..14), ready to be OR-ed with the sign and fraction.
-constexpr uint32_t kEsc = 0x80000000u;
-
+//   bits 16..23  right shift that brings the escape literal to bits 7..14
+//                (17 - escape length); 32 for a coded symbol, which clears it
+//   bits 27..31  bits consumed (code length, or escape length + 8)
 __device__ __forceinline__ uint32_t dec_entry(const DevCodebook &cb, int delta, int v)
 {
     const uint32_t d = cb.dec[v], sym = d & 0x1FF, l = d >> 12;
-    if (sym == 256) return kEsc | (l << 24) | ((l + 8u) << 16);
-    return (l << 16) | (((sym + (uint32_t)delta) & 0xFFu) << 7);
+    if (sym == 256) return ((l + 8u) << 27) | ((17u - l) << 16);
+    return (l << 27) | (32u << 16) | (((sym + (uint32_t)delta) & 0xFFu) << 7);
 }
 
 // ------------------------------------------------------ stream decoding
 
-// Reads one stream's slot, most significant bit first: `cur` is the word
-// holding the next bit, `nxt` the word after it, `off` the bits of `cur`
-// already taken, `wi` the index of the next word to load.  The slot image has
-// a zero guard row after its W rows and loads past the slot stay on that row,
-// so a corrupt stream never reads outside the image.
-struct Reader {
-    uint32_t cur, nxt, off, wi;
-};
-
+// One symbol of a stream read most significant bit first from its slot image
+// column (word w at col[w * 256]); p is the bit position, advanced past the
+// symbol.  Returns the exponent in bits 7..14 (other bits are to be ignored).
+// The word index is clamped to the slot and the image has a zero guard row
+// after it, so a corrupt stream never reads outside the image (it shows up as
+// p > 32*W instead).
 template <int W>
-__device__ __forceinline__ void rd_init(Reader &r, const uint32_t *col)
+__device__ __forceinline__ uint32_t rd_take(uint32_t &p, const uint32_t *__restrict__ col,
+                                            const uint32_t *__restrict__ lut)
 {
-    r.cur = col[0];
-    r.nxt = col[kStreams];
-    r.off = 0;
-    r.wi = 2;
+    const uint32_t w = min(p >> 5, (uint32_t)(W - 1));
+    const uint32_t hi = col[w * kStreams], lo = col[(w + 1) * kStreams];
+    const uint32_t win = __funnelshift_l(lo, hi, p);  // the next 32 bits
+    const uint32_t ent = lut[win >> 24];
+    const uint32_t lit = __funnelshift_rc(win, 0u, (ent >> 16) & 0xFFu);  // escape literal, or 0
+    p += ent >> 27;
+    return ent | lit;
 }
-
-// One symbol; returns its table entry with the exponent in bits 7..14 (the
-// literal already merged for an escape).
-template <int W>
-__device__ __forceinline__ uint32_t rd_take(Reader &r, const uint32_t *col, const uint32_t *lut)
-{
-    const uint32_t win = __funnelshift_l(r.nxt, r.cur, r.off);  // the next 32 bits
-    uint32_t ent = lut[win >> 24];
-    if (ent & kEsc) ent |= ((win << ((ent >> 24) & 15u)) >> 17) & 0x7F80u;
-    r.off += (ent >> 16) & 0xFFu;
-    if (r.off >= 32u) {
-        r.cur = r.nxt;
-        r.nxt = col[min(r.wi, (uint32_t)W) * kStreams];
-        ++r.wi;
-        r.off -= 32u;
-    }
-    return ent;
-}
-
-// Bits taken from the slot so far (more than 32*W means a corrupt stream).
-__device__ __forceinline__ uint32_t rd_consumed(const Reader &r) { return 32u * (r.wi - 2u) + r.off; }
 
 // ------------------------------------------------------- stream coding
 
 // Appends codes most significant bit first into one stream's W-word slot
 // image (word w at col[w * 256]) until the first code that does not fit; that
-// symbol's index is the marker.  `rem` is kept exact only on the checked path
-// (wr_fix_rem restores it after unchecked appends).
+// symbol's index is the marker.  Bits not yet written sit in a 64-bit
+// accumulator (hi:lo) holding `nbits` bits; at most one word is flushed per
+// flush call.  `rem` is kept exact only on the checked path (wr_fix_rem
+// restores it after unchecked appends).
 struct Writer {
-    uint32_t hi, nbits, wi, rem, marker;
+    uint32_t hi, lo, nbits, wi, rem, marker;
     bool alive;
 };
 
@@ -141,6 +119,7 @@ template <int W>
 __device__ __forceinline__ void wr_init(Writer &w, uint32_t nj)
 {
     w.hi = 0;
+    w.lo = 0;
     w.nbits = 0;
     w.wi = 0;
     w.rem = 32u * W;
@@ -148,19 +127,27 @@ __device__ __forceinline__ void wr_init(Writer &w, uint32_t nj)
     w.alive = true;
 }
 
-// Append without the fit check (the caller knows at least 16 bits remain).
-__device__ __forceinline__ void wr_put(Writer &w, const uint2 ent, uint32_t *col)
+// Append one code (left-aligned in ent.x, ent.y bits) without flushing; the
+// accumulator must have room (nbits + ent.y <= 64).
+__device__ __forceinline__ void wr_add(Writer &w, const uint2 ent)
 {
-    const uint32_t merged = w.hi | (ent.x >> w.nbits);
-    const uint32_t n2 = w.nbits + ent.y;
-    if (n2 >= 32u) {
-        col[w.wi * kStreams] = merged;
+    const uint64_t v = ((uint64_t)ent.x << 32) >> w.nbits;
+    w.hi |= (uint32_t)(v >> 32);
+    w.lo |= (uint32_t)v;
+    w.nbits += ent.y;
+}
+
+// Write out the accumulator's first word if it is complete (leaves nbits < 32
+// when nbits was below 64).
+__device__ __forceinline__ void wr_flush(Writer &w, uint32_t *__restrict__ col)
+{
+    if (w.nbits >= 32u) {
+        col[w.wi * kStreams] = w.hi;
         ++w.wi;
-        w.hi = ent.x << (32u - w.nbits);
-    } else {
-        w.hi = merged;
+        w.hi = w.lo;
+        w.lo = 0;
+        w.nbits -= 32u;
     }
-    w.nbits = n2 & 31u;
 }
 
 template <int W>
@@ -175,7 +162,8 @@ __device__ __forceinline__ bool wr_put_checked(Writer &w, const uint2 ent, uint3
 {
     if (w.alive && ent.y <= w.rem) {
         w.rem -= ent.y;
-        wr_put(w, ent, col);
+        wr_add(w, ent);
+        wr_flush(w, col);
         return false;
     }
     if (w.alive) {
@@ -195,30 +183,14 @@ __device__ __forceinline__ void wr_finish(const Writer &w, uint32_t *col)
     }
 }
 
-// ------------------------------------------------------- value pairs
-// Thread t owns the neighbouring streams 2t and 2t+1, so each row gives it two
-// neighbouring values: one 32-bit word of BF16, one 16-bit pair of bytes.
+// ------------------------------------------------------------ join
 
-// Two BF16 -> their two sign-fraction bytes (low byte: the first value).
-__device__ __forceinline__ uint32_t sf_pair(uint32_t x2)
+// One sign-fraction byte + an exponent in bits 7..14 (other bits ignored) ->
+// one BF16 in bits 0..15 (bits 16 and up are to be ignored).  sf * 0x101 puts
+// the sign at bit 15 and keeps the fraction in bits 0..6.
+__device__ __forceinline__ uint32_t join_one(uint32_t sf, uint32_t e)
 {
-    const uint32_t hb = __byte_perm(x2, 0u, 0x4431), lb = __byte_perm(x2, 0u, 0x4420);
-    return (hb & 0x8080u) | (lb & 0x7F7Fu);
-}
-
-// Two sign-fraction bytes + two decode-table entries -> two BF16.
-__device__ __forceinline__ uint32_t join_pair(uint32_t sf2, uint32_t ent0, uint32_t ent1)
-{
-    const uint32_t s = __byte_perm(sf2, 0u, 0x1100);       // sf0 sf0 sf1 sf1
-    const uint32_t e = __byte_perm(ent0, ent1, 0x5410);    // low halves: exponents in place
-    return (s & 0x807F807Fu) | e;
-}
-
-// One sign-fraction byte + one decode-table entry -> one BF16 in bits 0..15
-// (bits 16 and up carry the entry's other fields and are to be ignored).
-__device__ __forceinline__ uint32_t join_one(uint32_t sf, uint32_t ent)
-{
-    return ((sf * 0x101u) & 0x807Fu) | ent;
+    return ((sf * 0x101u) & 0x807Fu) | (e & 0xFFFF7F80u);
 }
 
 // ------------------------------------------------------------- scans

@@ -89,8 +89,7 @@ __global__ void __launch_bounds__(kDecThreads, 4) k_decode(const __grid_constant
 
     if (!mbar_wait(&bar_slot, 0, limit)) s_timeout = 1;
     const uint32_t *col = slot_s + j;
-    Reader rd;
-    rd_init<W>(rd, col);
+    uint32_t pos = 0;  // bit position in the slot
     uint16_t *yj = a.y + base + j;
 
     for (uint32_t c = 0; c < nchunks; ++c) {
@@ -100,18 +99,22 @@ __global__ void __launch_bounds__(kDecThreads, 4) k_decode(const __grid_constant
         const uint8_t *sfc = sf_s + slot * R * kStreams + j;
         uint16_t *yc = yj + (uint64_t)c * R * kStreams;
         if (bulk && __all_sync(kFull, marker >= (c + 1) * R)) {
+            // loads first (the decode chain and the chunk's sign-fraction
+            // bytes), stores last, so nothing orders a load behind a store
+            uint32_t e[R], sf[R];
 #pragma unroll
-            for (int r = 0; r < R; ++r) {
-                const uint32_t e = rd_take<W>(rd, col, lut);
-                yc[r * kStreams] = (uint16_t)join_one(sfc[r * kStreams], e);
-            }
+            for (int r = 0; r < R; ++r) e[r] = rd_take<W>(pos, col, lut);
+#pragma unroll
+            for (int r = 0; r < R; ++r) sf[r] = sfc[r * kStreams];
+#pragma unroll
+            for (int r = 0; r < R; ++r) yc[r * kStreams] = (uint16_t)join_one(sf[r], e[r]);
         } else {
             for (int r = 0; r < R; ++r) {
                 const uint32_t k = c * R + r;
                 if (k >= nj) break;
                 uint32_t e;
                 if (k < marker)
-                    e = rd_take<W>(rd, col, lut);
+                    e = rd_take<W>(pos, col, lut);
                 else
                     e = ovf_ok ? (uint32_t)__ldg(a.t.ovf + ovf_at + k) << 7 : 0u;
                 const uint32_t sf = bulk ? sfc[r * kStreams] : a.t.sf[base + (uint64_t)k * kStreams + j];
@@ -135,7 +138,7 @@ __global__ void __launch_bounds__(kDecThreads, 4) k_decode(const __grid_constant
             mbar_wait(&bar_sf[s], (last / S) & 1u, limit);
         }
     }
-    bad |= rd_consumed(rd) > 32u * W;
+    bad |= pos > 32u * W;
     if (bad) latch(hdr, LCT_ERR_CORRUPT);
     if (j == 0) {
         if (!ovf_ok) latch(hdr, off1 > a.t.ovf_cap && off0 <= off1 ? LCT_ERR_OVERFLOW_CAPACITY : LCT_ERR_CORRUPT);

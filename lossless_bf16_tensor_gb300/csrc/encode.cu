@@ -21,8 +21,8 @@ namespace lct {
 namespace dev {
 
 constexpr int kEncThreads = 256;
-constexpr int kEncRows = 8;     // rows per input chunk
-constexpr int kEncRing = 4;     // chunks in flight
+constexpr int kEncRows = 16;    // rows per input chunk
+constexpr int kEncRing = 2;     // chunks in flight
 constexpr int kSpillRows = 32;  // spilled-exponent rows kept
 
 template <int LEVEL>
@@ -164,11 +164,21 @@ __global__ void __launch_bounds__(kEncThreads, 4) k_encode(const __grid_constant
         const uint16_t *xc = x_s + slot * R * kStreams + j;
         uint8_t *sfc = sfj + (uint64_t)c * R * kStreams;
         if (bulk && __all_sync(kFull, wr.alive && wr.rem >= 16u * R)) {
+            // loads first (inputs, then their code-table entries), stores
+            // last, so nothing orders a load behind a store
+            uint32_t h[R];
+            uint2 ent[R];
 #pragma unroll
-            for (int r = 0; r < R; ++r) {
-                const uint32_t h = xc[r * kStreams];
-                sfc[r * kStreams] = sf_of(h);
-                wr_put(wr, tbl[exp_of(h)], col);
+            for (int r = 0; r < R; ++r) h[r] = xc[r * kStreams];
+#pragma unroll
+            for (int r = 0; r < R; ++r) ent[r] = tbl[exp_of(h[r])];
+#pragma unroll
+            for (int r = 0; r < R; ++r) sfc[r * kStreams] = sf_of(h[r]);
+#pragma unroll
+            for (int r = 0; r < R; r += 2) {  // two codes fit the accumulator, then one flush
+                wr_add(wr, ent[r]);
+                wr_add(wr, ent[r + 1]);
+                wr_flush(wr, col);
             }
             wr_fix_rem<W>(wr);
         } else {

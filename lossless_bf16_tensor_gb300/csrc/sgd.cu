@@ -87,7 +87,7 @@ __global__ void __launch_bounds__(256) k_sgd_prologue(DevTensor w_in, DevTensor 
 
 // One stream of one compressed input (W or M) inside the kernel.
 struct InStream {
-    Reader rd;
+    uint32_t pos;         // bit position in the slot
     const uint32_t *col;  // slot image column in shared memory
     uint32_t marker;
     uint64_t ovf_at;      // overflow index of spilled symbol k is ovf_at + k
@@ -98,7 +98,7 @@ template <int W>
 __device__ __forceinline__ uint32_t in_take(InStream &s, uint32_t k, const uint32_t *lut, const uint8_t *ovf,
                                             bool ovf_ok)
 {
-    if (k < s.marker) return rd_take<W>(s.rd, s.col, lut);
+    if (k < s.marker) return rd_take<W>(s.pos, s.col, lut);
     return ovf_ok ? (uint32_t)__ldg(ovf + s.ovf_at + k) << 7 : 0u;
 }
 
@@ -187,8 +187,8 @@ __global__ void __launch_bounds__(kSgdThreads, 2) k_sgd(const __grid_constant__ 
     const uint8_t *ovf_w = a.w_in.ovf, *ovf_m = a.m.ovf;
 
     if (!mbar_wait(&bar_slot, 0, limit)) s_flags = 1;
-    rd_init<W>(sw.rd, sw.col);
-    rd_init<W>(sm.rd, sm.col);
+    sw.pos = 0;
+    sm.pos = 0;
     Writer wo;
     wr_init<W>(wo, nj);
     uint32_t *colO = slotO + j;
@@ -205,13 +205,28 @@ __global__ void __launch_bounds__(kSgdThreads, 2) k_sgd(const __grid_constant__ 
         uint8_t *sfo = sfj + (uint64_t)c * R * kStreams;
         const uint32_t kend = (c + 1) * R;
         if (bulk && __all_sync(kFull, sw.marker >= kend && sm.marker >= kend && wo.alive && wo.rem >= 16u * R)) {
+            // loads first (both decode chains, the sign-fraction bytes, the
+            // new values' code-table entries), stores last, so nothing orders
+            // a load behind a store
+            uint32_t ew[R], em[R], h[R];
+            uint2 ent[R];
 #pragma unroll
             for (int r = 0; r < R; ++r) {
-                const uint32_t ew = rd_take<W>(sw.rd, sw.col, lutW);
-                const uint32_t em = rd_take<W>(sm.rd, sm.col, lutM);
-                const uint32_t h = sgd_one(join_one(sfwc[r * kStreams], ew), join_one(sfmc[r * kStreams], em), eta);
-                sfo[r * kStreams] = sf_of(h);
-                wr_put(wo, tbl[exp_of(h)], colO);
+                ew[r] = rd_take<W>(sw.pos, sw.col, lutW);
+                em[r] = rd_take<W>(sm.pos, sm.col, lutM);
+            }
+#pragma unroll
+            for (int r = 0; r < R; ++r)
+                h[r] = sgd_one(join_one(sfwc[r * kStreams], ew[r]), join_one(sfmc[r * kStreams], em[r]), eta);
+#pragma unroll
+            for (int r = 0; r < R; ++r) ent[r] = tbl[exp_of(h[r])];
+#pragma unroll
+            for (int r = 0; r < R; ++r) sfo[r * kStreams] = sf_of(h[r]);
+#pragma unroll
+            for (int r = 0; r < R; r += 2) {  // two codes fit the accumulator, then one flush
+                wr_add(wo, ent[r]);
+                wr_add(wo, ent[r + 1]);
+                wr_flush(wo, colO);
             }
             wr_fix_rem<W>(wo);
         } else {
@@ -238,7 +253,7 @@ __global__ void __launch_bounds__(kSgdThreads, 2) k_sgd(const __grid_constant__ 
                       &bar_sf[slot]);
         }
     }
-    bad |= rd_consumed(sw.rd) > 32u * W || rd_consumed(sm.rd) > 32u * W;
+    bad |= sw.pos > 32u * W || sm.pos > 32u * W;
     if (bad) atomicOr(&s_flags, 2u);
     wr_finish<W>(wo, colO);
     const uint32_t marker = wo.marker, spill = nj - marker;
@@ -292,8 +307,8 @@ __global__ void __launch_bounds__(kSgdThreads, 2) k_sgd(const __grid_constant__ 
             // older spilled exponents.  W's sign-fraction bytes are intact
             // because the step is out of place.
             InStream rw = sw, rm = sm;
-            rd_init<W>(rw.rd, rw.col);
-            rd_init<W>(rm.rd, rm.col);
+            rw.pos = 0;
+            rm.pos = 0;
             for (uint32_t k = 0; k < kept_from; ++k) {
                 const uint32_t ew = in_take<W>(rw, k, lutW, ovf_w, ovf_ok_w);
                 const uint32_t em = in_take<W>(rm, k, lutM, ovf_m, ovf_ok_m);

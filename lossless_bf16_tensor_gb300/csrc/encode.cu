@@ -21,8 +21,8 @@ namespace lct {
 namespace dev {
 
 constexpr int kEncThreads = 256;
-constexpr int kEncRows = 16;    // rows per input chunk
-constexpr int kEncRing = 2;     // chunks in flight
+constexpr int kEncRows = 8;     // rows per input chunk
+constexpr int kEncRing = 4;     // chunks in flight
 constexpr int kSpillRows = 32;  // spilled-exponent rows kept
 
 template <int LEVEL>
@@ -163,29 +163,41 @@ __global__ void __launch_bounds__(kEncThreads, 4) k_encode(const __grid_constant
         if (bulk && !mbar_wait(&bar[slot], (c / S) & 1u, s_timeout ? 1000000ull : limit)) s_timeout = 1;
         const uint16_t *xc = x_s + slot * R * kStreams + j;
         uint8_t *sfc = sfj + (uint64_t)c * R * kStreams;
-        if (bulk && __all_sync(kFull, wr.alive && wr.rem >= 16u * R)) {
+        if (bulk) {
             // loads first (inputs, then their code-table entries), stores
             // last, so nothing orders a load behind a store
-            uint32_t h[R];
+            uint32_t h[R], need = 0;
             uint2 ent[R];
 #pragma unroll
             for (int r = 0; r < R; ++r) h[r] = xc[r * kStreams];
 #pragma unroll
-            for (int r = 0; r < R; ++r) ent[r] = tbl[exp_of(h[r])];
+            for (int r = 0; r < R; ++r) {
+                ent[r] = tbl[exp_of(h[r])];
+                need += ent[r].y;
+            }
 #pragma unroll
             for (int r = 0; r < R; ++r) sfc[r * kStreams] = sf_of(h[r]);
+            if (__all_sync(kFull, wr.alive && need <= wr.rem)) {
+                // every stream of the warp keeps the whole chunk in its slot
 #pragma unroll
-            for (int r = 0; r < R; r += 2) {  // two codes fit the accumulator, then one flush
-                wr_add(wr, ent[r]);
-                wr_add(wr, ent[r + 1]);
-                wr_flush(wr, col);
+                for (int r = 0; r < R; r += 2) {  // two codes fit the accumulator, then one flush
+                    wr_add(wr, ent[r]);
+                    wr_add(wr, ent[r + 1]);
+                    wr_flush(wr, col);
+                }
+                wr.rem -= need;
+            } else {
+#pragma unroll
+                for (int r = 0; r < R; ++r) {
+                    const uint32_t k = c * R + r;
+                    if (wr_put_checked(wr, ent[r], k, col)) ringj[(k & (SP - 1)) * kRow] = (uint8_t)exp_of(h[r]);
+                }
             }
-            wr_fix_rem<W>(wr);
         } else {
             for (int r = 0; r < R; ++r) {
                 const uint32_t k = c * R + r;
                 if (k >= nj) break;
-                const uint32_t h = bulk ? xc[r * kStreams] : a.x[base + (uint64_t)k * kStreams + j];
+                const uint32_t h = a.x[base + (uint64_t)k * kStreams + j];
                 const uint32_t e = exp_of(h);
                 sfc[r * kStreams] = sf_of(h);
                 if (wr_put_checked(wr, tbl[e], k, col)) ringj[(k & (SP - 1)) * kRow] = (uint8_t)e;

@@ -204,11 +204,11 @@ __global__ void __launch_bounds__(kSgdThreads, 2) k_sgd(const __grid_constant__ 
         const uint8_t *sfmc = sfM_s + slot * R * kStreams + j;
         uint8_t *sfo = sfj + (uint64_t)c * R * kStreams;
         const uint32_t kend = (c + 1) * R;
-        if (bulk && __all_sync(kFull, sw.marker >= kend && sm.marker >= kend && wo.alive && wo.rem >= 16u * R)) {
+        if (bulk && __all_sync(kFull, sw.marker >= kend && sm.marker >= kend)) {
             // loads first (both decode chains, the sign-fraction bytes, the
             // new values' code-table entries), stores last, so nothing orders
             // a load behind a store
-            uint32_t ew[R], em[R], h[R];
+            uint32_t ew[R], em[R], h[R], need = 0;
             uint2 ent[R];
 #pragma unroll
             for (int r = 0; r < R; ++r) {
@@ -219,16 +219,28 @@ __global__ void __launch_bounds__(kSgdThreads, 2) k_sgd(const __grid_constant__ 
             for (int r = 0; r < R; ++r)
                 h[r] = sgd_one(join_one(sfwc[r * kStreams], ew[r]), join_one(sfmc[r * kStreams], em[r]), eta);
 #pragma unroll
-            for (int r = 0; r < R; ++r) ent[r] = tbl[exp_of(h[r])];
+            for (int r = 0; r < R; ++r) {
+                ent[r] = tbl[exp_of(h[r])];
+                need += ent[r].y;
+            }
 #pragma unroll
             for (int r = 0; r < R; ++r) sfo[r * kStreams] = sf_of(h[r]);
+            if (__all_sync(kFull, wo.alive && need <= wo.rem)) {
+                // every new stream of the warp keeps the whole chunk in its slot
 #pragma unroll
-            for (int r = 0; r < R; r += 2) {  // two codes fit the accumulator, then one flush
-                wr_add(wo, ent[r]);
-                wr_add(wo, ent[r + 1]);
-                wr_flush(wo, colO);
+                for (int r = 0; r < R; r += 2) {  // two codes fit the accumulator, then one flush
+                    wr_add(wo, ent[r]);
+                    wr_add(wo, ent[r + 1]);
+                    wr_flush(wo, colO);
+                }
+                wo.rem -= need;
+            } else {
+#pragma unroll
+                for (int r = 0; r < R; ++r) {
+                    const uint32_t k = c * R + r;
+                    if (wr_put_checked(wo, ent[r], k, colO)) ringj[(k % SP) * kRow] = (uint8_t)exp_of(h[r]);
+                }
             }
-            wr_fix_rem<W>(wo);
         } else {
             for (int r = 0; r < R; ++r) {
                 const uint32_t k = c * R + r;

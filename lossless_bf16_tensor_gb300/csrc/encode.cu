@@ -59,11 +59,14 @@ __global__ void __launch_bounds__(256) k_encode_prologue(const uint16_t *__restr
     __syncthreads();
     const uint64_t n = t.n;
     const uint32_t m = n < (uint64_t)LCT_SHIFT_SAMPLES ? (uint32_t)n : (uint32_t)LCT_SHIFT_SAMPLES;
+    // floor(k*n/m): with m = 4096 = 2^12 a shift, with m = n just k
+    static_assert(LCT_SHIFT_SAMPLES == 4096, "sample positions use a shift by 12");
     uint16_t v[kPer];
 #pragma unroll
     for (int i = 0; i < kPer; ++i) {  // all loads in flight at once
         const uint32_t k = tid + 256u * i;
-        v[i] = k < m ? __ldg(x + ((uint64_t)k * n) / m) : 0;
+        const uint64_t at = m == (uint32_t)LCT_SHIFT_SAMPLES ? ((uint64_t)k * n) >> 12 : (uint64_t)k;
+        v[i] = k < m ? __ldg(x + at) : 0;
     }
 #pragma unroll
     for (int i = 0; i < kPer; ++i) {

@@ -34,6 +34,8 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 WORKLOAD_TEXT = {
+    "gauss_block": "65,536 BF16 ~ N(0,0.02), Gaussian codebook, CLEAN (one block); step = encode + decode + fused "
+                   "SGD (M ~ Laplace(0,1e-3))",
     "laplace_16m": "2^24 BF16 ~ Laplace(0,0.01), Laplace codebook, CLEAN; step = encode + decode + fused SGD "
                    "(M ~ Laplace(0,1e-3))",
     "heavy_64m": "2^26 BF16 Student-t(3)*1e-3 with 0.1% x1e4 outliers and 1% subnormals, power-law codebook, "
@@ -43,7 +45,7 @@ WORKLOAD_TEXT = {
     "sgd_162m": "162,000,000 BF16 W ~ N(0,0.02), M ~ N(0,1e-3), Gaussian codebooks, CLEAN; step = encode + decode "
                 "+ fused SGD",
 }
-SGD_MOMENTUM = {"laplace_16m": ("laplace", 1e-3), "heavy_64m": ("laplace", 1e-3), "gelu_act": ("laplace", 1e-3),
+SGD_MOMENTUM = {"gauss_block": ("laplace", 1e-3), "laplace_16m": ("laplace", 1e-3), "heavy_64m": ("laplace", 1e-3), "gelu_act": ("laplace", 1e-3),
                 "sgd_162m": ("gaussian", 1e-3)}
 ETA = float(np.float32(1e-3))
 L2_FLUSH_BYTES = 256 << 20
@@ -65,6 +67,24 @@ def hbm_peak():
 def dist_env():
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     return int(os.environ.get("RANK", "0")), int(os.environ.get("LOCAL_RANK", "0")), ws
+
+
+def max_over_ranks(value: float, device=None) -> float:
+    """The largest `value` over all ranks (the job's time is its slowest
+    rank's); `value` itself when no process group is running."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(value)
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def replica_units(n_per_rank: int, world: int) -> int:
+    """Values the whole job processes per step: every rank runs its own
+    replica of the workload (weak scaling, no collective on the data path)."""
+    return n_per_rank * world
 
 
 # ----------------------------------------------------------------- clocks
@@ -209,11 +229,7 @@ def run_gpu(args):
     enc = [e[0].elapsed_time(e[1]) for e in evs]
     dec = [e[1].elapsed_time(e[2]) for e in evs]
     sgd = [e[2].elapsed_time(e[3]) for e in evs]
-    total_ms = sum(a + b + c for a, b, c in zip(enc, dec, sgd))
-    if world > 1:
-        t = torch.tensor([total_ms], dtype=torch.float64, device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(sum(a + b + c for a, b, c in zip(enc, dec, sgd)), device="cuda")
     ms_step = total_ms / args.steps
 
     sx, sm_, sw = X.state(), Mc.state(), Wn.state()
@@ -228,7 +244,7 @@ def run_gpu(args):
     dom = max(t_ms, key=t_ms.get)
     achieved = alg[dom] / (t_ms[dom] * 1e-3) / 1e9
     uncompressed_per_step = 10 * n
-    value = uncompressed_per_step * world / (ms_step * 1e-3) / 1e9
+    value = 10 * replica_units(n, world) / (ms_step * 1e-3) / 1e9
 
     traffic = None
     tpath = os.path.join(ROOT, "profiles", "traffic.json")
@@ -266,12 +282,8 @@ def run_gpu(args):
             ee[k][1].record(stream)
         torch.cuda.synchronize()
         assert torch.equal(hy, hx)
-        e_ms = sum(a.elapsed_time(b) for a, b in ee) / args.steps
-        if world > 1:
-            t = torch.tensor([e_ms], dtype=torch.float64, device="cuda")
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e_ms = float(t.item())
-        e2e = {"value": round(uncompressed_per_step * world / (e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+        e_ms = max_over_ranks(sum(a.elapsed_time(b) for a, b in ee) / args.steps, device="cuda")
+        e2e = {"value": round(10 * replica_units(n, world) / (e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
                "ms_per_step": round(e_ms, 4), "h2d_bytes_per_step": 2 * n, "d2h_bytes_per_step": 2 * n + 64}
 
     if rank != 0:

@@ -1,0 +1,66 @@
+"""Multi-process host logic of bench.py on CPU (gloo, world size 2): the job
+time is the slowest rank's, the job's value counts every rank's replica, and
+the CPU reference arm runs on rank 0 only."""
+import io
+import os
+import socket
+import sys
+from contextlib import redirect_stdout
+
+import pytest
+import torch
+import torch.distributed as dist
+import torch.multiprocessing as mp
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _free_port() -> int:
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _worker(rank, world, port, out):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank), WORLD_SIZE=str(world),
+                      LOCAL_RANK=str(rank))
+    sys.path.insert(0, ROOT)
+    import bench
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        slowest = bench.max_over_ranks(10.0 + rank)            # rank 1 is slower
+        units = bench.replica_units(1000, world)
+        buf = io.StringIO()
+
+        class A:  # the reference arm's arguments
+            workload, steps, warmup, cpu_blocks = "gauss_block", 1, 0, 1
+        with redirect_stdout(buf):
+            line = bench.run_reference(A)
+        out.put((rank, slowest, units, line is not None))
+        dist.barrier()
+    finally:
+        dist.destroy_process_group()
+
+
+def test_two_rank_timing_and_reference_arm():
+    world = 2
+    ctx = mp.get_context("spawn")
+    q = ctx.SimpleQueue()
+    port = _free_port()
+    procs = [ctx.Process(target=_worker, args=(r, world, port, q)) for r in range(world)]
+    for p in procs:
+        p.start()
+    for p in procs:
+        p.join(timeout=300)
+        assert p.exitcode == 0
+    got = sorted(q.get() for _ in range(world))
+    assert [g[1] for g in got] == [11.0, 11.0]        # max over ranks
+    assert [g[2] for g in got] == [2000, 2000]        # every rank's replica counts
+    assert [g[3] for g in got] == [True, False]       # only rank 0 runs the reference arm
+
+
+def test_single_process_defaults():
+    sys.path.insert(0, ROOT)
+    import bench
+    assert bench.max_over_ranks(3.5) == 3.5
+    assert bench.replica_units(7, 1) == 7

@@ -50,11 +50,12 @@ __global__ void __launch_bounds__(256) k_encode_prologue(const uint16_t *__restr
     // Shift: m = min(n, 4096) samples at floor(k*n/m); histogram of their
     // exponents in the normal range 1..254; lower median.
     constexpr int kPer = LCT_SHIFT_SAMPLES / 256;
-    __shared__ uint32_t hist[256];
+    __shared__ uint32_t hist[8][256];  // one histogram per warp
     __shared__ uint32_t wsum[8];
     __shared__ int32_t median;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    hist[tid] = 0;
+#pragma unroll
+    for (int w = 0; w < 8; ++w) hist[w][tid] = 0;
     if (tid == 0) median = -1;
     __syncthreads();
     const uint64_t n = t.n;
@@ -68,13 +69,19 @@ __global__ void __launch_bounds__(256) k_encode_prologue(const uint16_t *__restr
         const uint64_t at = m == (uint32_t)LCT_SHIFT_SAMPLES ? ((uint64_t)k * n) >> 12 : (uint64_t)k;
         v[i] = k < m ? __ldg(x + at) : 0;
     }
+    // Samples concentrate on a few exponents: lanes holding the same one are
+    // counted together by one lane, into the warp's own histogram.
 #pragma unroll
     for (int i = 0; i < kPer; ++i) {
         const uint32_t e = exp_of(v[i]);
-        if (tid + 256u * i < m && e >= 1 && e <= 254) atomicAdd(&hist[e], 1u);
+        const bool keep = tid + 256u * i < m && e >= 1 && e <= 254;
+        const uint32_t same = __match_any_sync(kFull, keep ? e : 256u);
+        if (keep && lane == __ffs(same) - 1) hist[warp][e] += __popc(same);
     }
     __syncthreads();
-    const uint32_t c = hist[tid];
+    uint32_t c = 0;
+#pragma unroll
+    for (int w = 0; w < 8; ++w) c += hist[w][tid];
     uint32_t inc = c;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {

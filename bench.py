@@ -44,6 +44,9 @@ WORKLOAD_TEXT = {
                 "fused SGD (M ~ Laplace(0,1e-3))",
     "sgd_162m": "162,000,000 BF16 W ~ N(0,0.02), M ~ N(0,1e-3), Gaussian codebooks, CLEAN; step = encode + decode "
                 "+ fused SGD",
+    "momentum_162m": "162,000,000 BF16 W ~ N(0,0.02), M ~ N(0,1e-3), dense BF16 gradient ~ N(0,1e-4), Gaussian "
+                     "codebooks, CLEAN, W and M updated in place; step = one fused SGD-with-momentum step "
+                     "(mu = 0.9, eta = 1e-3)",
 }
 SGD_MOMENTUM = {"gauss_block": ("laplace", 1e-3), "laplace_16m": ("laplace", 1e-3), "heavy_64m": ("laplace", 1e-3), "gelu_act": ("laplace", 1e-3),
                 "sgd_162m": ("gaussian", 1e-3)}
@@ -167,6 +170,8 @@ def run_gpu(args):
     from lossless_bf16_tensor_gb300 import synth
 
     wl = synth.WORKLOADS[args.workload]
+    if "gradient" in wl:
+        return run_gpu_momentum(args, rank, local_rank, world)
     n = wl["n"]
     level = B.LEVELS[wl["level"]]
     x_np = synth.generate(args.workload)
@@ -329,6 +334,121 @@ def run_gpu(args):
     return line
 
 
+def run_gpu_momentum(args, rank, local_rank, world):
+    """One fused SGD-with-momentum step per timed step on compressed W and M
+    (both in place, overflow regions ping-pong between steps)."""
+    import torch
+    import torch.distributed as dist
+    from lossless_bf16_tensor_gb300 import binding as B
+    from lossless_bf16_tensor_gb300 import synth
+
+    wl = synth.WORKLOADS[args.workload]
+    n = wl["n"]
+    level = B.LEVELS[wl["level"]]
+    eta, mu = float(np.float32(wl["eta"])), float(np.float32(wl["mu"]))
+    cbw = B.lct_codebook_build(wl["model"], wl["scale"], wl["shape"])
+    cbm = B.lct_codebook_build(wl["momentum"]["model"], wl["momentum"]["scale"])
+    stream = torch.cuda.current_stream()
+    W = B.CompressedTensor(n, level)
+    M = B.CompressedTensor(n, level)
+    B.lct_encode(torch.from_numpy(synth.generate(args.workload).view(np.int16)).cuda(), cbw, W, stream)
+    B.lct_encode(torch.from_numpy(synth.momentum(args.workload).view(np.int16)).cuda(), cbm, M, stream)
+    grads = [torch.from_numpy(synth.gradient(args.workload, s).view(np.int16)).cuda() for s in (1, 2)]
+    Wb = [W, B.CompressedTensor(n, level, like=W)]
+    Mb = [M, B.CompressedTensor(n, level, like=M)]
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.int32, device="cuda")
+    count = [0]
+
+    def step():
+        k = count[0]
+        B.lct_sgd_momentum_step_fused(Wb[k % 2], cbw, Mb[k % 2], cbm, grads[k % 2], eta, mu,
+                                      Wb[(k + 1) % 2], Mb[(k + 1) % 2], stream)
+        count[0] += 1
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    cur_w, cur_m = Wb[count[0] % 2], Mb[count[0] % 2]
+    assert cur_w.state().status == 0 and cur_m.state().status == 0
+    clocks = ClockSampler(None)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.4)
+    for k in range(args.steps):
+        flush.zero_()
+        evs[k][0].record(stream)
+        step()
+        evs[k][1].record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    clk = clocks.stop()
+    per = [a.elapsed_time(b) for a, b in evs]
+    ms_step = max_over_ranks(sum(per), device="cuda") / args.steps
+    sw, sm_ = Wb[count[0] % 2].state(), Mb[count[0] % 2].state()
+    assert sw.status == 0 and sm_.status == 0
+    sizes = W.sizes
+    # read W, M compressed and the dense gradient; write W, M compressed
+    alg = 2 * algorithmic_bytes(sizes, sw.ovf_used) + 2 * algorithmic_bytes(sizes, sm_.ovf_used) + 2 * n
+    peak, peak_kind = hbm_peak()
+    t_ms = statistics.mean(per)
+    achieved = alg / (t_ms * 1e-3) / 1e9
+    value = replica_units(n, world) / (ms_step * 1e-3) / 1e9
+    traffic = None
+    tpath = os.path.join(ROOT, "profiles", "traffic.json")
+    if os.path.exists(tpath):
+        with open(tpath) as f:
+            entry = json.load(f).get(args.workload, {}).get("momentum")
+        if entry and entry.get("source_hash") == kernel_source_hash():
+            traffic = entry["bytes_per_launch"]
+    if rank != 0:
+        return None
+    cpu = None
+    if not (args.no_cpu_baseline or world > 1):
+        dt, nv = oracle_momentum_time(args.workload, args.cpu_blocks or 256)
+        cpu = {"value": round(nv / dt / 1e9, 5), "unit": "Gelem/s", "cores": 1, "kind": "oracle",
+               "sample": "first %d values of %s, one momentum step; host %s, oracle single-threaded"
+                         % (nv, args.workload, cpu_model()), "seconds": round(dt, 3)}
+    return {
+        "metric": "fused SGD-with-momentum step on compressed W and M: elements per second",
+        "value": round(value, 3), "unit": "Gelem/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_step, 4), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "u32+f32", "data": "synthetic",
+        "config": {"workload": WORKLOAD_TEXT[args.workload], "name": args.workload, "n": n, "level": wl["level"],
+                   "l2": "flushed before every step (256 MiB write, outside the events)",
+                   "parallelism": "replicas" if world > 1 else "single"},
+        "roofline": {"bound": "hbm", "kernel": "momentum", "achieved": round(achieved, 1), "peak": peak,
+                     "peak_kind": peak_kind, "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": traffic,
+                     "algorithmic_bytes_per_launch": alg},
+        "breakdown": {"compression_ratio_all_in_w": round(2.0 * n / (sizes.fixed_bytes + sw.ovf_used), 5),
+                      "compression_ratio_all_in_m": round(2.0 * n / (sizes.fixed_bytes + sm_.ovf_used), 5),
+                      "overflow_bytes_w": int(sw.ovf_used), "overflow_bytes_m": int(sm_.ovf_used)},
+        "clocks": clk, "e2e": None, "gpu_launches": 2 * args.steps, "cpu_baseline": cpu,
+    }
+
+
+def oracle_momentum_time(workload: str, nblocks_sample: int):
+    """Time one oracle momentum step on the first `nblocks_sample` blocks."""
+    import oracle
+    from lossless_bf16_tensor_gb300 import synth
+    wl = synth.WORKLOADS[workload]
+    level = {"CLEAN": 0, "MEDIUM": 1, "HIGH": 2}[wl["level"]]
+    block, _ = oracle.geometry(level)
+    k = min(wl["n"], nblocks_sample * block)
+    w, m = synth.generate(workload, k), synth.momentum(workload, k)
+    g = synth.gradient(workload, 1, k)
+    cbw = oracle.codebook_build(0, wl["scale"])
+    cbm = oracle.codebook_build(0, wl["momentum"]["scale"])
+    W, M = oracle.encode(w, cbw, level), oracle.encode(m, cbm, level)
+    t0 = time.perf_counter()
+    oracle.sgd_momentum_step(W, cbw, M, cbm, g, float(np.float32(wl["eta"])), float(np.float32(wl["mu"])))
+    return time.perf_counter() - t0, k
+
+
 def kernel_source_hash() -> str:
     import hashlib
     h = hashlib.sha256()
@@ -394,6 +514,9 @@ def run_reference(args):
     if rank != 0:
         return None
     base = load_baseline()
+    from lossless_bf16_tensor_gb300 import synth
+    if "gradient" in synth.WORKLOADS[args.workload]:
+        return run_reference_momentum(args, world)
     times, nvals = [], 0
     for _ in range(args.warmup):
         oracle_step_time(args.workload, args.cpu_blocks)
@@ -412,6 +535,26 @@ def run_reference(args):
             "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
                              "sample": sample},
             "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def run_reference_momentum(args, world):
+    for _ in range(args.warmup):
+        oracle_momentum_time(args.workload, args.cpu_blocks)
+    times, nvals = [], 0
+    for _ in range(args.steps):
+        dt, nvals = oracle_momentum_time(args.workload, args.cpu_blocks)
+        times.append(dt)
+    s = sum(times) / len(times)
+    value = nvals / s / 1e9
+    sample = "first %d values of %s per step (%d blocks)" % (nvals, args.workload, args.cpu_blocks)
+    return {"impl": "reference", "metric": "fused SGD-with-momentum step on compressed W and M: elements per second",
+            "value": round(value, 5), "unit": "Gelem/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(s * 1e3, 3), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "u32+f32", "data": "synthetic",
+            "config": {"workload": WORKLOAD_TEXT[args.workload], "name": args.workload},
+            "cpu_baseline": {"value": round(value, 5), "unit": "Gelem/s", "cores": 1, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": round(value, 5), "unit": "Gelem/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
 def main():

@@ -251,6 +251,29 @@ lct_status lct_sgd_step_fused(const lct_tensor *W_in, const lct_codebook *cbW, c
                               const lct_codebook *cbM, float eta, const lct_tensor *W_out,
                               void *stream);
 
+/* One fused SGD-with-momentum step on compressed W and M with a dense BF16
+ * gradient d_g (n values, 16-byte aligned):
+ *   M' = bf16(round(round(mu*m) + g)),   W' = bf16(round(w - round(eta*M')))
+ * The pages name the momentum buffer of SGD with momentum as optimizer state
+ * that LCT keeps compressed ([EXP] "Jargon", entry "Optimizer state"; [ABS])
+ * and ask for a single-pass update of compressed tensors ([EXP] "Training
+ * adds a second problem"); they print no update rule, so this is the
+ * heavy-ball form without dampening or Nesterov term.  Every float32 product
+ * and sum is rounded on its own (no fused multiply-add); the weight step uses
+ * M' as stored (BF16); rounding to BF16 is round-to-nearest-even with
+ * subnormals kept and NaN -> 0x7FC0.  W' is coded with cbW and W_in's stored
+ * shift, M' with cbM and M_in's stored shift.
+ * All four tensors must have the same n and level.  Each output may share
+ * d_header, d_sf, d_slots, d_markers and d_blk_off with its own input (in
+ * place) but not partly overlap them; its d_ovf and d_work must be apart from
+ * every input region; W' and M' must not overlap each other, W' must not
+ * overlap M_in, M' must not overlap W_in, and d_g must not overlap either
+ * output.  Each output latches its own status (capacity, corrupt input,
+ * timeout); a corrupt input or a timeout is latched in both. */
+lct_status lct_sgd_momentum_step_fused(const lct_tensor *W_in, const lct_codebook *cbW, const lct_tensor *M_in,
+                                       const lct_codebook *cbM, const uint16_t *d_g, float eta, float mu,
+                                       const lct_tensor *W_out, const lct_tensor *M_out, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -5,7 +5,8 @@ The work happens in ``liblct.so`` (CUDA kernels behind a C ABI, declared in
 ``include/lct.h``); ``binding`` is its thin ctypes binding, re-exported here:
 
     from lossless_bf16_tensor_gb300 import (lct_codebook_build, lct_encode, lct_decode,
-                                            lct_sgd_step_fused, lct_compressed_size,
+                                            lct_sgd_step_fused, lct_sgd_momentum_step_fused,
+                                            lct_compressed_size,
                                             CompressedTensor)
 
 The binding is loaded on first attribute access and raises if the library is
@@ -13,6 +14,7 @@ not built; nothing falls back to the CPU.
 """
 
 _BINDING_NAMES = {"lct_codebook_build", "lct_encode", "lct_decode", "lct_sgd_step_fused",
+                  "lct_sgd_momentum_step_fused", "lct_encode_static_scratch",
                   "lct_compressed_size", "lct_debug_wait_timeout", "CompressedTensor", "LctError",
                   "library"}
 

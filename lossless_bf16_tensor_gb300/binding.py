@@ -80,10 +80,14 @@ _lib.lct_decode.argtypes = [ctypes.POINTER(lct_tensor), ctypes.POINTER(lct_codeb
 _lib.lct_sgd_step_fused.argtypes = [ctypes.POINTER(lct_tensor), ctypes.POINTER(lct_codebook),
                                     ctypes.POINTER(lct_tensor), ctypes.POINTER(lct_codebook), ctypes.c_float,
                                     ctypes.POINTER(lct_tensor), _P]
+_lib.lct_sgd_momentum_step_fused.argtypes = [ctypes.POINTER(lct_tensor), ctypes.POINTER(lct_codebook),
+                                             ctypes.POINTER(lct_tensor), ctypes.POINTER(lct_codebook), _P,
+                                             ctypes.c_float, ctypes.c_float, ctypes.POINTER(lct_tensor),
+                                             ctypes.POINTER(lct_tensor), _P]
 _lib.lct_debug_wait_timeout.argtypes = [_P, _P, ctypes.c_uint64, _P]
 _lib.lct_encode_static_scratch.argtypes = [_P, ctypes.POINTER(lct_codebook), ctypes.POINTER(lct_tensor), _P]
 for _fn in ("lct_codebook_build", "lct_compressed_size", "lct_encode", "lct_decode", "lct_sgd_step_fused",
-            "lct_debug_wait_timeout", "lct_encode_static_scratch"):
+            "lct_sgd_momentum_step_fused", "lct_debug_wait_timeout", "lct_encode_static_scratch"):
     getattr(_lib, _fn).restype = ctypes.c_int
 
 
@@ -159,6 +163,16 @@ def lct_sgd_step_fused(W_in: "CompressedTensor", cbW: lct_codebook, M: "Compress
     _check(_lib.lct_sgd_step_fused(ctypes.byref(W_in.desc), ctypes.byref(cbW), ctypes.byref(M.desc),
                                    ctypes.byref(cbM), ctypes.c_float(eta), ctypes.byref(W_out.desc),
                                    _stream(stream)), "lct_sgd_step_fused")
+
+
+def lct_sgd_momentum_step_fused(W_in: "CompressedTensor", cbW: lct_codebook, M_in: "CompressedTensor",
+                                cbM: lct_codebook, g: torch.Tensor, eta: float, mu: float,
+                                W_out: "CompressedTensor", M_out: "CompressedTensor", stream=None) -> None:
+    ptr = _dev_ptr(g, W_in.n) if W_in.n else None
+    _check(_lib.lct_sgd_momentum_step_fused(ctypes.byref(W_in.desc), ctypes.byref(cbW), ctypes.byref(M_in.desc),
+                                            ctypes.byref(cbM), ptr, ctypes.c_float(eta), ctypes.c_float(mu),
+                                            ctypes.byref(W_out.desc), ctypes.byref(M_out.desc), _stream(stream)),
+           "lct_sgd_momentum_step_fused")
 
 
 def lct_debug_wait_timeout(header: torch.Tensor, work: torch.Tensor, limit_ns: int, stream=None) -> None:

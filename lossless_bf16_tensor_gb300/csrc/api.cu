@@ -230,6 +230,67 @@ extern "C" lct_status lct_sgd_step_fused(const lct_tensor *W_in, const lct_codeb
     return launch_sgd(a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? LCT_OK : LCT_ERR_CUDA;
 }
 
+extern "C" lct_status lct_sgd_momentum_step_fused(const lct_tensor *W_in, const lct_codebook *cbW,
+                                                  const lct_tensor *M_in, const lct_codebook *cbM,
+                                                  const uint16_t *d_g, float eta, float mu, const lct_tensor *W_out,
+                                                  const lct_tensor *M_out, void *stream)
+{
+    lct_sizes sw, sm, sow, som;
+    lct_status rc;
+    if ((rc = check_tensor(W_in, false, &sw)) != LCT_OK) return rc;
+    if ((rc = check_tensor(M_in, false, &sm)) != LCT_OK) return rc;
+    if ((rc = check_tensor(W_out, true, &sow)) != LCT_OK) return rc;
+    if ((rc = check_tensor(M_out, true, &som)) != LCT_OK) return rc;
+    if (!cbW || !cbM || !codebook_valid(*cbW) || !codebook_valid(*cbM)) return LCT_ERR_INVALID_ARG;
+    const uint64_t n = W_in->n;
+    if (M_in->n != n || W_out->n != n || M_out->n != n) return LCT_ERR_INVALID_ARG;
+    if (M_in->level != W_in->level || W_out->level != W_in->level || M_out->level != W_in->level)
+        return LCT_ERR_UNSUPPORTED;
+    if (n > 0 && (!d_g || !aligned16(d_g))) return LCT_ERR_INVALID_ARG;
+    Range rw[7], rm[7], row_[7], rom[7];
+    regions(W_in, sw, rw);
+    regions(M_in, sm, rm);
+    regions(W_out, sow, row_);
+    regions(M_out, som, rom);
+    if (n > 0) {
+        const Range rg = range_of(d_g, 2 * n);
+        // an output against the other input, the other output and the gradient
+        for (int i = 0; i < 7; ++i) {
+            if (overlap(row_[i], rg) || overlap(rom[i], rg)) return LCT_ERR_INVALID_ARG;
+            for (int k = 0; k < 7; ++k) {
+                if (overlap(row_[i], rom[k])) return LCT_ERR_INVALID_ARG;
+                if (k < 6 && (overlap(row_[i], rm[k]) || overlap(rom[i], rw[k]))) return LCT_ERR_INVALID_ARG;
+            }
+        }
+        // an output against its own input: overflow and scratch apart from
+        // every input region; the others the same region or disjoint
+        const Range *outs[2] = {row_, rom}, *ins[2] = {rw, rm};
+        for (int o = 0; o < 2; ++o) {
+            for (int k = 0; k < 6; ++k)
+                if (overlap(outs[o][5], ins[o][k]) || overlap(outs[o][6], ins[o][k])) return LCT_ERR_INVALID_ARG;
+            for (int i = 0; i < 5; ++i)
+                for (int k = 0; k < 6; ++k) {
+                    const bool same = i == k && outs[o][i].lo == ins[o][k].lo;
+                    if (!same && overlap(outs[o][i], ins[o][k])) return LCT_ERR_INVALID_ARG;
+                }
+        }
+    }
+    MomentumArgs a;
+    a.w_in = dev_view(W_in, sw);
+    a.m_in = dev_view(M_in, sm);
+    a.w_out = dev_view(W_out, sow);
+    a.m_out = dev_view(M_out, som);
+    a.g = d_g;
+    a.cbw = dev_codebook(*cbW);
+    a.cbm = dev_codebook(*cbM);
+    a.eta = eta;
+    a.mu = mu;
+    a.in_place = (W_out->d_sf == W_in->d_sf || M_out->d_sf == M_in->d_sf) ? 1u : 0u;
+    a.pad = 0;
+    a.wait_ns = kDefaultWaitNs;
+    return launch_momentum(a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? LCT_OK : LCT_ERR_CUDA;
+}
+
 // ------------------------------------------------------------ test hook
 
 namespace lct {

@@ -193,6 +193,18 @@ __device__ __forceinline__ uint32_t join_one(uint32_t sf, uint32_t e)
     return ((sf * 0x101u) & 0x807Fu) | (e & 0xFFFF7F80u);
 }
 
+// float32 -> BF16 (bits 0..15), round to nearest even, subnormals kept.  The
+// conversion writes NaN as 0x7FFF; this library's NaN is 0x7FC0.
+__device__ __forceinline__ uint32_t bf16_rne(float r)
+{
+    uint16_t h;
+    asm("cvt.rn.bf16.f32 %0, %1;" : "=h"(h) : "f"(r));
+    return h == 0x7FFFu ? 0x7FC0u : (uint32_t)h;
+}
+
+// BF16 in bits 0..15 -> float32 (exact).
+__device__ __forceinline__ float bf16_f(uint32_t h) { return __uint_as_float(h << 16); }
+
 // ------------------------------------------------------------- scans
 
 // Exclusive scan of one value per thread over `group_warps` warps starting at
@@ -240,6 +252,12 @@ __device__ __forceinline__ void mbar_expect_tx(uint64_t *bar, uint32_t bytes)
 {
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)), "r"(bytes)
                  : "memory");
+}
+
+// One arrival (consumer release of a ring slot).
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar)
+{
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
 }
 
 __device__ __forceinline__ bool mbar_try(uint64_t *bar, uint32_t parity)

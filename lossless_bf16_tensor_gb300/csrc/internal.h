@@ -85,9 +85,20 @@ struct SgdArgs {
     uint64_t wait_ns;
 };
 
+struct MomentumArgs {
+    DevTensor w_in, m_in, w_out, m_out;
+    const uint16_t *g;  // dense BF16 gradient, n values
+    DevCodebook cbw, cbm;
+    float eta, mu;
+    uint32_t in_place;  // an output shares its input's sign-fraction bytes
+    uint32_t pad;
+    uint64_t wait_ns;
+};
+
 cudaError_t launch_encode(const EncodeArgs &a, cudaStream_t s);
 cudaError_t launch_decode(const DecodeArgs &a, cudaStream_t s);
 cudaError_t launch_sgd(const SgdArgs &a, cudaStream_t s);
+cudaError_t launch_momentum(const MomentumArgs &a, cudaStream_t s);
 cudaError_t launch_wait_probe(lct_header *hdr, unsigned long long *work, uint64_t wait_ns,
                               cudaStream_t s);
 

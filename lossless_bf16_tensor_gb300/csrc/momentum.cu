@@ -1,0 +1,427 @@
+// Fused compressed SGD-with-momentum step of liblct:
+//   M <- bf16(mu*M + g),  W <- bf16(W - eta*M)
+//
+// [EXP] "Jargon", entry "Optimizer state": the momentum buffer of SGD with
+// momentum is the optimizer state the pages have in mind; [ABS]: optimizer
+// states are stored compressed; [EXP] "Training adds a second problem": the
+// update reads the compressed tensors and writes them back compressed in one
+// pass instead of a decode / update / encode round trip through HBM.  The
+// update rule is a reading (heavy ball, no dampening, no Nesterov term); every
+// float32 operation is rounded on its own and the weight step uses the new
+// momentum as stored, in BF16.  Each output keeps its input's codebook and
+// stored shift.
+//
+// Thread j of a block's CTA owns stream j of W, M and of both outputs.  The
+// input slot images come in by TMA bulk copy; the two sign-fraction byte
+// arrays and the dense BF16 gradient stream through a ring of row chunks.
+// Each output's codes are appended straight into its slot words in global
+// memory (there is no shared-memory output image), which leaves room for the
+// spilled new exponents of both outputs.  Spilled exponents are kept for 32
+// rows per output (every row when an output is updated in place); an
+// out-of-place step whose stream spills more than that recomputes the older
+// rows of that stream at the end.
+#include "codec_dev.cuh"
+
+namespace lct {
+namespace dev {
+
+constexpr int kMomThreads = 256;
+constexpr int kMomRows = 8;     // rows per chunk
+constexpr int kMomRing = 3;     // chunks in flight
+constexpr int kMomSpill = 32;   // spilled new-exponent rows kept per output (out of place)
+
+// One element: w, m, g as BF16 in bits 0..15.  *mo = bf16(fl32(fl32(mu*m) +
+// g)); returns bf16(fl32(w - fl32(eta * mo))).
+__device__ __forceinline__ uint32_t momentum_one(uint32_t w, uint32_t m, uint32_t g, float eta, float mu,
+                                                 uint32_t *mo)
+{
+    const uint32_t mn = bf16_rne(__fadd_rn(__fmul_rn(mu, bf16_f(m)), bf16_f(g)));
+    *mo = mn;
+    return bf16_rne(__fsub_rn(bf16_f(w), __fmul_rn(eta, bf16_f(mn))));
+}
+
+template <int LEVEL, bool INPLACE>
+struct MomSmem {
+    static constexpr int W = Geo<LEVEL>::W, NJ = Geo<LEVEL>::NJ;
+    static constexpr int kSpillRows = INPLACE ? NJ : kMomSpill;
+    static constexpr int kSlotIn = (W + 1) * kStreams * 4;        // + zero guard row
+    static constexpr int kChunk = kMomRows * kStreams * 4;        // sf W, sf M, 2-byte g
+    static constexpr int kRing = kMomRing * kChunk;
+    static constexpr int kLuts = 2 * 256 * 4 + 2 * 256 * 8;
+    static constexpr int kSpill = (kSpillRows * kRow + 127) / 128 * 128;  // per output
+    static constexpr int kBytes = 2 * kSlotIn + kRing + kLuts + 2 * kSpill;
+    static_assert(kBytes <= 227 * 1024, "shared memory of one CTA");
+};
+
+// Prologue: both output headers (shift and codebook carried over from the
+// matching input, status cleared but inheriting an error already latched in
+// W or M, or CORRUPT if either input header is not valid) and cleared
+// look-back words of both outputs.  Every input header field is read before
+// any output header is written, since an output header may be its input's.
+__global__ void __launch_bounds__(256) k_momentum_prologue(DevTensor w_in, DevTensor m_in, DevTensor w_out,
+                                                            DevTensor m_out, uint32_t hash_w, uint32_t hash_m)
+{
+    pdl_wait();
+    pdl_launch_dependents();
+    for (uint64_t i = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x; i < w_out.nblocks;
+         i += (uint64_t)gridDim.x * blockDim.x) {
+        w_out.work[i] = 0ull;
+        m_out.work[i] = 0ull;
+    }
+    if (blockIdx.x == 0 && threadIdx.x == 0) {
+        const lct_header *hw = w_in.hdr;
+        const lct_header *hm = m_in.hdr;
+        uint32_t st = hw->status ? hw->status : hm->status;
+        const bool ok_w = hw->magic == LCT_MAGIC && hw->n == w_in.n && hw->level == w_in.level && hw->cb_hash == hash_w;
+        const bool ok_m = hm->magic == LCT_MAGIC && hm->n == m_in.n && hm->level == m_in.level && hm->cb_hash == hash_m;
+        if (!st && !(ok_w && ok_m)) st = LCT_ERR_CORRUPT;
+        const int32_t delta_w = hw->delta, delta_m = hm->delta;
+        const DevTensor *outs[2] = {&w_out, &m_out};
+        const int32_t deltas[2] = {delta_w, delta_m};
+        const uint32_t hashes[2] = {hash_w, hash_m};
+        for (int o = 0; o < 2; ++o) {
+            lct_header *h = outs[o]->hdr;
+            h->magic = LCT_MAGIC;
+            h->version = 1;
+            h->n = outs[o]->n;
+            h->level = outs[o]->level;
+            h->delta = deltas[o];
+            h->status = st;
+            h->cb_hash = hashes[o];
+            h->ovf_used = 0;
+            h->ovf_cap = outs[o]->ovf_cap;
+        }
+    }
+}
+
+// One stream of one compressed input inside the kernel.
+struct MomIn {
+    uint32_t pos;         // bit position in the slot
+    const uint32_t *col;  // slot image column in shared memory
+    uint32_t marker;
+    uint64_t ovf_at;      // overflow index of spilled symbol k is ovf_at + k
+};
+
+template <int W>
+__device__ __forceinline__ uint32_t mom_take(MomIn &s, uint32_t k, const uint32_t *lut, const uint8_t *ovf, bool ovf_ok)
+{
+    if (k < s.marker) return rd_take<W>(s.pos, s.col, lut);
+    return ovf_ok ? (uint32_t)__ldg(ovf + s.ovf_at + k) << 7 : 0u;
+}
+
+// Appends one chunk's R new exponents of one output to its stream: without
+// per-code checks when every stream of the warp has room for the whole
+// chunk, else one checked append per code (a spilled exponent goes to the
+// staging ring).
+template <int R, int SP>
+__device__ __forceinline__ void mom_put_chunk(Writer &wo, const uint32_t (&h)[R], const uint2 *__restrict__ tbl,
+                                              uint32_t k0, uint32_t *__restrict__ col, uint8_t *__restrict__ stage)
+{
+    uint2 ent[R];
+    uint32_t need = 0;
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+        ent[r] = tbl[exp_of(h[r])];
+        need += ent[r].y;
+    }
+    if (__all_sync(kFull, wo.alive && need <= wo.rem)) {
+#pragma unroll
+        for (int r = 0; r < R; r += 2) {  // two codes fit the accumulator, then one flush
+            wr_add(wo, ent[r]);
+            wr_add(wo, ent[r + 1]);
+            wr_flush(wo, col);
+        }
+        wo.rem -= need;
+    } else {
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+            const uint32_t k = k0 + r;
+            if (wr_put_checked(wo, ent[r], k, col)) stage[(k % SP) * kRow] = (uint8_t)exp_of(h[r]);
+        }
+    }
+}
+
+template <int LEVEL, bool INPLACE>
+__global__ void __launch_bounds__(kMomThreads, INPLACE ? 1 : 2) k_momentum(const __grid_constant__ MomentumArgs a)
+{
+    using G = Geo<LEVEL>;
+    using L = MomSmem<LEVEL, INPLACE>;
+    constexpr int W = G::W, R = kMomRows, S = kMomRing, SP = L::kSpillRows;
+    constexpr int NW = kMomThreads / 32;
+    constexpr int kRowsB = R * kStreams;  // bytes of one sign-fraction chunk
+    extern __shared__ __align__(128) uint8_t smem[];
+    uint32_t *slotW = reinterpret_cast<uint32_t *>(smem);
+    uint32_t *slotM = reinterpret_cast<uint32_t *>(smem + L::kSlotIn);
+    uint8_t *ring = smem + 2 * L::kSlotIn;  // per chunk: sf W | sf M | g
+    uint32_t *lutW = reinterpret_cast<uint32_t *>(ring + L::kRing);
+    uint32_t *lutM = lutW + 256;
+    uint2 *tblW = reinterpret_cast<uint2 *>(lutM + 256);
+    uint2 *tblM = tblW + 256;
+    uint8_t *stageW = reinterpret_cast<uint8_t *>(tblM + 256);
+    uint8_t *stageM = stageW + L::kSpill;
+    __shared__ __align__(8) uint64_t bar_slot, bar_in[S];
+    __shared__ uint32_t warp_tot[NW];
+    __shared__ unsigned long long s_excl[2];
+    __shared__ uint32_t s_flags;  // bit 0: a wait gave up, bit 1: corrupt input
+
+    const int j = threadIdx.x, lane = j & 31, warp = j >> 5;
+    const uint32_t b = blockIdx.x;
+    const uint64_t base = (uint64_t)b * G::B;
+    const uint32_t nb = (uint32_t)min((uint64_t)G::B, a.w_in.n - base);
+    const uint32_t nrows = (nb + 255) >> 8, nbulk = (nb >> 8) / R, nchunks = (nrows + R - 1) / R;
+    const uint64_t limit = a.wait_ns;
+
+    if (j == 0) {
+        mbar_init(&bar_slot, 1);
+        for (int s = 0; s < S; ++s) mbar_init(&bar_in[s], 1);
+        fence_mbar_init();
+        s_flags = 0;
+    }
+    // inputs, the new headers and the cleared look-back words are all ready
+    pdl_wait();
+    const lct_header *hw = a.w_in.hdr, *hm = a.m_in.hdr;
+    bool bad = !(hw->magic == LCT_MAGIC && hw->n == a.w_in.n && hw->level == LEVEL && hw->cb_hash == a.cbw.hash) ||
+               !(hm->magic == LCT_MAGIC && hm->n == a.m_in.n && hm->level == LEVEL && hm->cb_hash == a.cbm.hash);
+    const int delta_w = a.w_out.hdr->delta, delta_m = a.m_out.hdr->delta;  // copied by the prologue
+    lutW[j] = dec_entry(a.cbw, delta_w, j);
+    lutM[j] = dec_entry(a.cbm, delta_m, j);
+    tblW[j] = enc_entry(a.cbw, delta_w, j);
+    tblM[j] = enc_entry(a.cbm, delta_m, j);
+    slotW[W * kStreams + j] = 0u;
+    slotM[W * kStreams + j] = 0u;
+    __syncthreads();  // barriers initialised
+    auto issue = [&](uint32_t c) {
+        uint8_t *dst = ring + (c % S) * L::kChunk;
+        const uint64_t at = base + (uint64_t)c * kRowsB;
+        mbar_expect_tx(&bar_in[c % S], L::kChunk);
+        bulk_load(dst, a.w_in.sf + at, kRowsB, &bar_in[c % S]);
+        bulk_load(dst + kRowsB, a.m_in.sf + at, kRowsB, &bar_in[c % S]);
+        bulk_load(dst + 2 * kRowsB, a.g + at, 2 * kRowsB, &bar_in[c % S]);
+    };
+    if (j == 0) {
+        mbar_expect_tx(&bar_slot, 2 * W * kStreams * 4);
+        bulk_load(slotW, a.w_in.slots + (uint64_t)b * W * kStreams, W * kStreams * 4, &bar_slot);
+        bulk_load(slotM, a.m_in.slots + (uint64_t)b * W * kStreams, W * kStreams * 4, &bar_slot);
+        for (uint32_t c = 0; c < (uint32_t)S && c < nbulk; ++c) issue(c);
+    }
+
+    // input markers, spill prefixes and overflow ranges
+    const uint32_t nj = nb > (uint32_t)j ? (nb - j + 255) / 256 : 0;
+    MomIn sw, sm;
+    sw.col = slotW + j;
+    sm.col = slotM + j;
+    {
+        const uint32_t mw = a.w_in.markers[(uint64_t)b * kStreams + j], mm = a.m_in.markers[(uint64_t)b * kStreams + j];
+        bad |= mw > nj || mm > nj;
+        sw.marker = min(mw, nj);
+        sm.marker = min(mm, nj);
+    }
+    bool ovf_ok_w, ovf_ok_m;
+    {
+        uint32_t tot_w, tot_m;
+        const uint32_t pre_w = group_exclusive_scan(nj - sw.marker, warp_tot, NW, 0, &tot_w);
+        const uint32_t pre_m = group_exclusive_scan(nj - sm.marker, warp_tot, NW, 0, &tot_m);
+        const uint64_t a0 = a.w_in.blk_off[b], a1 = a.w_in.blk_off[b + 1];
+        const uint64_t c0 = a.m_in.blk_off[b], c1 = a.m_in.blk_off[b + 1];
+        ovf_ok_w = a1 <= a.w_in.ovf_cap && a0 <= a1 && a1 - a0 == tot_w;
+        ovf_ok_m = c1 <= a.m_in.ovf_cap && c0 <= c1 && c1 - c0 == tot_m;
+        sw.ovf_at = a0 + pre_w - sw.marker;
+        sm.ovf_at = c0 + pre_m - sm.marker;
+        bad |= !ovf_ok_w || !ovf_ok_m;
+    }
+    const uint8_t *ovf_w = a.w_in.ovf, *ovf_m = a.m_in.ovf;
+
+    if (!mbar_wait(&bar_slot, 0, limit)) s_flags = 1;
+    sw.pos = 0;
+    sm.pos = 0;
+    Writer ow, om;
+    wr_init<W>(ow, nj);
+    wr_init<W>(om, nj);
+    uint32_t *colW = a.w_out.slots + (uint64_t)b * W * kStreams + j;
+    uint32_t *colM = a.m_out.slots + (uint64_t)b * W * kStreams + j;
+    uint8_t *sfWj = a.w_out.sf + base + j;
+    uint8_t *sfMj = a.m_out.sf + base + j;
+    const float eta = a.eta, mu = a.mu;
+
+    for (uint32_t c = 0; c < nchunks; ++c) {
+        const bool bulk = c < nbulk;
+        const uint32_t slot = c % S;
+        if (bulk && !mbar_wait(&bar_in[slot], (c / S) & 1u, (s_flags & 1u) ? 1000000ull : limit)) s_flags = 1;
+        const uint8_t *chunk = ring + slot * L::kChunk;
+        const uint8_t *sfwc = chunk + j;
+        const uint8_t *sfmc = chunk + kRowsB + j;
+        const uint16_t *gc = reinterpret_cast<const uint16_t *>(chunk + 2 * kRowsB) + j;
+        const uint64_t row0 = (uint64_t)c * kRowsB;
+        const uint32_t k0 = c * R, kend = k0 + R;
+        if (bulk && __all_sync(kFull, sw.marker >= kend && sm.marker >= kend)) {
+            // loads first (both decode chains, the chunk's bytes), stores last
+            uint32_t hW[R], hM[R];
+            {
+                uint32_t ew[R], em[R];
+#pragma unroll
+                for (int r = 0; r < R; ++r) {
+                    ew[r] = rd_take<W>(sw.pos, sw.col, lutW);
+                    em[r] = rd_take<W>(sm.pos, sm.col, lutM);
+                }
+#pragma unroll
+                for (int r = 0; r < R; ++r)
+                    hW[r] = momentum_one(join_one(sfwc[r * kStreams], ew[r]), join_one(sfmc[r * kStreams], em[r]),
+                                         gc[r * kStreams], eta, mu, &hM[r]);
+            }
+#pragma unroll
+            for (int r = 0; r < R; ++r) {
+                sfWj[row0 + r * kStreams] = sf_of(hW[r]);
+                sfMj[row0 + r * kStreams] = sf_of(hM[r]);
+            }
+            mom_put_chunk<R, SP>(ow, hW, tblW, k0, colW, stageW + j);
+            mom_put_chunk<R, SP>(om, hM, tblM, k0, colM, stageM + j);
+        } else {
+            for (int r = 0; r < R; ++r) {
+                const uint32_t k = k0 + r;
+                if (k >= nj) break;
+                const uint32_t ew = mom_take<W>(sw, k, lutW, ovf_w, ovf_ok_w);
+                const uint32_t em = mom_take<W>(sm, k, lutM, ovf_m, ovf_ok_m);
+                const uint64_t at = base + (uint64_t)k * kStreams + j;
+                const uint32_t fw = bulk ? sfwc[r * kStreams] : a.w_in.sf[at];
+                const uint32_t fm = bulk ? sfmc[r * kStreams] : a.m_in.sf[at];
+                const uint32_t gv = bulk ? gc[r * kStreams] : a.g[at];
+                uint32_t hMo;
+                const uint32_t hWo = momentum_one(join_one(fw, ew), join_one(fm, em), gv, eta, mu, &hMo);
+                const uint32_t eW = exp_of(hWo), eM = exp_of(hMo);
+                sfWj[row0 + r * kStreams] = sf_of(hWo);
+                sfMj[row0 + r * kStreams] = sf_of(hMo);
+                if (wr_put_checked(ow, tblW[eW], k, colW)) stageW[(k % SP) * kRow + j] = (uint8_t)eW;
+                if (wr_put_checked(om, tblM[eM], k, colM)) stageM[(k % SP) * kRow + j] = (uint8_t)eM;
+            }
+        }
+        __syncthreads();  // every thread is done with this chunk's ring slot
+        if (j == 0 && c + S < nbulk) issue(c + S);
+    }
+    bad |= sw.pos > 32u * W || sm.pos > 32u * W;
+    if (bad) atomicOr(&s_flags, 2u);
+    wr_finish<W>(ow, colW);
+    wr_finish<W>(om, colM);
+    const uint32_t mk_w = ow.marker, sp_w = nj - mk_w;
+    const uint32_t mk_m = om.marker, sp_m = nj - mk_m;
+    uint32_t tot_w, tot_m;
+    const uint32_t pre_w = group_exclusive_scan(sp_w, warp_tot, NW, 0, &tot_w);
+    const uint32_t pre_m = group_exclusive_scan(sp_m, warp_tot, NW, 0, &tot_m);
+    a.w_out.markers[(uint64_t)b * kStreams + j] = (uint16_t)mk_w;
+    a.m_out.markers[(uint64_t)b * kStreams + j] = (uint16_t)mk_m;
+
+    // warp 0 places W's overflow bytes, warp 1 places M's
+    if (warp < 2) {
+        const DevTensor &t = warp == 0 ? a.w_out : a.m_out;
+        const uint32_t total = warp == 0 ? tot_w : tot_m;
+        bool timed_out;
+        const unsigned long long excl = warp_lookback(t.work, b, total, limit, &timed_out);
+        if (lane == 0) {
+            if (s_flags & 2u) latch(t.hdr, LCT_ERR_CORRUPT);
+            if (timed_out || (s_flags & 1u)) latch(t.hdr, LCT_ERR_TIMEOUT);
+            t.blk_off[b] = excl;
+            if (b == t.nblocks - 1) {
+                t.blk_off[b + 1] = excl + total;
+                t.hdr->ovf_used = excl + total;
+            }
+            if (excl + total > t.ovf_cap) latch(t.hdr, LCT_ERR_OVERFLOW_CAPACITY);
+            s_excl[warp] = excl;
+        }
+    }
+    __syncthreads();
+
+    const unsigned long long excl_w = s_excl[0], excl_m = s_excl[1];
+    const bool room_w = tot_w > 0 && excl_w + tot_w <= a.w_out.ovf_cap;
+    const bool room_m = tot_m > 0 && excl_m + tot_m <= a.m_out.ovf_cap;
+    uint8_t *out_w = a.w_out.ovf + excl_w;
+    uint8_t *out_m = a.m_out.ovf + excl_m;
+    // spilled rows still kept in shared memory: one warp per stream at a time
+    for (int i = 0; i < 32; ++i) {
+        const uint32_t sj = (uint32_t)(warp * 32 + i);
+        if (room_w) {
+            const uint32_t smk = __shfl_sync(kFull, mk_w, i), ssp = __shfl_sync(kFull, sp_w, i);
+            const uint32_t spr = __shfl_sync(kFull, pre_w, i);
+            const uint32_t kept_from = smk + ssp > (uint32_t)SP ? smk + ssp - SP : 0u;
+            for (uint32_t l = lane; l < ssp; l += 32) {
+                const uint32_t k = smk + l;
+                if (k >= kept_from) out_w[spr + l] = stageW[(k % SP) * kRow + sj];
+            }
+        }
+        if (room_m) {
+            const uint32_t smk = __shfl_sync(kFull, mk_m, i), ssp = __shfl_sync(kFull, sp_m, i);
+            const uint32_t spr = __shfl_sync(kFull, pre_m, i);
+            const uint32_t kept_from = smk + ssp > (uint32_t)SP ? smk + ssp - SP : 0u;
+            for (uint32_t l = lane; l < ssp; l += 32) {
+                const uint32_t k = smk + l;
+                if (k >= kept_from) out_m[spr + l] = stageM[(k % SP) * kRow + sj];
+            }
+        }
+    }
+    if (!INPLACE) {
+        const uint32_t kept_from = nj > (uint32_t)SP ? nj - SP : 0u;
+        const bool redo_w = room_w && mk_w < kept_from, redo_m = room_m && mk_m < kept_from;
+        if (redo_w || redo_m) {
+            // This stream spilled past the kept rows: decode its W and M again
+            // from the slot images (still in shared memory) and recompute the
+            // older spilled exponents.  The input sign-fraction bytes are
+            // intact because the step is out of place.
+            MomIn rw = sw, rm = sm;
+            rw.pos = 0;
+            rm.pos = 0;
+            const uint32_t first = min(redo_w ? mk_w : kept_from, redo_m ? mk_m : kept_from);
+            for (uint32_t k = 0; k < kept_from; ++k) {
+                const uint32_t ew = mom_take<W>(rw, k, lutW, ovf_w, ovf_ok_w);
+                const uint32_t em = mom_take<W>(rm, k, lutM, ovf_m, ovf_ok_m);
+                if (k < first) continue;
+                const uint64_t at = base + (uint64_t)k * kStreams + j;
+                uint32_t hMo;
+                const uint32_t hWo = momentum_one(join_one(a.w_in.sf[at], ew), join_one(a.m_in.sf[at], em), a.g[at],
+                                                  eta, mu, &hMo);
+                if (redo_w && k >= mk_w) out_w[pre_w + (k - mk_w)] = exp_of(hWo);
+                if (redo_m && k >= mk_m) out_m[pre_m + (k - mk_m)] = exp_of(hMo);
+            }
+        }
+    }
+    pdl_launch_dependents();
+    if (j == 0 && (s_flags & 1u)) {
+        // a wait gave up: let every copy still in flight land before the CTA
+        // (and its shared memory) goes away
+        mbar_wait(&bar_slot, 0, limit);
+        for (uint32_t s = 0; s < (uint32_t)S && s < nbulk; ++s) {
+            const uint32_t last = s + (nbulk - 1 - s) / S * S;
+            mbar_wait(&bar_in[s], (last / S) & 1u, limit);
+        }
+    }
+}
+
+template <int LEVEL, bool INPLACE>
+cudaError_t launch_level(const MomentumArgs &a, cudaStream_t s)
+{
+    constexpr int smem = MomSmem<LEVEL, INPLACE>::kBytes;
+    cudaError_t err =
+        cudaFuncSetAttribute(k_momentum<LEVEL, INPLACE>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (err != cudaSuccess) return err;
+    return launch_pdl(k_momentum<LEVEL, INPLACE>, dim3(a.w_out.nblocks), dim3(kMomThreads), smem, s, a);
+}
+
+template <int LEVEL>
+cudaError_t launch_momentum_level(const MomentumArgs &a, cudaStream_t s)
+{
+    return a.in_place ? launch_level<LEVEL, true>(a, s) : launch_level<LEVEL, false>(a, s);
+}
+
+}  // namespace dev
+
+cudaError_t launch_momentum(const MomentumArgs &a, cudaStream_t s)
+{
+    const uint32_t zero_ctas = 1 + a.w_out.nblocks / 8192;
+    cudaError_t err = dev::launch_pdl(dev::k_momentum_prologue, dim3(zero_ctas < 64 ? zero_ctas : 64), dim3(256), 0,
+                                      s, a.w_in, a.m_in, a.w_out, a.m_out, a.cbw.hash, a.cbm.hash);
+    if (err != cudaSuccess || a.w_out.nblocks == 0) return err;
+    switch (a.w_out.level) {
+    case LCT_LEVEL_CLEAN: return dev::launch_momentum_level<LCT_LEVEL_CLEAN>(a, s);
+    case LCT_LEVEL_MEDIUM: return dev::launch_momentum_level<LCT_LEVEL_MEDIUM>(a, s);
+    default: return dev::launch_momentum_level<LCT_LEVEL_HIGH>(a, s);
+    }
+}
+
+}  // namespace lct

@@ -25,15 +25,6 @@ constexpr int kSgdRows = 8;    // rows per sign-fraction chunk
 constexpr int kSgdRing = 3;    // chunks in flight
 constexpr int kSgdSpill = 64;  // spilled new-exponent rows kept (out of place)
 
-// float32 -> BF16 (bits 0..15), round to nearest even, subnormals kept.  The
-// conversion writes NaN as 0x7FFF; this library's NaN is 0x7FC0.
-__device__ __forceinline__ uint32_t bf16_rne(float r)
-{
-    uint16_t h;
-    asm("cvt.rn.bf16.f32 %0, %1;" : "=h"(h) : "f"(r));
-    return h == 0x7FFFu ? 0x7FC0u : (uint32_t)h;
-}
-
 // One value of W and one of M (BF16 in bits 0..15) -> the updated BF16:
 // fl32(w - fl32(eta*m)), product and difference rounded separately.
 __device__ __forceinline__ uint32_t sgd_one(uint32_t w, uint32_t m, float eta)

@@ -17,6 +17,9 @@ and activations):
                     (BF16 subnormals); MEDIUM.
 * ``sgd_162m``      W ~ N(0, 0.02) (seed 3) and M ~ N(0, 1e-3) (seed 4),
                     162,000,000 values each, CLEAN, eta = 1e-3.
+* ``momentum_162m`` the ``sgd_162m`` W and M with a dense BF16 gradient
+                    g ~ N(0, 1e-4) (seed 6 on odd steps, 7 on even ones),
+                    mu = 0.9, eta = 1e-3: SGD with momentum.
 * ``gelu_act``      [8, 4096, 3072] GELU(z), z ~ N(0, 1), seed 5, with 30% of
                     positions set to +0.0; HIGH; scaled by 2^k, k = -4..4.
 """
@@ -26,7 +29,7 @@ import numpy as np
 import torch
 
 __all__ = ["bf16_bits", "normal", "laplace", "heavy_tail", "gelu_sparse", "scale_pow2",
-           "all_bf16_patterns", "WORKLOADS"]
+           "all_bf16_patterns", "random_bits", "generate", "momentum", "gradient", "WORKLOADS"]
 
 
 def bf16_bits(a: np.ndarray) -> np.ndarray:
@@ -85,6 +88,13 @@ def scale_pow2(h: np.ndarray, k: int) -> np.ndarray:
     return bf16_bits(f)
 
 
+def random_bits(n: int, seed: int) -> np.ndarray:
+    """n uniformly random BF16 bit patterns: exponents spread evenly over all
+    256 values, so almost every one falls outside any fitted codebook."""
+    rng = np.random.default_rng(seed)
+    return rng.integers(0, 65536, size=n, dtype=np.uint32).astype(np.uint16)
+
+
 def all_bf16_patterns(seed: int = 7) -> np.ndarray:
     """Every one of the 65,536 BF16 bit patterns (zeros, subnormals, normals,
     infinities, NaN payloads) in a seeded random order."""
@@ -105,6 +115,10 @@ WORKLOADS = {
                      model="gaussian", scale=0.02, shape=0.0, level="CLEAN",
                      momentum=dict(sigma=1e-3, seed=4, model="gaussian", scale=1e-3),
                      eta=1e-3, steps=100),
+    "momentum_162m": dict(n=162_000_000, gen="normal", args=dict(sigma=0.02, seed=3),
+                          model="gaussian", scale=0.02, shape=0.0, level="CLEAN",
+                          momentum=dict(sigma=1e-3, seed=4, model="gaussian", scale=1e-3),
+                          gradient=dict(sigma=1e-4, seeds=(6, 7)), eta=1e-3, mu=0.9),
     "gelu_act": dict(n=8 * 4096 * 3072, gen="gelu_sparse", args=dict(seed=5),
                      model="gaussian", scale=1.0, shape=0.0, level="HIGH",
                      pow2=list(range(-4, 5))),
@@ -124,3 +138,11 @@ def momentum(name: str, n: int | None = None) -> np.ndarray:
     w = WORKLOADS[name]
     m = w["momentum"]
     return normal(w["n"] if n is None else n, m["sigma"], m["seed"])
+
+
+def gradient(name: str, step: int, n: int | None = None) -> np.ndarray:
+    """The dense BF16 gradient of a momentum workload at step 1, 2, ...
+    (two seeded draws, alternating)."""
+    w = WORKLOADS[name]
+    g = w["gradient"]
+    return normal(w["n"] if n is None else n, g["sigma"], g["seeds"][(step - 1) % 2])

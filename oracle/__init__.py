@@ -104,6 +104,7 @@ def lib():
         l.orc_bf16_rne.argtypes = [ctypes.c_float]
         l.orc_bf16_rne.restype = ctypes.c_uint16
         l.orc_sgd_step.argtypes = [P, P, P, P, ctypes.c_float, P]
+        l.orc_sgd_momentum_step.argtypes = [P, P, P, P, P, ctypes.c_float, ctypes.c_float, P, P, P]
         _lib = l
     return _lib
 
@@ -267,6 +268,27 @@ def sgd_step(W: Compressed, cbW: Codebook, M: Compressed, cbM: Codebook, eta: fl
     out.delta = int(to.delta)
     out.ovf_used = int(to.ovf_used)
     return out
+
+
+def sgd_momentum_step(W: Compressed, cbW: Codebook, M: Compressed, cbM: Codebook, g: np.ndarray,
+                      eta: float, mu: float, ovf_cap_w=None, ovf_cap_m=None) -> tuple[Compressed, Compressed]:
+    """Heavy-ball momentum step on compressed W and M with a dense BF16
+    gradient (uint16 bit patterns): returns the new (W, M)."""
+    g = np.ascontiguousarray(g, dtype=np.uint16).reshape(-1)
+    if g.size != W.n:
+        raise ValueError("gradient size differs from W")
+    w_out = Compressed.empty(W.n, W.block, W.slot_words, ovf_cap_w)
+    m_out = Compressed.empty(M.n, M.block, M.slot_words, ovf_cap_m)
+    tw, tm, tow, tom = W._struct(), M._struct(), w_out._struct(), m_out._struct()
+    rc = (ctypes.c_int * 2)()
+    lib().orc_sgd_momentum_step(ctypes.byref(tw), ctypes.byref(cbW), ctypes.byref(tm), ctypes.byref(cbM),
+                                _ptr(g) if g.size else None, ctypes.c_float(eta), ctypes.c_float(mu),
+                                ctypes.byref(tow), ctypes.byref(tom), rc)
+    for out, t, st in ((w_out, tow, rc[0]), (m_out, tom, rc[1])):
+        out.status = int(st)
+        out.delta = int(t.delta)
+        out.ovf_used = int(t.ovf_used)
+    return w_out, m_out
 
 
 if __name__ == "__main__":  # pragma: no cover

@@ -556,3 +556,51 @@ int orc_sgd_step(const orc_tensor *W, const orc_codebook *cbW, const orc_tensor 
     free(m);
     return rc;
 }
+
+/* SGD with momentum on compressed W and M, with a dense BF16 gradient g
+ * ([EXP] "Jargon", entry "Optimizer state": the momentum buffer of SGD with
+ * momentum is the example of optimizer state; [ABS]: optimizer states are
+ * kept compressed; [EXP] "Training adds a second problem": the update reads
+ * and rewrites the compressed tensors).  The pages print no update rule;
+ * (reading) the common heavy-ball form without dampening or Nesterov term:
+ *   M' = bf16( fl32( fl32(mu*m) + g ) )
+ *   W' = bf16( fl32( w - fl32(eta*M') ) )
+ * Every float32 operation is rounded on its own (no fused multiply-add), and
+ * the weight update uses the new momentum as stored (BF16).  Each output is
+ * coded with its own input's codebook and stored shift.  rc[0] and rc[1] get
+ * the status of W' and M'. */
+int orc_sgd_momentum_step(const orc_tensor *W, const orc_codebook *cbW, const orc_tensor *M,
+                          const orc_codebook *cbM, const uint16_t *g, float eta, float mu,
+                          orc_tensor *W_out, orc_tensor *M_out, int rc[2])
+{
+    rc[0] = rc[1] = ORC_BAD_ARG;
+    if (W->n != M->n || W_out->n != W->n || M_out->n != M->n || W_out->block != W->block ||
+        W_out->slot_words != W->slot_words || M_out->block != M->block ||
+        M_out->slot_words != M->slot_words)
+        return ORC_BAD_ARG;
+    uint64_t n = W->n;
+    uint16_t *w = (uint16_t *)malloc(2 * (n > 0 ? n : 1));
+    uint16_t *m = (uint16_t *)malloc(2 * (n > 0 ? n : 1));
+    int st = orc_decode(W, cbW, w);
+    if (st == ORC_OK) st = orc_decode(M, cbM, m);
+    if (st == ORC_OK) {
+        for (uint64_t i = 0; i < n; i++) {
+            float scaled = mu * bf16_value(m[i]);
+            float sum = scaled + bf16_value(g[i]);
+            m[i] = orc_bf16_rne(sum);
+            float step = eta * bf16_value(m[i]);
+            float r = bf16_value(w[i]) - step;
+            w[i] = orc_bf16_rne(r);
+        }
+        W_out->delta = W->delta;
+        M_out->delta = M->delta;
+        rc[0] = orc_encode(w, cbW, W_out);
+        rc[1] = orc_encode(m, cbM, M_out);
+        st = rc[0] != ORC_OK ? rc[0] : rc[1];
+    } else {
+        rc[0] = rc[1] = st;
+    }
+    free(w);
+    free(m);
+    return st;
+}

@@ -31,6 +31,8 @@
  *                        the stream layout itself is a reading the pages do
  *                        not print, so only the hand fixture pins it)
  *   orc_sgd_step         torch CPU float32 ops + bf16 cast           (pinned)
+ *   orc_sgd_momentum_step  torch CPU float32 ops + bf16 casts, one-FMA
+ *                        sensitivity, the mu = 0 reduction           (pinned)
  */
 #ifndef LCT_ORACLE_H
 #define LCT_ORACLE_H
@@ -103,6 +105,9 @@ int orc_decode(const orc_tensor *t, const orc_codebook *cb, uint16_t *y);
 uint16_t orc_bf16_rne(float f);
 int orc_sgd_step(const orc_tensor *W, const orc_codebook *cbW, const orc_tensor *M,
                  const orc_codebook *cbM, float eta, orc_tensor *W_out);
+int orc_sgd_momentum_step(const orc_tensor *W, const orc_codebook *cbW, const orc_tensor *M,
+                          const orc_codebook *cbM, const uint16_t *g, float eta, float mu,
+                          orc_tensor *W_out, orc_tensor *M_out, int rc[2]);
 
 #ifdef __cplusplus
 }

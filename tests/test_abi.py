@@ -153,3 +153,47 @@ def test_host_argument_errors_never_reach_the_device(lct_lib):
     assert lib.lct_debug_wait_timeout(None, 0x10000000, 1000, None) == E
     assert lib.lct_debug_wait_timeout(0x10000000, 0x10000000 + 4, 1000, None) == E
     assert lib.lct_debug_wait_timeout(0x10000000, 0x10000010, 0, None) == E
+
+
+def test_momentum_host_argument_errors_never_reach_the_device(lct_lib):
+    """Host checks of lct_sgd_momentum_step_fused: sizes, levels, gradient
+    pointer and the aliasing rules between the two inputs, the two outputs
+    and the gradient (no CUDA call is made on any of these)."""
+    lib = lct_lib.library()
+    cb = lct_lib.lct_codebook_build(0, 0.02)
+    E = lct_lib.LCT_ERR_INVALID_ARG
+    g = 0x60000000
+
+    def mom(w, m, ow, om, gp=g, c=cb):
+        return lib.lct_sgd_momentum_step_fused(ctypes.byref(w), ctypes.byref(c), ctypes.byref(m), ctypes.byref(c),
+                                               gp, ctypes.c_float(1e-3), ctypes.c_float(0.9), ctypes.byref(ow),
+                                               ctypes.byref(om), None)
+
+    def four():
+        return (_fake_tensor(lct_lib), _fake_tensor(lct_lib, base=0x40000000),
+                _fake_tensor(lct_lib, base=0x50000000), _fake_tensor(lct_lib, base=0x70000000))
+
+    w, m, ow, om = four()
+    bad_cb = lct_lib.lct_codebook_build(0, 0.02)
+    bad_cb.len[3] = 9
+    assert mom(w, m, ow, om, c=bad_cb) == E             # malformed codebook
+    assert mom(w, m, ow, om, gp=None) == E               # NULL gradient
+    assert mom(w, m, ow, om, gp=g + 2) == E              # misaligned gradient
+    assert mom(w, m, ow, om, gp=ow.d_sf) == E            # gradient overlaps an output
+    m2 = _fake_tensor(lct_lib, n=999, base=0x40000000)
+    assert mom(w, m2, ow, om) == E                       # n mismatch
+    om2 = _fake_tensor(lct_lib, level=1, base=0x70000000)
+    assert mom(w, m, ow, om2) == lct_lib.LCT_ERR_UNSUPPORTED
+    w, m, ow, om = four()
+    om.d_ovf = ow.d_ovf                                  # the outputs share an overflow region
+    assert mom(w, m, ow, om) == E
+    w, m, ow, om = four()
+    ow2 = _fake_tensor(lct_lib, base=0x40000000)         # W' written into M
+    assert mom(w, m, ow2, om) == E
+    om3 = _fake_tensor(lct_lib, base=0x10000000)         # M' written into W
+    assert mom(w, m, ow, om3) == E
+    ow4 = _fake_tensor(lct_lib, base=0x10000000)         # W' fully aliases W_in, overflow included
+    assert mom(w, m, ow4, om) == E
+    ow5 = _fake_tensor(lct_lib, base=0x50000000)
+    ow5.d_sf = w.d_sf + 16                               # partly overlaps W_in's bytes
+    assert mom(w, m, ow5, om) == E

@@ -490,3 +490,98 @@ def test_sgd_nan_is_canonical(orc):
     out = orc.sgd_step(W, cb, M, cb, 1.0)
     rc, got = orc.decode(out, cb)
     assert rc == orc.OK and list(got) == [0x7FC0, 0x7FC0, 0x7FC0]
+
+
+# ------------------------------------------------------ momentum step
+
+def _bits(t):
+    return t.to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+
+
+def test_momentum_step_matches_torch_separate_roundings(orc):
+    """Heavy-ball momentum on compressed optimizer state ([EXP] 'Jargon',
+    'Optimizer state'; [ABS]): M' = bf16(mu*m + g), W' = bf16(w - eta*M'),
+    every float32 op rounded on its own, the weight step taking the stored
+    BF16 M'.  torch CPU runs the same separate ops.  Cancellation slices make
+    a fused multiply-add in either update show up in the bits."""
+    n = 2 * 65536 + 4321
+    w = synth.normal(n, 0.02, 3)
+    m = synth.normal(n, 1e-3, 4)
+    g = synth.normal(n, 1e-4, 6)
+    w[:5] = [0x0001, 0x8001, 0x0000, 0x7F80, 0x3F80]   # subnormals, zero, +inf, 1
+    m[:5] = [0x0003, 0x0001, 0x8000, 0x3F80, 0x0000]
+    g[:5] = [0x8000, 0x0002, 0x8000, 0x0000, 0x8000]
+    eta, mu = np.float32(1e-3), np.float32(0.9)
+    eta_t, mu_t = torch.tensor(float(eta)), torch.tensor(float(mu))
+    # g ~ -mu*m: the rounding of the product decides the new momentum
+    sl = slice(1000, 3000)
+    g[sl] = _bits(-(mu_t * _bf16_tensor(m[sl]).float()))
+    mt, gt = _bf16_tensor(m).float(), _bf16_tensor(g).float()
+    m_new = _bits((mu_t * mt) + gt)
+    # w ~ eta*M': the rounding of the weight step's product decides
+    sl2 = slice(5000, 7000)
+    w[sl2] = _bits(eta_t * _bf16_tensor(m_new[sl2]).float())
+    wt = _bf16_tensor(w).float()
+    w_new = _bits(wt - eta_t * _bf16_tensor(m_new).float())
+
+    cbw, cbm = orc.codebook_build(0, 0.02), orc.codebook_build(0, 1e-3)
+    W, M = orc.encode(w, cbw, orc.CLEAN), orc.encode(m, cbm, orc.CLEAN)
+    W2, M2 = orc.sgd_momentum_step(W, cbw, M, cbm, g, float(eta), float(mu))
+    assert W2.status == orc.OK and M2.status == orc.OK
+    assert W2.delta == W.delta and M2.delta == M.delta
+    rc_w, got_w = orc.decode(W2, cbw)
+    rc_m, got_m = orc.decode(M2, cbm)
+    assert rc_w == orc.OK and rc_m == orc.OK
+    assert np.array_equal(got_m, m_new)
+    assert np.array_equal(got_w, w_new)
+    # the checks above would catch a fused multiply-add in either update
+    fma_m = _bits((mu_t.double() * mt.double() + gt.double()).float())
+    assert (fma_m != m_new).any()
+    fma_w = _bits((wt.double() - eta_t.double() * _bf16_tensor(m_new).float().double()).float())
+    assert (fma_w != w_new).any()
+    # ... and the weight step taking the old momentum, or the unrounded new one
+    old_m = _bits(wt - eta_t * mt)
+    assert (old_m != w_new).any()
+    unrounded = _bits(wt - eta_t * ((mu_t * mt) + gt))
+    assert (unrounded != w_new).any()
+    # each output is coded with its input's stored shift
+    again = orc.encode(got_m, cbm, orc.CLEAN, delta=M.delta)
+    assert np.array_equal(again.slots, M2.slots) and np.array_equal(again.markers, M2.markers)
+
+
+def test_momentum_step_with_zero_mu_is_plain_sgd_on_the_gradient(orc):
+    """With mu = 0 and finite m the new momentum is the gradient itself
+    (0*m + g = g exactly, except that -0 + +0 gives +0), so the weight step
+    reduces to the plain fused SGD step with M = g."""
+    n = 65536 + 777
+    w = synth.normal(n, 0.02, 7)
+    m = synth.normal(n, 1e-3, 8)
+    g = synth.normal(n, 1e-4, 9)
+    g[g == 0x8000] = 0x0000
+    cbw, cbm = orc.codebook_build(0, 0.02), orc.codebook_build(0, 1e-3)
+    W, M = orc.encode(w, cbw, orc.CLEAN), orc.encode(m, cbm, orc.CLEAN)
+    W2, M2 = orc.sgd_momentum_step(W, cbw, M, cbm, g, 1e-3, 0.0)
+    _, got_m = orc.decode(M2, cbm)
+    assert np.array_equal(got_m, g)
+    G = orc.encode(g, cbm, orc.CLEAN)
+    plain = orc.sgd_step(W, cbw, G, cbm, 1e-3)
+    assert np.array_equal(W2.slots, plain.slots) and np.array_equal(W2.sf, plain.sf)
+    assert np.array_equal(W2.markers, plain.markers)
+
+
+def test_momentum_step_spills_and_status_per_output(orc):
+    """Each output has its own overflow region: a too-small capacity for the
+    new momentum latches capacity on M' only."""
+    n = 65536
+    w = synth.normal(n, 0.02, 10)
+    m = synth.gelu_sparse(n, 11)   # far off the momentum codebook: heavy spill
+    g = synth.normal(n, 1e-2, 12)
+    cbw, cbm = orc.codebook_build(0, 0.02), orc.codebook_build(0, 1e-3)
+    W, M = orc.encode(w, cbw, orc.CLEAN), orc.encode(m, cbm, orc.CLEAN)
+    W2, M2 = orc.sgd_momentum_step(W, cbw, M, cbm, g, 1e-3, 0.9, ovf_cap_m=16)
+    assert W2.status == orc.OK
+    assert M2.status == orc.CAPACITY and M2.ovf_used > 16
+    W3, M3 = orc.sgd_momentum_step(W, cbw, M, cbm, g, 1e-3, 0.9)
+    assert M3.status == orc.OK and M3.ovf_used == M2.ovf_used
+    rc, got = orc.decode(M3, cbm)
+    assert rc == orc.OK

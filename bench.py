@@ -257,7 +257,7 @@ def run_gpu(args):
         with open(tpath) as f:
             tr = json.load(f)
         entry = tr.get(args.workload, {}).get(dom)
-        if entry and entry.get("source_hash") == kernel_source_hash():
+        if entry and entry.get("source_hash") == kernel_source_hash(dom):
             traffic = entry["bytes_per_launch"]
 
     # ---- end to end through the public API with host buffers
@@ -403,7 +403,7 @@ def run_gpu_momentum(args, rank, local_rank, world):
     if os.path.exists(tpath):
         with open(tpath) as f:
             entry = json.load(f).get(args.workload, {}).get("momentum")
-        if entry and entry.get("source_hash") == kernel_source_hash():
+        if entry and entry.get("source_hash") == kernel_source_hash("momentum"):
             traffic = entry["bytes_per_launch"]
     if rank != 0:
         return None
@@ -449,11 +449,18 @@ def oracle_momentum_time(workload: str, nblocks_sample: int):
     return time.perf_counter() - t0, k
 
 
-def kernel_source_hash() -> str:
+# Device source each kernel's DRAM traffic depends on (the shared device
+# header and the kernel's own file); host code does not enter the hash.
+KERNEL_SOURCES = {"encode": "encode.cu", "decode": "decode.cu", "sgd": "sgd.cu", "momentum": "momentum.cu"}
+
+
+def kernel_source_hash(kernel: str) -> str:
+    """Hash of the source a kernel's measured traffic belongs to: a stored
+    ncu traffic figure is used only while this hash is unchanged."""
     import hashlib
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "lossless_bf16_tensor_gb300", "csrc")
-    for fn in sorted(os.listdir(csrc)):
+    for fn in ("codec_dev.cuh", "internal.h", KERNEL_SOURCES[kernel]):
         with open(os.path.join(csrc, fn), "rb") as f:
             h.update(fn.encode() + f.read())
     return h.hexdigest()[:16]

@@ -7,14 +7,16 @@
 //
 // Thread j of a block's CTA owns stream j of W, of M and of the new W: per
 // row it decodes one symbol of W and one of M, updates the value, writes its
-// sign-fraction byte and appends its exponent to the new slot.  The slot
-// images of W and M come in by TMA bulk copy; the sign-fraction bytes stream
-// through a ring of row chunks.  A chunk
+// sign-fraction byte and appends its exponent to the new slot, whose words go
+// straight to global memory.  The slot images of W and M come in by TMA bulk
+// copy; the sign-fraction bytes stream through a ring of row chunks.  A chunk
 // in which no stream of a warp reaches a spill marker and every new slot has
 // room takes a fast path with no per-value checks.  Spilled new exponents are
-// kept for 64 rows (every row when W is updated in place); an out-of-place
-// step whose stream spills more than that re-decodes the older rows of that
-// stream at the end.
+// kept for 32 rows out of place, which leaves room for three CTAs per SM; an
+// out-of-place step whose stream spills more than that re-decodes the older
+// rows of that stream at the end.  In place every spilled exponent is kept:
+// a code is at most 16 bits, so a stream holds at least 2W symbols of its
+// slot and spills at most NJ - 2W.
 #include "codec_dev.cuh"
 
 namespace lct {
@@ -22,8 +24,7 @@ namespace dev {
 
 constexpr int kSgdThreads = 256;
 constexpr int kSgdRows = 8;    // rows per sign-fraction chunk
-constexpr int kSgdRing = 3;    // chunks in flight
-constexpr int kSgdSpill = 64;  // spilled new-exponent rows kept (out of place)
+constexpr int kSgdSpill = 32;  // spilled new-exponent rows kept (out of place; a power of two)
 
 // One value of W and one of M (BF16 in bits 0..15) -> the updated BF16:
 // fl32(w - fl32(eta*m)), product and difference rounded separately.
@@ -35,13 +36,15 @@ __device__ __forceinline__ uint32_t sgd_one(uint32_t w, uint32_t m, float eta)
 template <int LEVEL, bool INPLACE>
 struct SgdSmem {
     static constexpr int W = Geo<LEVEL>::W, NJ = Geo<LEVEL>::NJ;
-    static constexpr int kSpillRows = INPLACE ? NJ : kSgdSpill;
+    static constexpr int kSpillRows = INPLACE ? NJ - 2 * W : kSgdSpill;
+    static constexpr int kStages = INPLACE ? 3 : 2;  // chunks in flight
     static constexpr int kSlotIn = (W + 1) * kStreams * 4;  // + zero guard row
-    static constexpr int kSlotOut = W * kStreams * 4;
-    static constexpr int kRing = kSgdRing * kSgdRows * kStreams;  // per input
+    static constexpr int kRing = kStages * kSgdRows * kStreams;  // per input
     static constexpr int kLuts = 2 * 256 * 4 + 256 * 8;
     static constexpr int kSpill = (kSpillRows * kRow + 127) / 128 * 128;
-    static constexpr int kBytes = 2 * kSlotIn + kSlotOut + 2 * kRing + kLuts + kSpill;
+    static constexpr int kBytes = 2 * kSlotIn + 2 * kRing + kLuts + kSpill;
+    static constexpr int kCtas = INPLACE ? 1 : 3;  // CTAs per SM the launch bounds ask for
+    static_assert(INPLACE || (kSgdSpill & (kSgdSpill - 1)) == 0, "ring index uses a mask");
 };
 
 // Prologue: the new W's header (shift and codebook carried over, status
@@ -93,18 +96,25 @@ __device__ __forceinline__ uint32_t in_take(InStream &s, uint32_t k, const uint3
     return ovf_ok ? (uint32_t)__ldg(ovf + s.ovf_at + k) << 7 : 0u;
 }
 
+// Slot of a spilled new exponent in the staging rows: t = k - marker counts
+// the stream's spilled symbols; out of place the rows are a ring.
+template <bool INPLACE, int SP>
+__device__ __forceinline__ uint32_t stage_row(uint32_t t)
+{
+    return INPLACE ? t : (t & (SP - 1));
+}
+
 template <int LEVEL, bool INPLACE>
-__global__ void __launch_bounds__(kSgdThreads, 2) k_sgd(const __grid_constant__ SgdArgs a)
+__global__ void __launch_bounds__(kSgdThreads, SgdSmem<LEVEL, INPLACE>::kCtas) k_sgd(const __grid_constant__ SgdArgs a)
 {
     using G = Geo<LEVEL>;
     using L = SgdSmem<LEVEL, INPLACE>;
-    constexpr int W = G::W, R = kSgdRows, S = kSgdRing, SP = L::kSpillRows;
+    constexpr int W = G::W, R = kSgdRows, S = L::kStages, SP = L::kSpillRows;
     constexpr int NW = kSgdThreads / 32;
     extern __shared__ __align__(128) uint8_t smem[];
     uint32_t *slotW = reinterpret_cast<uint32_t *>(smem);
     uint32_t *slotM = reinterpret_cast<uint32_t *>(smem + L::kSlotIn);
-    uint32_t *slotO = reinterpret_cast<uint32_t *>(smem + 2 * L::kSlotIn);
-    uint8_t *sfW_s = smem + 2 * L::kSlotIn + L::kSlotOut;
+    uint8_t *sfW_s = smem + 2 * L::kSlotIn;
     uint8_t *sfM_s = sfW_s + L::kRing;
     uint32_t *lutW = reinterpret_cast<uint32_t *>(sfM_s + L::kRing);
     uint32_t *lutM = lutW + 256;
@@ -182,7 +192,7 @@ __global__ void __launch_bounds__(kSgdThreads, 2) k_sgd(const __grid_constant__ 
     sm.pos = 0;
     Writer wo;
     wr_init<W>(wo, nj);
-    uint32_t *colO = slotO + j;
+    uint32_t *colO = a.w_out.slots + (uint64_t)b * W * kStreams + j;
     uint8_t *sfj = a.w_out.sf + base + j;
     uint8_t *ringj = ring + j;
     const float eta = a.eta;
@@ -229,7 +239,8 @@ __global__ void __launch_bounds__(kSgdThreads, 2) k_sgd(const __grid_constant__ 
 #pragma unroll
                 for (int r = 0; r < R; ++r) {
                     const uint32_t k = c * R + r;
-                    if (wr_put_checked(wo, ent[r], k, colO)) ringj[(k % SP) * kRow] = (uint8_t)exp_of(h[r]);
+                    if (wr_put_checked(wo, ent[r], k, colO))
+                        ringj[stage_row<INPLACE, SP>(k - wo.marker) * kRow] = (uint8_t)exp_of(h[r]);
                 }
             }
         } else {
@@ -244,7 +255,7 @@ __global__ void __launch_bounds__(kSgdThreads, 2) k_sgd(const __grid_constant__ 
                 const uint32_t h = sgd_one(join_one(fw, ew), join_one(fm, em), eta);
                 const uint32_t e = exp_of(h);
                 sfo[r * kStreams] = sf_of(h);
-                if (wr_put_checked(wo, tbl[e], k, colO)) ringj[(k % SP) * kRow] = (uint8_t)e;
+                if (wr_put_checked(wo, tbl[e], k, colO)) ringj[stage_row<INPLACE, SP>(k - wo.marker) * kRow] = (uint8_t)e;
             }
         }
         __syncthreads();  // every thread is done with this chunk's ring slot
@@ -261,13 +272,7 @@ __global__ void __launch_bounds__(kSgdThreads, 2) k_sgd(const __grid_constant__ 
     wr_finish<W>(wo, colO);
     const uint32_t marker = wo.marker, spill = nj - marker;
     uint32_t total;
-    const uint32_t pre = group_exclusive_scan(spill, warp_tot, NW, 0, &total);  // syncs: slot image complete
-
-    if (j == 0) {
-        fence_proxy_async();
-        bulk_store(a.w_out.slots + (uint64_t)b * W * kStreams, slotO, W * kStreams * 4);
-        bulk_commit();
-    }
+    const uint32_t pre = group_exclusive_scan(spill, warp_tot, NW, 0, &total);
     a.w_out.markers[(uint64_t)b * kStreams + j] = (uint16_t)marker;
 
     if (warp == 0) {
@@ -296,12 +301,9 @@ __global__ void __launch_bounds__(kSgdThreads, 2) k_sgd(const __grid_constant__ 
             const uint32_t ssp = __shfl_sync(kFull, spill, i);
             const uint32_t spr = __shfl_sync(kFull, pre, i);
             const uint32_t sj = (uint32_t)(warp * 32 + i);
-            const uint32_t nj_i = smk + ssp;
-            const uint32_t kept_from = nj_i > (uint32_t)SP ? nj_i - SP : 0u;
-            for (uint32_t l = lane; l < ssp; l += 32) {
-                const uint32_t k = smk + l;
-                if (k >= kept_from) out[spr + l] = ring[(k % SP) * kRow + sj];
-            }
+            const uint32_t kept_from = INPLACE || ssp <= (uint32_t)SP ? 0u : ssp - SP;  // older ones were overwritten
+            for (uint32_t l = lane; l < ssp; l += 32)
+                if (l >= kept_from) out[spr + l] = ring[stage_row<INPLACE, SP>(l) * kRow + sj];
         }
         const uint32_t kept_from = nj > (uint32_t)SP ? nj - SP : 0u;
         if (!INPLACE && marker < kept_from) {
@@ -322,14 +324,14 @@ __global__ void __launch_bounds__(kSgdThreads, 2) k_sgd(const __grid_constant__ 
         }
     }
     pdl_launch_dependents();
-    if (j == 0) {
-        if (s_flags & 1u) {
-            for (uint32_t s = 0; s < (uint32_t)S && s < nbulk; ++s) {
-                const uint32_t last = s + (nbulk - 1 - s) / S * S;
-                mbar_wait(&bar_sf[s], (last / S) & 1u, limit);
-            }
+    if (j == 0 && (s_flags & 1u)) {
+        // a wait gave up: let every copy still in flight land before the CTA
+        // (and its shared memory) goes away
+        mbar_wait(&bar_slot, 0, limit);
+        for (uint32_t s = 0; s < (uint32_t)S && s < nbulk; ++s) {
+            const uint32_t last = s + (nbulk - 1 - s) / S * S;
+            mbar_wait(&bar_sf[s], (last / S) & 1u, limit);
         }
-        bulk_wait_all();  // the slot image store has read shared memory
     }
 }
 

@@ -73,6 +73,31 @@ def test_sgd_with_spill_and_special_values():
     assert_same_format(out.to_host(), ref)
 
 
+@pytest.mark.parametrize("level", [0, 1, 2])
+@pytest.mark.parametrize("in_place", [False, True])
+def test_sgd_worst_case_spill(level, in_place):
+    """Every new exponent of the first block is 255 (W is NaN there), which no
+    codebook codes: each of its streams keeps exactly 2W escapes (16 bits
+    each) in its slot and spills all the rest, the most an in-place step has
+    to keep.  The other blocks hold uniformly random bit patterns (mostly
+    escapes too), so an out-of-place step spills far beyond its kept rows."""
+    bsz = 65536 if level == 0 else 32768
+    words = {0: 25, 1: 16, 2: 20}[level]
+    n = 2 * bsz + 999
+    w = synth.random_bits(n, 21)
+    w[:bsz] = 0x7FC1
+    m = synth.normal(n, 1e-3, 4)
+    W, M, cbw, cbm, oW, oM, ocbw, ocbm = _setup(w, m, level)
+    ref = oracle.sgd_step(oW, ocbw, oM, ocbm, ETA)
+    assert (ref.markers[:256] == 2 * words).all()
+    out = B.CompressedTensor(n, level, like=W) if in_place else B.CompressedTensor(n, level)
+    B.lct_sgd_step_fused(W, cbw, M, cbm, ETA, out)
+    torch.cuda.synchronize()
+    got = out.to_host()
+    assert got["status"] == ref.status == 0
+    assert_same_format(got, ref)
+
+
 def test_sgd_162m_step_one_full_and_sampled_steps():
     """162,000,000-value W ~ N(0, 0.02) and M ~ N(0, 1e-3), CLEAN, eta = 1e-3,
     100 steps on the GPU with ping-pong overflow buffers.  Step 1 is compared

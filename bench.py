@@ -42,14 +42,16 @@ WORKLOAD_TEXT = {
                  "MEDIUM; step = encode + decode + fused SGD (M ~ Laplace(0,1e-3))",
     "gelu_act": "[8,4096,3072] GELU(N(0,1)) with 30% zeros, Gaussian(1) codebook, HIGH; step = encode + decode + "
                 "fused SGD (M ~ Laplace(0,1e-3))",
+    "gelu_act_zero": "[8,4096,3072] GELU(N(0,1)) with 30% zeros, Gaussian(1) codebook with a 0.3 point mass at zero, "
+                     "HIGH; step = encode + decode + fused SGD (M ~ Laplace(0,1e-3))",
     "sgd_162m": "162,000,000 BF16 W ~ N(0,0.02), M ~ N(0,1e-3), Gaussian codebooks, CLEAN; step = encode + decode "
                 "+ fused SGD",
     "momentum_162m": "162,000,000 BF16 W ~ N(0,0.02), M ~ N(0,1e-3), dense BF16 gradient ~ N(0,1e-4), Gaussian "
                      "codebooks, CLEAN, W and M updated in place; step = one fused SGD-with-momentum step "
                      "(mu = 0.9, eta = 1e-3)",
 }
-SGD_MOMENTUM = {"gauss_block": ("laplace", 1e-3), "laplace_16m": ("laplace", 1e-3), "heavy_64m": ("laplace", 1e-3), "gelu_act": ("laplace", 1e-3),
-                "sgd_162m": ("gaussian", 1e-3)}
+SGD_MOMENTUM = {"gauss_block": ("laplace", 1e-3), "laplace_16m": ("laplace", 1e-3), "heavy_64m": ("laplace", 1e-3),
+                "gelu_act": ("laplace", 1e-3), "gelu_act_zero": ("laplace", 1e-3), "sgd_162m": ("gaussian", 1e-3)}
 ETA = float(np.float32(1e-3))
 L2_FLUSH_BYTES = 256 << 20
 
@@ -177,7 +179,10 @@ def run_gpu(args):
     x_np = synth.generate(args.workload)
     mm, ms = SGD_MOMENTUM[args.workload]
     m_np = synth.laplace(n, ms, seed=2) if mm == "laplace" else synth.momentum(args.workload)
-    cb = B.lct_codebook_build(wl["model"], wl["scale"], wl["shape"])
+    if "zero_frac" in wl:
+        cb = B.lct_codebook_build_zero_atom(wl["model"], wl["scale"], wl["shape"], wl["zero_frac"])
+    else:
+        cb = B.lct_codebook_build(wl["model"], wl["scale"], wl["shape"])
     cbm = B.lct_codebook_build(mm, ms)
 
     stream = torch.cuda.current_stream()
@@ -483,7 +488,10 @@ def oracle_step_time(workload: str, nblocks_sample: int | None):
         k = min(x.size, nblocks_sample * block)
         x, m = x[:k], m[:k]
     model = {"gaussian": 0, "laplace": 1, "powerlaw": 2}
-    cb = oracle.codebook_build(model[wl["model"]], wl["scale"], wl["shape"])
+    if "zero_frac" in wl:
+        cb = oracle.codebook_build_zero_atom(model[wl["model"]], wl["scale"], wl["shape"], wl["zero_frac"])
+    else:
+        cb = oracle.codebook_build(model[wl["model"]], wl["scale"], wl["shape"])
     cbm = oracle.codebook_build(model[mm], ms)
     M = oracle.encode(m, cbm, level)
     t0 = time.perf_counter()

@@ -89,8 +89,12 @@ typedef struct {
     uint16_t nsym;        /* symbols with their own code */
     int32_t median_exp;   /* the model's median biased exponent (1..254) */
     int32_t model;        /* lct_model it was built from */
-    uint32_t hash;        /* 32-bit FNV-1a of len, code, esc_len, esc_code */
+    uint32_t hash;        /* 32-bit FNV-1a of len, code, esc_len, esc_code, zero_atom */
     double scale, shape;  /* model parameters it was built from */
+    double zero_frac;     /* point mass at zero it was built with (0 = none) */
+    uint32_t zero_atom;   /* 1: exponent 0 always codes as symbol 0, unshifted;
+                             a nonzero exponent the shift maps to symbol 0 escapes */
+    uint32_t reserved;
 } lct_codebook;
 
 /* Device header, LCT_HEADER_BYTES at t->d_header.  Written by lct_encode and
@@ -173,6 +177,22 @@ typedef struct {
  * bad parameters. */
 lct_status lct_codebook_build(int model, double scale, double shape, lct_codebook *out);
 
+/* The same with a point mass at zero: a fraction zero_frac (0 <= zero_frac <
+ * 1) of the values are exactly zero, as in ReLU/GELU activations, and the
+ * rest follow the model.  Bucket masses are (1 - zero_frac) * p(e), plus
+ * zero_frac at e = 0; the rest of the construction is lct_codebook_build's.
+ * The pages note that the user supplies the distribution and that one which
+ * does not fit the tensor raises storage ([EXP] "Read the 3.5x longer context
+ * claim carefully"); zeros are a common misfit, since any shift moves them to
+ * an unused symbol and they escape at 16 bits each.  The resulting codebook
+ * has zero_atom = 1: exponent 0 (zeros and subnormals) always codes as symbol
+ * 0 whatever the tensor's shift, and a nonzero exponent that the shift maps
+ * onto symbol 0 is escaped.  The pages have no such model; its encoding is
+ * decoded by lct_decode like any other.  Returns LCT_ERR_INVALID_ARG for bad
+ * parameters. */
+lct_status lct_codebook_build_zero_atom(int model, double scale, double shape, double zero_frac,
+                                        lct_codebook *out);
+
 /* Region sizes for an n-value tensor at `level`, and, when `t` is not NULL,
  * the state of a written tensor: synchronises `stream`, then reads the
  * device header into out->ovf_used / status / delta.
@@ -236,6 +256,19 @@ lct_status lct_encode_static_scratch(const uint16_t *d_x, const lct_codebook *cb
  * markers) or LCT_ERR_OVERFLOW_CAPACITY (overflow never written); d_y is then
  * unspecified.  d_y must not overlap the tensor. */
 lct_status lct_decode(const lct_tensor *t, const lct_codebook *cb, uint16_t *d_y, void *stream);
+
+/* Decode only blocks first_block .. first_block + nblocks - 1 of `t` into d_y
+ * (device, 16-byte aligned): value i of block first_block goes to d_y[i], so
+ * d_y holds min(nblocks * block, n - first_block * block) values.  This is
+ * the piece for decoding a compressed matmul operand tile by tile into a
+ * small dense buffer that a GEMM reads ([EXP] "Read the 3.5x longer context
+ * claim carefully": decoding inside matmul kernels is named as future work;
+ * decoding a tile at a time ahead of a library GEMM keeps only one tile
+ * dense).  Blocks are independent given the stored shift and offsets.
+ * nblocks = 0 enqueues nothing.  Errors as lct_decode (latched in t's
+ * header), plus LCT_ERR_INVALID_ARG for a range past the last block. */
+lct_status lct_decode_blocks(const lct_tensor *t, const lct_codebook *cb, uint64_t first_block, uint64_t nblocks,
+                             uint16_t *d_y, void *stream);
 
 /* One fused SGD step W <- W - eta*M on compressed W and M ([EXP] "Training
  * adds a second problem": read the compressed inputs, compute, write the new

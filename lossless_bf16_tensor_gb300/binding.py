@@ -51,7 +51,8 @@ class lct_codebook(ctypes.Structure):
                 ("dec", ctypes.c_uint16 * 256), ("esc_len", ctypes.c_uint8),
                 ("esc_code", ctypes.c_uint8), ("nsym", ctypes.c_uint16),
                 ("median_exp", ctypes.c_int32), ("model", ctypes.c_int32),
-                ("hash", ctypes.c_uint32), ("scale", ctypes.c_double), ("shape", ctypes.c_double)]
+                ("hash", ctypes.c_uint32), ("scale", ctypes.c_double), ("shape", ctypes.c_double),
+                ("zero_frac", ctypes.c_double), ("zero_atom", ctypes.c_uint32), ("reserved", ctypes.c_uint32)]
 
 
 class lct_tensor(ctypes.Structure):
@@ -73,10 +74,14 @@ class lct_sizes(ctypes.Structure):
 
 _P = ctypes.c_void_p
 _lib.lct_codebook_build.argtypes = [ctypes.c_int, ctypes.c_double, ctypes.c_double, ctypes.POINTER(lct_codebook)]
+_lib.lct_codebook_build_zero_atom.argtypes = [ctypes.c_int, ctypes.c_double, ctypes.c_double, ctypes.c_double,
+                                              ctypes.POINTER(lct_codebook)]
 _lib.lct_compressed_size.argtypes = [ctypes.c_uint64, ctypes.c_int, ctypes.POINTER(lct_tensor), _P,
                                      ctypes.POINTER(lct_sizes)]
 _lib.lct_encode.argtypes = [_P, ctypes.POINTER(lct_codebook), ctypes.POINTER(lct_tensor), _P]
 _lib.lct_decode.argtypes = [ctypes.POINTER(lct_tensor), ctypes.POINTER(lct_codebook), _P, _P]
+_lib.lct_decode_blocks.argtypes = [ctypes.POINTER(lct_tensor), ctypes.POINTER(lct_codebook), ctypes.c_uint64,
+                                   ctypes.c_uint64, _P, _P]
 _lib.lct_sgd_step_fused.argtypes = [ctypes.POINTER(lct_tensor), ctypes.POINTER(lct_codebook),
                                     ctypes.POINTER(lct_tensor), ctypes.POINTER(lct_codebook), ctypes.c_float,
                                     ctypes.POINTER(lct_tensor), _P]
@@ -86,7 +91,8 @@ _lib.lct_sgd_momentum_step_fused.argtypes = [ctypes.POINTER(lct_tensor), ctypes.
                                              ctypes.POINTER(lct_tensor), _P]
 _lib.lct_debug_wait_timeout.argtypes = [_P, _P, ctypes.c_uint64, _P]
 _lib.lct_encode_static_scratch.argtypes = [_P, ctypes.POINTER(lct_codebook), ctypes.POINTER(lct_tensor), _P]
-for _fn in ("lct_codebook_build", "lct_compressed_size", "lct_encode", "lct_decode", "lct_sgd_step_fused",
+for _fn in ("lct_codebook_build", "lct_codebook_build_zero_atom", "lct_compressed_size", "lct_encode", "lct_decode",
+            "lct_decode_blocks", "lct_sgd_step_fused",
             "lct_sgd_momentum_step_fused", "lct_debug_wait_timeout", "lct_encode_static_scratch"):
     getattr(_lib, _fn).restype = ctypes.c_int
 
@@ -125,6 +131,13 @@ def lct_codebook_build(model, scale: float, shape: float = 0.0) -> lct_codebook:
     return cb
 
 
+def lct_codebook_build_zero_atom(model, scale: float, shape: float, zero_frac: float) -> lct_codebook:
+    cb = lct_codebook()
+    _check(_lib.lct_codebook_build_zero_atom(_model(model), float(scale), float(shape), float(zero_frac),
+                                             ctypes.byref(cb)), "lct_codebook_build_zero_atom")
+    return cb
+
+
 def lct_compressed_size(n: int, level, t: "CompressedTensor | None" = None, stream=None) -> lct_sizes:
     s = lct_sizes()
     desc = ctypes.byref(t.desc) if t is not None else None
@@ -156,6 +169,18 @@ def lct_encode_static_scratch(x: torch.Tensor, cb: lct_codebook, t: "CompressedT
 def lct_decode(t: "CompressedTensor", cb: lct_codebook, y: torch.Tensor, stream=None) -> None:
     ptr = _dev_ptr(y, t.n) if t.n else None
     _check(_lib.lct_decode(ctypes.byref(t.desc), ctypes.byref(cb), ptr, _stream(stream)), "lct_decode")
+
+
+def lct_decode_blocks(t: "CompressedTensor", cb: lct_codebook, first_block: int, nblocks: int, y: torch.Tensor,
+                      stream=None) -> None:
+    """Decode blocks first_block .. first_block+nblocks-1 into y (a CUDA
+    16-bit tensor holding exactly those blocks' values)."""
+    block = int(t.sizes.block)
+    lo = int(first_block) * block
+    hi = min(t.n, (int(first_block) + int(nblocks)) * block)
+    ptr = _dev_ptr(y, max(hi - lo, 0)) if nblocks else None
+    _check(_lib.lct_decode_blocks(ctypes.byref(t.desc), ctypes.byref(cb), int(first_block), int(nblocks), ptr,
+                                  _stream(stream)), "lct_decode_blocks")
 
 
 def lct_sgd_step_fused(W_in: "CompressedTensor", cbW: lct_codebook, M: "CompressedTensor", cbM: lct_codebook,
@@ -195,7 +220,7 @@ class CompressedTensor:
     """
 
     def __init__(self, n: int, level, ovf_cap: int | None = None, device="cuda", ovf: torch.Tensor | None = None,
-                 like: "CompressedTensor | None" = None):
+                 like: "CompressedTensor | None" = None, zero_fill: bool = True):
         self.n = int(n)
         self.level = _level(level)
         self.sizes = lct_compressed_size(self.n, self.level)
@@ -216,7 +241,11 @@ class CompressedTensor:
         for name, size in parts:
             offs[name] = (total, int(size))
             total = _round_up(total + int(size))
-        self.buffer = torch.zeros(max(total, 256), dtype=torch.uint8, device=device)
+        # a writer fills every region it owns (header, sign-fraction bytes,
+        # slots, markers, offsets, the used overflow) and clears its scratch,
+        # so zero filling is only for tidiness
+        alloc = torch.zeros if zero_fill else torch.empty
+        self.buffer = alloc(max(total, 256), dtype=torch.uint8, device=device)
         self.regions = {name: self.buffer[o:o + sz] for name, (o, sz) in offs.items()}
         if like is not None:
             for name in ("header", "sf", "slots", "markers", "blk_off"):

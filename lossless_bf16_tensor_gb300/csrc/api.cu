@@ -1,6 +1,7 @@
 // Host entry points of liblct (the C ABI declared in include/lct.h):
 // argument checks, sizing, and kernel launches.  No device memory is ever
 // allocated here; every buffer belongs to the caller.
+#include <algorithm>
 #include <cstdint>
 #include <cstring>
 
@@ -98,6 +99,7 @@ DevCodebook dev_codebook(const lct_codebook &cb)
     std::memcpy(d.dec, cb.dec, sizeof(d.dec));
     d.esc_len = cb.esc_len;
     d.esc_code = cb.esc_code;
+    d.zero_atom = static_cast<uint8_t>(cb.zero_atom);
     d.pad = 0;
     d.hash = cb.hash;
     return d;
@@ -182,7 +184,37 @@ extern "C" lct_status lct_decode(const lct_tensor *t, const lct_codebook *cb, ui
     a.y = d_y;
     a.cb = dev_codebook(*cb);
     a.wait_ns = kDefaultWaitNs;
-    return launch_decode(a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? LCT_OK : LCT_ERR_CUDA;
+    a.first_block = 0;
+    a.pad = 0;
+    return launch_decode(a, a.t.nblocks, static_cast<cudaStream_t>(stream)) == cudaSuccess ? LCT_OK : LCT_ERR_CUDA;
+}
+
+extern "C" lct_status lct_decode_blocks(const lct_tensor *t, const lct_codebook *cb, uint64_t first_block,
+                                        uint64_t nblocks, uint16_t *d_y, void *stream)
+{
+    lct_sizes s;
+    lct_status rc = check_tensor(t, false, &s);
+    if (rc != LCT_OK) return rc;
+    if (!cb || !codebook_valid(*cb)) return LCT_ERR_INVALID_ARG;
+    if (first_block > s.nblocks || nblocks > s.nblocks - first_block) return LCT_ERR_INVALID_ARG;
+    if (nblocks == 0) return LCT_OK;
+    const uint64_t lo = first_block * s.block;
+    const uint64_t hi = std::min<uint64_t>(t->n, (first_block + nblocks) * s.block);
+    if (!d_y || !aligned16(d_y)) return LCT_ERR_INVALID_ARG;
+    Range r[7];
+    regions(t, s, r);
+    for (int i = 0; i < 6; ++i)
+        if (overlap(r[i], range_of(d_y, 2 * (hi - lo)))) return LCT_ERR_INVALID_ARG;
+    DecodeArgs a;
+    a.t = dev_view(t, s);
+    a.y = d_y;
+    a.cb = dev_codebook(*cb);
+    a.wait_ns = kDefaultWaitNs;
+    a.first_block = static_cast<uint32_t>(first_block);
+    a.pad = 0;
+    return launch_decode(a, static_cast<uint32_t>(nblocks), static_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? LCT_OK
+               : LCT_ERR_CUDA;
 }
 
 extern "C" lct_status lct_sgd_step_fused(const lct_tensor *W_in, const lct_codebook *cbW, const lct_tensor *M,

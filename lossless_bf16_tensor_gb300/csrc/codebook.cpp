@@ -30,13 +30,19 @@ double cdf_abs(int model, double scale, double shape, double t)
 }
 
 // Integer weight of every biased-exponent bucket: mass * 2^40, rounded.
-std::array<uint64_t, 256> bucket_weights(int model, double scale, double shape)
+// With a point mass at zero the model's masses are scaled by (1 - zero) and
+// the point mass is added to bucket 0.
+std::array<uint64_t, 256> bucket_weights(int model, double scale, double shape, bool atom, double zero)
 {
     std::array<uint64_t, 256> w{};
     for (int e = 0; e < 255; ++e) {
         const double lo = e == 0 ? 0.0 : std::ldexp(1.0, e - 127);
         const double hi = e == 254 ? HUGE_VAL : std::ldexp(1.0, e - 126);
-        const double p = cdf_abs(model, scale, shape, hi) - cdf_abs(model, scale, shape, lo);
+        double p = cdf_abs(model, scale, shape, hi) - cdf_abs(model, scale, shape, lo);
+        if (atom) {
+            p = (1.0 - zero) * p;
+            if (e == 0) p = p + zero;
+        }
         w[e] = static_cast<uint64_t>(std::llround(std::ldexp(p, 40)));
     }
     w[255] = 0;
@@ -114,6 +120,7 @@ uint32_t fnv1a(const lct_codebook &cb)
     for (int s = 0; s < 256; ++s) mix(cb.code[s]);
     mix(cb.esc_len);
     mix(cb.esc_code);
+    mix(static_cast<uint8_t>(cb.zero_atom));
     return h;
 }
 
@@ -125,7 +132,7 @@ uint32_t codebook_hash(const lct_codebook &cb) { return fnv1a(cb); }
 // the escape form a complete prefix code, and the window table agrees.
 bool codebook_valid(const lct_codebook &cb)
 {
-    if (cb.esc_len < 1 || cb.esc_len > LCT_MAX_CODE_BITS) return false;
+    if (cb.esc_len < 1 || cb.esc_len > LCT_MAX_CODE_BITS || cb.zero_atom > 1) return false;
     uint32_t kraft = 1u << (LCT_MAX_CODE_BITS - cb.esc_len);
     for (int s = 0; s < 256; ++s) {
         if (cb.len[s] > LCT_MAX_CODE_BITS) return false;
@@ -144,16 +151,19 @@ bool codebook_valid(const lct_codebook &cb)
 
 }  // namespace lct
 
-extern "C" lct_status lct_codebook_build(int model, double scale, double shape, lct_codebook *out)
+namespace lct {
+namespace {
+
+lct_status build(int model, double scale, double shape, bool atom, double zero, lct_codebook *out)
 {
-    using namespace lct;
     if (!out) return LCT_ERR_INVALID_ARG;
     if (model < LCT_MODEL_GAUSSIAN || model > LCT_MODEL_POWERLAW) return LCT_ERR_INVALID_ARG;
     if (!(scale > 0.0) || std::isinf(scale)) return LCT_ERR_INVALID_ARG;
     if (model == LCT_MODEL_POWERLAW && (!(shape > 0.0) || std::isinf(shape)))
         return LCT_ERR_INVALID_ARG;
+    if (atom && !(zero >= 0.0 && zero < 1.0)) return LCT_ERR_INVALID_ARG;
 
-    const std::array<uint64_t, 256> w = bucket_weights(model, scale, shape);
+    const std::array<uint64_t, 256> w = bucket_weights(model, scale, shape, atom, zero);
 
     // Buckets of nonzero weight, heaviest first (smaller exponent on ties).
     std::vector<int> ranked;
@@ -242,7 +252,23 @@ extern "C" lct_status lct_codebook_build(int model, double scale, double shape, 
     cb.model = model;
     cb.scale = scale;
     cb.shape = model == LCT_MODEL_POWERLAW ? shape : 0.0;
+    cb.zero_frac = atom ? zero : 0.0;
+    cb.zero_atom = atom ? 1u : 0u;
     cb.hash = fnv1a(cb);
     *out = cb;
     return LCT_OK;
+}
+
+}  // namespace
+}  // namespace lct
+
+extern "C" lct_status lct_codebook_build(int model, double scale, double shape, lct_codebook *out)
+{
+    return lct::build(model, scale, shape, false, 0.0, out);
+}
+
+extern "C" lct_status lct_codebook_build_zero_atom(int model, double scale, double shape, double zero_frac,
+                                                   lct_codebook *out)
+{
+    return lct::build(model, scale, shape, true, zero_frac, out);
 }

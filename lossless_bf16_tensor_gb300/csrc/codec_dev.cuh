@@ -54,10 +54,13 @@ __device__ __forceinline__ uint8_t sf_of(uint32_t h) { return (uint8_t)(((h >> 8
 
 // Encode table for shift delta: entry e = {code left-aligned in 32 bits, bit
 // count}.  Symbol s = e - delta gets its own code when it has one; any other
-// exponent costs the escape prefix plus the raw 8-bit exponent.
+// exponent costs the escape prefix plus the raw 8-bit exponent.  With a zero
+// atom, exponent 0 is symbol 0 whatever the shift, and a nonzero exponent
+// the shift maps onto symbol 0 escapes.
 __device__ __forceinline__ uint2 enc_entry(const DevCodebook &cb, int delta, int e)
 {
-    const int s = e - delta;
+    int s = e - delta;
+    if (cb.zero_atom) s = e == 0 ? 0 : (s == 0 ? -1 : s);
     uint32_t code, len;
     if (s >= 0 && s <= 255 && cb.len[s] != 0) {
         code = cb.code[s];
@@ -78,7 +81,8 @@ __device__ __forceinline__ uint32_t dec_entry(const DevCodebook &cb, int delta, 
 {
     const uint32_t d = cb.dec[v], sym = d & 0x1FF, l = d >> 12;
     if (sym == 256) return ((l + 8u) << 27) | ((17u - l) << 16);
-    return (l << 27) | (32u << 16) | (((sym + (uint32_t)delta) & 0xFFu) << 7);
+    const uint32_t e = cb.zero_atom && sym == 0 ? 0u : (sym + (uint32_t)delta) & 0xFFu;
+    return (l << 27) | (32u << 16) | (e << 7);
 }
 
 // ------------------------------------------------------ stream decoding

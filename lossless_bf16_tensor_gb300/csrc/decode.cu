@@ -44,7 +44,7 @@ __global__ void __launch_bounds__(kDecThreads, 4) k_decode(const __grid_constant
     __shared__ uint32_t s_timeout;
 
     const int j = threadIdx.x;
-    const uint32_t b = blockIdx.x;
+    const uint32_t b = blockIdx.x + a.first_block;
     const uint64_t base = (uint64_t)b * G::B;
     const uint32_t nb = (uint32_t)min((uint64_t)G::B, a.t.n - base);
     const uint32_t nrows = (nb + 255) >> 8, nbulk = (nb >> 8) / R, nchunks = (nrows + R - 1) / R;
@@ -90,7 +90,7 @@ __global__ void __launch_bounds__(kDecThreads, 4) k_decode(const __grid_constant
     if (!mbar_wait(&bar_slot, 0, limit)) s_timeout = 1;
     const uint32_t *col = slot_s + j;
     uint32_t pos = 0;  // bit position in the slot
-    uint16_t *yj = a.y + base + j;
+    uint16_t *yj = a.y + (base - (uint64_t)a.first_block * G::B) + j;
 
     for (uint32_t c = 0; c < nchunks; ++c) {
         const bool bulk = c < nbulk;
@@ -147,23 +147,23 @@ __global__ void __launch_bounds__(kDecThreads, 4) k_decode(const __grid_constant
 }
 
 template <int LEVEL>
-cudaError_t launch_level(const DecodeArgs &a, cudaStream_t s)
+cudaError_t launch_level(const DecodeArgs &a, uint32_t nblocks, cudaStream_t s)
 {
     constexpr int smem = DecodeSmem<LEVEL>::kBytes;
     cudaError_t err = cudaFuncSetAttribute(k_decode<LEVEL>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (err != cudaSuccess) return err;
-    return launch_pdl(k_decode<LEVEL>, dim3(a.t.nblocks), dim3(kDecThreads), smem, s, a);
+    return launch_pdl(k_decode<LEVEL>, dim3(nblocks), dim3(kDecThreads), smem, s, a);
 }
 
 }  // namespace dev
 
-cudaError_t launch_decode(const DecodeArgs &a, cudaStream_t s)
+cudaError_t launch_decode(const DecodeArgs &a, uint32_t nblocks, cudaStream_t s)
 {
-    if (a.t.nblocks == 0) return cudaSuccess;
+    if (nblocks == 0) return cudaSuccess;
     switch (a.t.level) {
-    case LCT_LEVEL_CLEAN: return dev::launch_level<LCT_LEVEL_CLEAN>(a, s);
-    case LCT_LEVEL_MEDIUM: return dev::launch_level<LCT_LEVEL_MEDIUM>(a, s);
-    default: return dev::launch_level<LCT_LEVEL_HIGH>(a, s);
+    case LCT_LEVEL_CLEAN: return dev::launch_level<LCT_LEVEL_CLEAN>(a, nblocks, s);
+    case LCT_LEVEL_MEDIUM: return dev::launch_level<LCT_LEVEL_MEDIUM>(a, nblocks, s);
+    default: return dev::launch_level<LCT_LEVEL_HIGH>(a, nblocks, s);
     }
 }
 

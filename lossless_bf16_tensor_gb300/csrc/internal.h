@@ -42,7 +42,8 @@ struct DevCodebook {
     uint16_t dec[256];
     uint8_t esc_len;
     uint8_t esc_code;
-    uint16_t pad;
+    uint8_t zero_atom;  // exponent 0 <-> symbol 0, unshifted
+    uint8_t pad;
     uint32_t hash;
 };
 
@@ -72,9 +73,11 @@ struct EncodeArgs {
 
 struct DecodeArgs {
     DevTensor t;
-    uint16_t *y;
+    uint16_t *y;          // value i of block first_block is y[i]
     DevCodebook cb;
     uint64_t wait_ns;
+    uint32_t first_block;  // the launch decodes blocks first_block .. + grid size
+    uint32_t pad;
 };
 
 struct SgdArgs {
@@ -96,7 +99,7 @@ struct MomentumArgs {
 };
 
 cudaError_t launch_encode(const EncodeArgs &a, cudaStream_t s);
-cudaError_t launch_decode(const DecodeArgs &a, cudaStream_t s);
+cudaError_t launch_decode(const DecodeArgs &a, uint32_t nblocks, cudaStream_t s);
 cudaError_t launch_sgd(const SgdArgs &a, cudaStream_t s);
 cudaError_t launch_momentum(const MomentumArgs &a, cudaStream_t s);
 cudaError_t launch_wait_probe(lct_header *hdr, unsigned long long *work, uint64_t wait_ns,

@@ -1,0 +1,66 @@
+"""Matmul with a compressed operand, decoded one tile at a time.
+
+[EXP] "LCT paper -- Lossless Huffman coding of BF16 training tensors -- What
+does it mean?", paragraph "Read the 3.5x longer context claim carefully":
+decoding inside matmul kernels is named as future work.  Here the compressed
+weight is decoded tile by tile (``lct_decode_blocks``) into a double buffer
+on a side stream while cuBLAS (torch.matmul) consumes the previous tile on
+the caller's stream, so only two tiles of the weight are ever dense.
+
+Only orchestration lives here: decoding runs in liblct's kernels, the GEMM in
+cuBLAS.
+"""
+from __future__ import annotations
+
+import torch
+
+from . import binding as B
+
+
+def tile_rows(ct: B.CompressedTensor, in_features: int, tile_blocks: int) -> int:
+    """Rows of a row-major [out, in] weight that `tile_blocks` blocks hold."""
+    vals = tile_blocks * int(ct.sizes.block)
+    if vals % in_features:
+        raise ValueError("a tile of %d blocks (%d values) does not hold whole rows of %d" %
+                         (tile_blocks, vals, in_features))
+    return vals // in_features
+
+
+def compressed_linear(x: torch.Tensor, w: B.CompressedTensor, cb: B.lct_codebook, out_features: int,
+                      in_features: int, tile_blocks: int = 16) -> torch.Tensor:
+    """y = x @ W^T for a BF16 weight W [out_features, in_features], stored
+    compressed in row-major order; x [..., in_features] BF16 on CUDA.  W is
+    decoded `tile_blocks` blocks (a whole number of rows) at a time."""
+    if w.n != out_features * in_features:
+        raise ValueError("weight size does not match its shape")
+    if x.dtype != torch.bfloat16 or not x.is_cuda or x.shape[-1] != in_features:
+        raise ValueError("x must be a CUDA BF16 tensor [..., in_features]")
+    rows = tile_rows(w, in_features, tile_blocks)
+    main = torch.cuda.current_stream(x.device)
+    side = torch.cuda.Stream(device=x.device)
+    bufs = [torch.empty(rows * in_features, dtype=torch.bfloat16, device=x.device) for _ in range(2)]
+    decoded = [torch.cuda.Event() for _ in range(2)]
+    consumed = [torch.cuda.Event() for _ in range(2)]
+    x2 = x.reshape(-1, in_features)
+    # y^T [out, M]: the rows of one weight tile give contiguous rows of y^T
+    yt = torch.empty(out_features, x2.shape[0], dtype=torch.bfloat16, device=x.device)
+    ntiles = (w.nblocks + tile_blocks - 1) // tile_blocks
+    side.wait_stream(main)  # x, w and the buffers are ready
+    for t in range(ntiles):
+        k = t % 2
+        first = t * tile_blocks
+        count = min(tile_blocks, w.nblocks - first)
+        r0 = t * rows
+        r1 = min(out_features, r0 + rows)
+        tile = bufs[k][:(r1 - r0) * in_features]
+        with torch.cuda.stream(side):
+            if t >= 2:
+                side.wait_event(consumed[k])  # the GEMM two tiles back has read this buffer
+            B.lct_decode_blocks(w, cb, first, count, tile.view(torch.int16), side)
+            decoded[k].record(side)
+        main.wait_event(decoded[k])
+        torch.matmul(tile.view(r1 - r0, in_features), x2.t(), out=yt[r0:r1])
+        consumed[k].record(main)
+    # every decode on the side stream finished before the main stream's last
+    # GEMM, so the buffers (allocated on the main stream) can be freed as usual
+    return yt.t().contiguous().reshape(*x.shape[:-1], out_features)

@@ -22,6 +22,8 @@ and activations):
                     mu = 0.9, eta = 1e-3: SGD with momentum.
 * ``gelu_act``      [8, 4096, 3072] GELU(z), z ~ N(0, 1), seed 5, with 30% of
                     positions set to +0.0; HIGH; scaled by 2^k, k = -4..4.
+* ``gelu_act_zero`` the same activations coded with a zero-atom Gaussian(1)
+                    model (a point mass of 0.3 at zero).
 """
 from __future__ import annotations
 
@@ -84,7 +86,8 @@ def gelu_sparse(n: int, seed: int = 5, zero_frac: float = 0.3) -> np.ndarray:
 
 def scale_pow2(h: np.ndarray, k: int) -> np.ndarray:
     """x * 2^k for BF16 bit patterns (exact while no value leaves the normal range)."""
-    f = bits_to_f32(h) * np.float32(2.0 ** k)
+    with np.errstate(over="ignore", invalid="ignore"):  # infinities and NaNs stay what they are
+        f = bits_to_f32(h) * np.float32(2.0 ** k)
     return bf16_bits(f)
 
 
@@ -122,6 +125,9 @@ WORKLOADS = {
     "gelu_act": dict(n=8 * 4096 * 3072, gen="gelu_sparse", args=dict(seed=5),
                      model="gaussian", scale=1.0, shape=0.0, level="HIGH",
                      pow2=list(range(-4, 5))),
+    "gelu_act_zero": dict(n=8 * 4096 * 3072, gen="gelu_sparse", args=dict(seed=5),
+                          model="gaussian", scale=1.0, shape=0.0, zero_frac=0.3, level="HIGH",
+                          pow2=list(range(-4, 5))),
 }
 
 

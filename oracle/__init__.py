@@ -56,6 +56,7 @@ class Codebook(ctypes.Structure):
         ("median_exp", ctypes.c_int32),
         ("lut_sym", ctypes.c_uint16 * 256),
         ("lut_len", ctypes.c_uint8 * 256),
+        ("zero_atom", ctypes.c_int32),
     ]
 
     def lengths(self) -> np.ndarray:
@@ -97,6 +98,8 @@ def lib():
         l.orc_package_merge.argtypes = [ctypes.c_int, P, P, ctypes.c_int, P]
         l.orc_codebook_from_weights.argtypes = [P, P]
         l.orc_codebook_build.argtypes = [ctypes.c_int, ctypes.c_double, ctypes.c_double, P]
+        l.orc_codebook_build_zero_atom.argtypes = [ctypes.c_int, ctypes.c_double, ctypes.c_double,
+                                                   ctypes.c_double, P]
         l.orc_codebook_assign_codes.argtypes = [P]
         l.orc_shift.argtypes = [P, ctypes.c_uint64, ctypes.c_int]
         l.orc_encode.argtypes = [P, P, P]
@@ -160,6 +163,16 @@ def codebook_from_weights(w) -> Codebook:
 def codebook_build(model: int, scale: float, shape: float = 0.0) -> Codebook:
     cb = Codebook()
     rc = lib().orc_codebook_build(model, scale, shape, ctypes.byref(cb))
+    if rc != OK:
+        raise ValueError("bad model parameters")
+    return cb
+
+
+def codebook_build_zero_atom(model: int, scale: float, shape: float, zero_frac: float) -> Codebook:
+    """A model with a point mass of zero_frac at exponent 0 (zeros), coded
+    as an unshifted symbol 0."""
+    cb = Codebook()
+    rc = lib().orc_codebook_build_zero_atom(model, scale, shape, zero_frac, ctypes.byref(cb))
     if rc != OK:
         raise ValueError("bad model parameters")
     return cb

@@ -320,6 +320,33 @@ int orc_codebook_build(int model, double scale, double shape, orc_codebook *cb)
     return orc_codebook_from_weights(w, cb);
 }
 
+/* A model with a point mass at zero: a fraction zero_frac of the values are
+ * exactly zero (ReLU/GELU activations), the rest follow the model.  Not in
+ * the pages, which note that the user supplies the distribution and that one
+ * which does not fit the tensor raises storage ([EXP] "Read the 3.5x longer
+ * context claim carefully"); (reading) mixture pmf
+ * p'(e) = (1 - z) p(e) + z [e = 0].  The
+ * codebook is marked so that exponent 0 always codes as symbol 0, whatever
+ * the shift, and a nonzero exponent that the shift would map onto symbol 0
+ * is escaped instead (see symbol_code). */
+int orc_codebook_build_zero_atom(int model, double scale, double shape, double zero_frac, orc_codebook *cb)
+{
+    if (!(zero_frac >= 0.0 && zero_frac < 1.0)) return ORC_BAD_ARG;
+    double p[256];
+    uint64_t w[256];
+    int rc = orc_model_pmf(model, scale, shape, p);
+    if (rc != ORC_OK) return rc;
+    for (int e = 0; e < 256; e++) {
+        double mixed = (1.0 - zero_frac) * p[e];
+        if (e == 0) mixed = mixed + zero_frac;
+        p[e] = mixed;
+    }
+    orc_weights_from_pmf(p, w);
+    rc = orc_codebook_from_weights(w, cb);
+    if (rc == ORC_OK) cb->zero_atom = 1;
+    return rc;
+}
+
 /* ---------------------------------------------------------- scale shift */
 
 /* The shift that makes the codebook follow the tensor's scale, from at most
@@ -362,6 +389,11 @@ int orc_shift(const uint16_t *x, uint64_t n, int median_exp)
 static int symbol_code(const orc_codebook *cb, int delta, uint8_t e, uint32_t *code)
 {
     int s = (int)e - delta;
+    if (cb->zero_atom) {
+        /* exponent 0 is the unshifted zero atom; symbol 0 belongs to it alone */
+        if (e == 0) s = 0;
+        else if (s == 0) s = -1;
+    }
     if (s >= 0 && s <= 255 && cb->len[s] > 0) {
         *code = cb->code[s];
         return cb->len[s];
@@ -483,6 +515,8 @@ int orc_decode(const orc_tensor *t, const orc_codebook *cb, uint16_t *y)
                         q++;
                     }
                     ev = (int)lit;
+                } else if (cb->zero_atom && sym == 0) {
+                    ev = 0;
                 } else {
                     ev = sym + t->delta;
                     if (ev < 0 || ev > 255) rc = ORC_CORRUPT;

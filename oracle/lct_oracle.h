@@ -25,6 +25,9 @@
  *                        when the cap does not bind, all-8 special case (pinned)
  *   orc_codebook_*       Kraft equality, prefix freedom, E[len] in [H, H+0.2],
  *                        the pages' 2.5-3.2 bit figures            (pinned)
+ *   ..._zero_atom        mass 1, the plain model's lengths at zero_frac 0,
+ *                        one-bit zero code past p = 2/5, lossless for every
+ *                        shift, 2^k scaling invariance of the markers (pinned)
  *   orc_shift            hand example, 2^k scaling law             (pinned)
  *   orc_encode/decode    bit-exact roundtrip on all 65,536 BF16 patterns,
  *                        hand-worked stream fixture, bit accounting (pinned;
@@ -68,6 +71,7 @@ typedef struct {
     int32_t median_exp;   /* model median of the biased exponent, in [1, 254] */
     uint16_t lut_sym[256];/* 8-bit window -> symbol, or ORC_ESC */
     uint8_t lut_len[256]; /* 8-bit window -> length of the code at its head */
+    int32_t zero_atom;    /* 1: symbol 0 is the zero atom (exponent 0, never shifted) */
 } orc_codebook;
 
 /* One compressed tensor, as plain host arrays owned by the caller. */
@@ -95,6 +99,7 @@ int orc_package_merge(int n, const uint64_t *w, const int32_t *id, int L, uint8_
 
 int orc_codebook_from_weights(const uint64_t w[256], orc_codebook *cb);
 int orc_codebook_build(int model, double scale, double shape, orc_codebook *cb);
+int orc_codebook_build_zero_atom(int model, double scale, double shape, double zero_frac, orc_codebook *cb);
 int orc_codebook_assign_codes(orc_codebook *cb);
 
 int orc_shift(const uint16_t *x, uint64_t n, int median_exp);

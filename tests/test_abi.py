@@ -197,3 +197,59 @@ def test_momentum_host_argument_errors_never_reach_the_device(lct_lib):
     ow5 = _fake_tensor(lct_lib, base=0x50000000)
     ow5.d_sf = w.d_sf + 16                               # partly overlaps W_in's bytes
     assert mom(w, m, ow5, om) == E
+
+
+ZERO_ATOM_MODELS = [(0, 1.0, 0.0, 0.3), (0, 0.02, 0.0, 0.0), (1, 0.01, 0.0, 0.5), (2, 1e-3, 3.0, 0.1),
+                    (0, 1.0, 0.0, 0.95)]
+
+
+@pytest.mark.parametrize("model,scale,shape,zf", ZERO_ATOM_MODELS)
+def test_zero_atom_codebook_matches_oracle(lct_lib, orc, model, scale, shape, zf):
+    cb = lct_lib.lct_codebook_build_zero_atom(model, scale, shape, zf)
+    ref = orc.codebook_build_zero_atom(model, scale, shape, zf)
+    assert cb.zero_atom == 1 and ref.zero_atom == 1 and cb.zero_frac == zf
+    assert bytes(cb.len) == bytes(ref.len)
+    assert list(cb.code) == [int(c) for c in ref.code]
+    assert cb.esc_len == ref.esc_len and cb.esc_code == ref.esc_code
+    assert cb.nsym == ref.k and cb.median_exp == ref.median_exp
+    for v in range(256):
+        assert cb.dec[v] & 0x1FF == ref.lut_sym[v] and cb.dec[v] >> 12 == ref.lut_len[v]
+    # the flag is part of the codebook's identity: the plain model's codes
+    # with zero_frac = 0 hash differently
+    if zf == 0.0:
+        plain = lct_lib.lct_codebook_build(model, scale, shape)
+        assert bytes(plain.len) == bytes(cb.len) and plain.hash != cb.hash
+
+
+def test_zero_atom_rejects_bad_parameters(lct_lib):
+    lib = lct_lib.library()
+    cb = lct_lib.lct_codebook()
+    E = lct_lib.LCT_ERR_INVALID_ARG
+    for zf in (-0.1, 1.0, 1.5, float("nan")):
+        assert lib.lct_codebook_build_zero_atom(0, 1.0, 0.0, zf, ctypes.byref(cb)) == E
+    assert lib.lct_codebook_build_zero_atom(0, -1.0, 0.0, 0.3, ctypes.byref(cb)) == E
+    assert lib.lct_codebook_build_zero_atom(0, 1.0, 0.0, 0.3, None) == E
+    # a codebook whose flag is neither 0 nor 1 is refused by every entry point
+    good = lct_lib.lct_codebook_build_zero_atom(0, 1.0, 0.0, 0.3)
+    good.zero_atom = 2
+    t = _fake_tensor(lct_lib)
+    assert lib.lct_encode(0x20000000, ctypes.byref(good), ctypes.byref(t), None) == E
+
+
+def test_decode_blocks_host_checks(lct_lib):
+    """lct_decode_blocks refuses ranges past the last block and output that
+    overlaps the tensor; an empty range enqueues nothing and succeeds."""
+    lib = lct_lib.library()
+    cb = lct_lib.lct_codebook_build(0, 0.02)
+    E = lct_lib.LCT_ERR_INVALID_ARG
+    t = _fake_tensor(lct_lib, n=3 * 65536 + 5)          # 4 blocks
+    y = 0x60000000
+
+    def dec(first, count, yp=y):
+        return lib.lct_decode_blocks(ctypes.byref(t), ctypes.byref(cb), first, count, yp, None)
+
+    assert dec(0, 5) == E and dec(4, 1) == E and dec(5, 0) == E and dec(2, (1 << 64) - 1) == E
+    assert dec(1, 1, yp=y + 2) == E                      # misaligned
+    assert dec(1, 1, yp=None) == E
+    assert dec(1, 1, yp=t.d_sf) == E                     # overlaps the tensor
+    assert dec(4, 0) == lct_lib.LCT_OK and dec(0, 0) == lct_lib.LCT_OK

@@ -216,3 +216,21 @@ def test_async_on_side_stream():
         B.lct_decode(ct, cb, y, stream=s)
     s.synchronize()
     assert np.array_equal(from_device(y), x)
+
+
+@pytest.mark.parametrize("level", [0, 2])
+def test_decode_blocks_equals_full_decode(level):
+    """Decoding any block range, the ragged last block included, gives the
+    same values as the full decode of those positions."""
+    x, m, s, sh, _ = workload("gelu_act", n=5 * 65536 + 1234)
+    cb, ocb = codebooks(m, s, sh)
+    ct = gpu_encode(x, cb, level)
+    block = 65536 if level == 0 else 32768
+    nb = ct.nblocks
+    for first, count in [(0, 1), (1, 2), (nb - 1, 1), (0, nb), (nb - 3, 3)]:
+        lo, hi = first * block, min(x.size, (first + count) * block)
+        y = torch.empty(hi - lo, dtype=torch.int16, device="cuda")
+        B.lct_decode_blocks(ct, cb, first, count, y)
+        torch.cuda.synchronize()
+        assert np.array_equal(from_device(y), x[lo:hi]), (first, count)
+    assert ct.state().status == 0

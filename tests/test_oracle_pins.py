@@ -585,3 +585,83 @@ def test_momentum_step_spills_and_status_per_output(orc):
     assert M3.status == orc.OK and M3.ovf_used == M2.ovf_used
     rc, got = orc.decode(M3, cbm)
     assert rc == orc.OK
+
+
+# ------------------------------------------------------ zero-atom model
+
+def test_zero_atom_reduces_to_the_plain_model(orc):
+    """With no point mass the mixture is the plain model: same lengths and
+    codes; with one, every other bucket's weight is scaled by 1 - z."""
+    for model, scale, shape in [(0, 1.0, 0.0), (1, 0.01, 0.0), (2, 1e-3, 3.0)]:
+        plain = orc.codebook_build(model, scale, shape)
+        z0 = orc.codebook_build_zero_atom(model, scale, shape, 0.0)
+        assert z0.zero_atom == 1
+        assert np.array_equal(z0.lengths(), plain.lengths()) and np.array_equal(z0.codes(), plain.codes())
+        assert z0.esc_len == plain.esc_len and z0.median_exp == plain.median_exp
+        z = orc.codebook_build_zero_atom(model, scale, shape, 0.3)
+        wp = np.array(plain.weight[:], dtype=np.float64)
+        wz = np.array(z.weight[:], dtype=np.float64)
+        big = wp[1:] > 1e8                                 # integer rounding below 1e-8 relative
+        assert np.allclose(wz[1:][big] / wp[1:][big], 0.7, rtol=1e-8)
+        assert abs(wz.sum() - 2.0 ** 40) < 256          # total mass 1, up to rounding
+        assert z.median_exp == plain.median_exp          # the atom sits outside 1..254
+        _check_codebook(z)
+
+
+def test_zero_atom_above_two_fifths_gets_a_one_bit_code(orc):
+    """A symbol of probability above 2/5 has a one-bit codeword in every
+    optimal prefix code (a textbook property of Huffman codes)."""
+    for zf in (0.41, 0.5, 0.9):
+        cb = orc.codebook_build_zero_atom(0, 1.0, 0.0, zf)
+        assert cb.len[0] == 1
+    assert orc.codebook_build_zero_atom(0, 1.0, 0.0, 0.3).len[0] >= 2
+
+
+def test_zero_atom_lossless_for_every_pattern_and_shift(orc):
+    """All 65,536 BF16 patterns round-trip for shifts that put the zero
+    symbol's collision (a nonzero exponent equal to the shift) anywhere."""
+    x = synth.all_bf16_patterns()
+    cb = orc.codebook_build_zero_atom(0, 1.0, 0.0, 0.3)
+    for level in (orc.CLEAN, orc.HIGH):
+        for delta in (-127, -3, 0, 5, 126, 127):
+            c = orc.encode(x, cb, level, delta=delta)
+            rc, y = orc.decode(c, cb)
+            assert rc == orc.OK and np.array_equal(y, x), (level, delta)
+
+
+def test_zero_atom_codes_zeros_unshifted_and_escapes_the_collision(orc):
+    """Zeros cost len[0] bits whatever the shift; a nonzero value whose
+    exponent equals the shift (symbol 0 after the shift) is escaped with its
+    raw exponent.  Checked on the bits of one stream (MSB first)."""
+    cb = orc.codebook_build_zero_atom(0, 1.0, 0.0, 0.3)
+    l0, c0 = int(cb.len[0]), int(cb.code[0])
+    delta = 40
+    x = np.zeros(65536, np.uint16)                   # +0.0 everywhere
+    x[256] = 0x8000                                  # -0.0, stream 0 symbol 1
+    x[512] = delta << 7                              # exponent == shift, stream 0 symbol 2
+    c = orc.encode(x, cb, orc.CLEAN, delta=delta)
+    bits = "".join(format(int(w), "032b") for w in c.slots.reshape(25, 256)[:, 0])
+    code0 = format(c0, "0%db" % l0)
+    esc = format(int(cb.esc_code), "0%db" % int(cb.esc_len)) + format(delta, "08b")
+    assert bits.startswith(code0 + code0 + esc + code0)
+    # a stream of zeros only holds floor(800 / len0) of them in its slot
+    assert c.markers[1] == min(256, 800 // l0)
+    rc, y = orc.decode(c, cb)
+    assert rc == orc.OK and np.array_equal(y, x)
+
+
+def test_zero_atom_keeps_markers_under_power_of_two_scaling(orc):
+    """x * 2^k moves the shift by k; zeros stay symbol 0 and every other
+    exponent keeps its symbol, so the markers and the spill do not change,
+    and the spill is far below the plain model's (whose zeros escape)."""
+    x0 = synth.gelu_sparse(1 << 17, seed=5)
+    cb = orc.codebook_build_zero_atom(0, 1.0, 0.0, 0.3)
+    plain = orc.encode(x0, orc.codebook_build(0, 1.0), orc.HIGH)
+    ref = None
+    for k in range(-4, 5):
+        c = orc.encode(synth.scale_pow2(x0, k), cb, orc.HIGH)
+        if ref is None:
+            ref, d0 = c, c.delta - k
+        assert c.delta == d0 + k
+        assert np.array_equal(c.markers, ref.markers) and c.ovf_used == ref.ovf_used
+    assert ref.ovf_used < plain.ovf_used / 4

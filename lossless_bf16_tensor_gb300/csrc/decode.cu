@@ -17,8 +17,8 @@ namespace lct {
 namespace dev {
 
 constexpr int kDecThreads = 256;
-constexpr int kDecRows = 16;  // rows per sign-fraction chunk
-constexpr int kDecRing = 4;   // chunks in flight
+constexpr int kDecRows = 32;  // rows per sign-fraction chunk
+constexpr int kDecRing = 2;   // chunks in flight
 
 template <int LEVEL>
 struct DecodeSmem {

@@ -21,8 +21,8 @@ namespace lct {
 namespace dev {
 
 constexpr int kEncThreads = 256;
-constexpr int kEncRows = 8;     // rows per input chunk
-constexpr int kEncRing = 4;     // chunks in flight
+constexpr int kEncRows = 16;    // rows per input chunk
+constexpr int kEncRing = 2;     // chunks in flight
 constexpr int kSpillRows = 32;  // spilled-exponent rows kept
 
 template <int LEVEL>

@@ -26,8 +26,8 @@ namespace lct {
 namespace dev {
 
 constexpr int kMomThreads = 256;
-constexpr int kMomRows = 8;     // rows per chunk
-constexpr int kMomRing = 3;     // chunks in flight
+constexpr int kMomRows = 16;    // rows per chunk
+constexpr int kMomRing = 2;     // chunks in flight
 constexpr int kMomSpill = 32;   // spilled new-exponent rows kept per output (out of place)
 
 // One element: w, m, g as BF16 in bits 0..15.  *mo = bf16(fl32(fl32(mu*m) +

@@ -305,6 +305,8 @@ def run_gpu(args):
             "compression_ratio_all_in": round(ratio_all_in, 5),
             "compression_ratio_payload": round(ratio_payload, 5),
             "overflow_bytes": int(sx.ovf_used),
+            "spill_fraction": round(sx.ovf_used / n, 6),
+            "allocated_bits_per_exponent": round(8.0 * sizes.slot_bytes / n, 4),
         },
         "clocks": clk,
         "e2e": e2e,

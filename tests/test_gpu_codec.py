@@ -234,3 +234,19 @@ def test_decode_blocks_equals_full_decode(level):
         torch.cuda.synchronize()
         assert np.array_equal(from_device(y), x[lo:hi]), (first, count)
     assert ct.state().status == 0
+
+
+def test_compressed_tensor_moves_through_host_memory():
+    """A compressed tensor is self-describing (its header holds no pointer):
+    copied to host memory and back into fresh device buffers, it decodes to
+    the same values, and the fused SGD reads it like the original."""
+    x, m, s, sh, lv = workload("heavy_64m", n=3 * 32768 + 555)
+    cb, ocb = codebooks(m, s, sh)
+    ct = gpu_encode(x, cb, lv)
+    saved = ct.buffer.cpu()                      # checkpoint
+    back = B.CompressedTensor(x.size, lv, zero_fill=False)
+    assert back.buffer.numel() == saved.numel()
+    back.buffer.copy_(saved)                     # resume into other device memory
+    torch.cuda.synchronize()
+    assert np.array_equal(gpu_decode(back, cb), x)
+    assert_same_format(back.to_host(), oracle.encode(x, ocb, lv))

@@ -106,6 +106,26 @@ __device__ __forceinline__ uint32_t rd_take(uint32_t &p, const uint32_t *__restr
     return ent | lit;
 }
 
+// Two symbols of a stream from one 32-bit window: a symbol (escape and
+// literal included) is at most 16 bits, so after the first one the window
+// still holds the whole second one.  Both symbols must lie in the slot (the
+// caller has checked the marker).  Same results as two rd_take calls.
+template <int W>
+__device__ __forceinline__ void rd_take2(uint32_t &p, const uint32_t *__restrict__ col,
+                                         const uint32_t *__restrict__ lut, uint32_t &e0, uint32_t &e1)
+{
+    const uint32_t w = min(p >> 5, (uint32_t)(W - 1));
+    const uint32_t hi = col[w * kStreams], lo = col[(w + 1) * kStreams];
+    const uint32_t win = __funnelshift_l(lo, hi, p);  // the next 32 bits
+    const uint32_t ent0 = lut[win >> 24];
+    const uint32_t l0 = ent0 >> 27;
+    e0 = ent0 | __funnelshift_rc(win, 0u, (ent0 >> 16) & 0xFFu);
+    const uint32_t win1 = win << l0;
+    const uint32_t ent1 = lut[win1 >> 24];
+    e1 = ent1 | __funnelshift_rc(win1, 0u, (ent1 >> 16) & 0xFFu);
+    p += l0 + (ent1 >> 27);
+}
+
 // ------------------------------------------------------- stream coding
 
 // Appends codes most significant bit first into one stream's W-word slot

@@ -103,7 +103,7 @@ __global__ void __launch_bounds__(kDecThreads, 4) k_decode(const __grid_constant
             // bytes), stores last, so nothing orders a load behind a store
             uint32_t e[R], sf[R];
 #pragma unroll
-            for (int r = 0; r < R; ++r) e[r] = rd_take<W>(pos, col, lut);
+            for (int r = 0; r < R; r += 2) rd_take2<W>(pos, col, lut, e[r], e[r + 1]);
 #pragma unroll
             for (int r = 0; r < R; ++r) sf[r] = sfc[r * kStreams];
 #pragma unroll

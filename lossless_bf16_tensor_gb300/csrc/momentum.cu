@@ -259,9 +259,9 @@ __global__ void __launch_bounds__(kMomThreads, INPLACE ? 1 : 2) k_momentum(const
             {
                 uint32_t ew[R], em[R];
 #pragma unroll
-                for (int r = 0; r < R; ++r) {
-                    ew[r] = rd_take<W>(sw.pos, sw.col, lutW);
-                    em[r] = rd_take<W>(sm.pos, sm.col, lutM);
+                for (int r = 0; r < R; r += 2) {
+                    rd_take2<W>(sw.pos, sw.col, lutW, ew[r], ew[r + 1]);
+                    rd_take2<W>(sm.pos, sm.col, lutM, em[r], em[r + 1]);
                 }
 #pragma unroll
                 for (int r = 0; r < R; ++r)

@@ -212,9 +212,9 @@ __global__ void __launch_bounds__(kSgdThreads, SgdSmem<LEVEL, INPLACE>::kCtas) k
             uint32_t ew[R], em[R], h[R], need = 0;
             uint2 ent[R];
 #pragma unroll
-            for (int r = 0; r < R; ++r) {
-                ew[r] = rd_take<W>(sw.pos, sw.col, lutW);
-                em[r] = rd_take<W>(sm.pos, sm.col, lutM);
+            for (int r = 0; r < R; r += 2) {
+                rd_take2<W>(sw.pos, sw.col, lutW, ew[r], ew[r + 1]);
+                rd_take2<W>(sm.pos, sm.col, lutM, em[r], em[r + 1]);
             }
 #pragma unroll
             for (int r = 0; r < R; ++r)

@@ -73,16 +73,25 @@ __device__ __forceinline__ uint2 enc_entry(const DevCodebook &cb, int delta, int
 }
 
 // Decode table for shift delta, indexed by the next 8 bits of the stream:
+//   bits  0..4   s: a left funnel shift of (0 : window) by s brings the
+//                escape literal to bits 7..14 (s = 15 + escape length); 0
+//                for a coded symbol, which yields 0
 //   bits  7..14  the exponent, for a symbol with its own code (0 for escape)
-//   bits 16..23  right shift that brings the escape literal to bits 7..14
-//                (17 - escape length); 32 for a coded symbol, which clears it
 //   bits 27..31  bits consumed (code length, or escape length + 8)
 __device__ __forceinline__ uint32_t dec_entry(const DevCodebook &cb, int delta, int v)
 {
     const uint32_t d = cb.dec[v], sym = d & 0x1FF, l = d >> 12;
-    if (sym == 256) return ((l + 8u) << 27) | ((17u - l) << 16);
+    if (sym == 256) return ((l + 8u) << 27) | (15u + l);
     const uint32_t e = cb.zero_atom && sym == 0 ? 0u : (sym + (uint32_t)delta) & 0xFFu;
-    return (l << 27) | (32u << 16) | (e << 7);
+    return (l << 27) | (e << 7);
+}
+
+// The escape literal of a table entry's symbol at the head of `win` in bits
+// 7..14 (bits above are to be ignored), or 0 for a coded symbol: the
+// funnel shift takes its amount from the entry's low 5 bits.
+__device__ __forceinline__ uint32_t esc_literal(uint32_t win, uint32_t ent)
+{
+    return __funnelshift_l(win, 0u, ent);
 }
 
 // ------------------------------------------------------ stream decoding
@@ -101,9 +110,8 @@ __device__ __forceinline__ uint32_t rd_take(uint32_t &p, const uint32_t *__restr
     const uint32_t hi = col[w * kStreams], lo = col[(w + 1) * kStreams];
     const uint32_t win = __funnelshift_l(lo, hi, p);  // the next 32 bits
     const uint32_t ent = lut[win >> 24];
-    const uint32_t lit = __funnelshift_rc(win, 0u, (ent >> 16) & 0xFFu);  // escape literal, or 0
     p += ent >> 27;
-    return ent | lit;
+    return ent | esc_literal(win, ent);
 }
 
 // Two symbols of a stream from one 32-bit window: a symbol (escape and
@@ -119,10 +127,10 @@ __device__ __forceinline__ void rd_take2(uint32_t &p, const uint32_t *__restrict
     const uint32_t win = __funnelshift_l(lo, hi, p);  // the next 32 bits
     const uint32_t ent0 = lut[win >> 24];
     const uint32_t l0 = ent0 >> 27;
-    e0 = ent0 | __funnelshift_rc(win, 0u, (ent0 >> 16) & 0xFFu);
+    e0 = ent0 | esc_literal(win, ent0);
     const uint32_t win1 = win << l0;
     const uint32_t ent1 = lut[win1 >> 24];
-    e1 = ent1 | __funnelshift_rc(win1, 0u, (ent1 >> 16) & 0xFFu);
+    e1 = ent1 | esc_literal(win1, ent1);
     p += l0 + (ent1 >> 27);
 }
 
@@ -159,6 +167,13 @@ __device__ __forceinline__ void wr_add(Writer &w, const uint2 ent)
     w.hi |= (uint32_t)(v >> 32);
     w.lo |= (uint32_t)v;
     w.nbits += ent.y;
+}
+
+// Append two codes (together at most 32 bits) with one accumulator update:
+// the pair is assembled in one register first.
+__device__ __forceinline__ void wr_add2(Writer &w, const uint2 a, const uint2 b)
+{
+    wr_add(w, make_uint2(a.x | (b.x >> a.y), a.y + b.y));
 }
 
 // Write out the accumulator's first word if it is complete (leaves nbits < 32

@@ -191,8 +191,7 @@ __global__ void __launch_bounds__(kEncThreads, 4) k_encode(const __grid_constant
                 // every stream of the warp keeps the whole chunk in its slot
 #pragma unroll
                 for (int r = 0; r < R; r += 2) {  // two codes fit the accumulator, then one flush
-                    wr_add(wr, ent[r]);
-                    wr_add(wr, ent[r + 1]);
+                    wr_add2(wr, ent[r], ent[r + 1]);
                     wr_flush(wr, col);
                 }
                 wr.rem -= need;

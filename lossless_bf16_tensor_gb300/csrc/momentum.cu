@@ -127,8 +127,7 @@ __device__ __forceinline__ void mom_put_chunk(Writer &wo, const uint32_t (&h)[R]
     if (__all_sync(kFull, wo.alive && need <= wo.rem)) {
 #pragma unroll
         for (int r = 0; r < R; r += 2) {  // two codes fit the accumulator, then one flush
-            wr_add(wo, ent[r]);
-            wr_add(wo, ent[r + 1]);
+            wr_add2(wo, ent[r], ent[r + 1]);
             wr_flush(wo, col);
         }
         wo.rem -= need;

@@ -230,8 +230,7 @@ __global__ void __launch_bounds__(kSgdThreads, SgdSmem<LEVEL, INPLACE>::kCtas) k
                 // every new stream of the warp keeps the whole chunk in its slot
 #pragma unroll
                 for (int r = 0; r < R; r += 2) {  // two codes fit the accumulator, then one flush
-                    wr_add(wo, ent[r]);
-                    wr_add(wo, ent[r + 1]);
+                    wr_add2(wo, ent[r], ent[r + 1]);
                     wr_flush(wo, colO);
                 }
                 wo.rem -= need;

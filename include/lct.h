@@ -307,6 +307,47 @@ lct_status lct_sgd_momentum_step_fused(const lct_tensor *W_in, const lct_codeboo
                                        const lct_codebook *cbM, const uint16_t *d_g, float eta, float mu,
                                        const lct_tensor *W_out, const lct_tensor *M_out, void *stream);
 
+/* Hyper-parameters of one AdamW step (step >= 1 counts the steps taken,
+ * this one included). */
+typedef struct {
+    double lr;
+    double beta1, beta2;   /* in [0, 1) */
+    double eps;            /* > 0 */
+    double weight_decay;   /* decoupled: W <- W - lr*weight_decay*W */
+    uint64_t step;
+} lct_adamw_params;
+
+/* One fused AdamW step on compressed W, M (first moment) and V (second
+ * moment) with a dense BF16 gradient d_g (n values, 16-byte aligned).  The
+ * pages name optimizer state -- buffers the size of the weights that the
+ * optimizer keeps -- among the tensors LCT stores compressed ([EXP] "Jargon",
+ * entry "Optimizer state"; [ABS]) and ask for updates that read and write
+ * compressed tensors in one pass ([EXP] "Training adds a second problem");
+ * they print no optimizer, so this is AdamW with decoupled weight decay.
+ * With float constants rounded once from the parameters in double,
+ *   b1 = beta1, c1 = 1 - beta1, b2 = beta2, c2 = 1 - beta2,
+ *   a = lr / (1 - beta1^step), r = 1 / sqrt(1 - beta2^step), e = eps,
+ *   d = lr * weight_decay,
+ * every value is updated with each float32 operation rounded on its own (no
+ * fused multiply-add; sqrt and division correctly rounded):
+ *   M' = bf16(b1*m + c1*g)
+ *   V' = bf16(b2*v + c2*(g*g))
+ *   W' = bf16((w - d*w) - (a*M') / (sqrt(V')*r + e))
+ * where the weight update takes M' and V' as stored (BF16); rounding to BF16
+ * is round-to-nearest-even with subnormals kept and NaN -> 0x7FC0.  Each
+ * output is coded with its input's codebook and stored shift.  Two passes:
+ * one kernel writes M' and V', a second one W' (reading M' and V').
+ * All six tensors must have the same n and level.  Each output may share
+ * d_header, d_sf, d_slots, d_markers and d_blk_off with its own input (in
+ * place) but not partly overlap them; its d_ovf and d_work must be apart from
+ * every input region; an output must not overlap another output or another
+ * tensor's input, and d_g must not overlap any output.  Each output latches
+ * its own status; LCT_ERR_INVALID_ARG for bad parameters. */
+lct_status lct_adamw_step_fused(const lct_tensor *W_in, const lct_codebook *cbW, const lct_tensor *M_in,
+                                const lct_codebook *cbM, const lct_tensor *V_in, const lct_codebook *cbV,
+                                const uint16_t *d_g, const lct_adamw_params *p, const lct_tensor *W_out,
+                                const lct_tensor *M_out, const lct_tensor *V_out, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

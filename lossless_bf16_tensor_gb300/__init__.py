@@ -14,7 +14,7 @@ not built; nothing falls back to the CPU.
 """
 
 _BINDING_NAMES = {"lct_codebook_build", "lct_codebook_build_zero_atom", "lct_encode", "lct_decode", "lct_decode_blocks", "lct_sgd_step_fused",
-                  "lct_sgd_momentum_step_fused", "lct_encode_static_scratch",
+                  "lct_sgd_momentum_step_fused", "lct_adamw_step_fused", "lct_encode_static_scratch",
                   "lct_compressed_size", "lct_debug_wait_timeout", "CompressedTensor", "LctError",
                   "library"}
 

@@ -55,6 +55,11 @@ class lct_codebook(ctypes.Structure):
                 ("zero_frac", ctypes.c_double), ("zero_atom", ctypes.c_uint32), ("reserved", ctypes.c_uint32)]
 
 
+class lct_adamw_params(ctypes.Structure):
+    _fields_ = [("lr", ctypes.c_double), ("beta1", ctypes.c_double), ("beta2", ctypes.c_double),
+                ("eps", ctypes.c_double), ("weight_decay", ctypes.c_double), ("step", ctypes.c_uint64)]
+
+
 class lct_tensor(ctypes.Structure):
     _fields_ = [("n", ctypes.c_uint64), ("level", ctypes.c_int32), ("reserved", ctypes.c_int32),
                 ("d_header", ctypes.c_void_p), ("d_sf", ctypes.c_void_p), ("d_slots", ctypes.c_void_p),
@@ -89,11 +94,15 @@ _lib.lct_sgd_momentum_step_fused.argtypes = [ctypes.POINTER(lct_tensor), ctypes.
                                              ctypes.POINTER(lct_tensor), ctypes.POINTER(lct_codebook), _P,
                                              ctypes.c_float, ctypes.c_float, ctypes.POINTER(lct_tensor),
                                              ctypes.POINTER(lct_tensor), _P]
+_lib.lct_adamw_step_fused.argtypes = [ctypes.POINTER(lct_tensor), ctypes.POINTER(lct_codebook)] * 3 + [
+    _P, ctypes.POINTER(lct_adamw_params), ctypes.POINTER(lct_tensor), ctypes.POINTER(lct_tensor),
+    ctypes.POINTER(lct_tensor), _P]
 _lib.lct_debug_wait_timeout.argtypes = [_P, _P, ctypes.c_uint64, _P]
 _lib.lct_encode_static_scratch.argtypes = [_P, ctypes.POINTER(lct_codebook), ctypes.POINTER(lct_tensor), _P]
 for _fn in ("lct_codebook_build", "lct_codebook_build_zero_atom", "lct_compressed_size", "lct_encode", "lct_decode",
             "lct_decode_blocks", "lct_sgd_step_fused",
-            "lct_sgd_momentum_step_fused", "lct_debug_wait_timeout", "lct_encode_static_scratch"):
+            "lct_sgd_momentum_step_fused", "lct_adamw_step_fused", "lct_debug_wait_timeout",
+            "lct_encode_static_scratch"):
     getattr(_lib, _fn).restype = ctypes.c_int
 
 
@@ -198,6 +207,18 @@ def lct_sgd_momentum_step_fused(W_in: "CompressedTensor", cbW: lct_codebook, M_i
                                             ctypes.byref(cbM), ptr, ctypes.c_float(eta), ctypes.c_float(mu),
                                             ctypes.byref(W_out.desc), ctypes.byref(M_out.desc), _stream(stream)),
            "lct_sgd_momentum_step_fused")
+
+
+def lct_adamw_step_fused(W_in: "CompressedTensor", cbW: lct_codebook, M_in: "CompressedTensor", cbM: lct_codebook,
+                         V_in: "CompressedTensor", cbV: lct_codebook, g: torch.Tensor, lr: float, beta1: float,
+                         beta2: float, eps: float, weight_decay: float, step: int, W_out: "CompressedTensor",
+                         M_out: "CompressedTensor", V_out: "CompressedTensor", stream=None) -> None:
+    ptr = _dev_ptr(g, W_in.n) if W_in.n else None
+    p = lct_adamw_params(float(lr), float(beta1), float(beta2), float(eps), float(weight_decay), int(step))
+    _check(_lib.lct_adamw_step_fused(ctypes.byref(W_in.desc), ctypes.byref(cbW), ctypes.byref(M_in.desc),
+                                     ctypes.byref(cbM), ctypes.byref(V_in.desc), ctypes.byref(cbV), ptr,
+                                     ctypes.byref(p), ctypes.byref(W_out.desc), ctypes.byref(M_out.desc),
+                                     ctypes.byref(V_out.desc), _stream(stream)), "lct_adamw_step_fused")
 
 
 def lct_debug_wait_timeout(header: torch.Tensor, work: torch.Tensor, limit_ns: int, stream=None) -> None:

@@ -2,6 +2,7 @@
 // argument checks, sizing, and kernel launches.  No device memory is ever
 // allocated here; every buffer belongs to the caller.
 #include <algorithm>
+#include <cmath>
 #include <cstdint>
 #include <cstring>
 
@@ -250,16 +251,19 @@ extern "C" lct_status lct_sgd_step_fused(const lct_tensor *W_in, const lct_codeb
                 if (!same && overlap(ro[i], rw[k])) return LCT_ERR_INVALID_ARG;
             }
     }
-    SgdArgs a;
-    a.w_in = dev_view(W_in, sw);
-    a.m = dev_view(M, sm);
+    UpdateArgs a;
+    std::memset(&a, 0, sizeof(a));
+    a.in[0] = dev_view(W_in, sw);
+    a.in[1] = dev_view(M, sm);
     a.w_out = dev_view(W_out, so);
-    a.cbw = dev_codebook(*cbW);
-    a.cbm = dev_codebook(*cbM);
-    a.eta = eta;
+    a.cb[0] = dev_codebook(*cbW);
+    a.cb[1] = dev_codebook(*cbM);
+    a.k[0] = eta;
+    a.op = OP_SGD;
+    a.nin = 2;
     a.in_place = W_out->d_sf == W_in->d_sf ? 1u : 0u;
     a.wait_ns = kDefaultWaitNs;
-    return launch_sgd(a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? LCT_OK : LCT_ERR_CUDA;
+    return launch_update(a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? LCT_OK : LCT_ERR_CUDA;
 }
 
 extern "C" lct_status lct_sgd_momentum_step_fused(const lct_tensor *W_in, const lct_codebook *cbW,
@@ -315,12 +319,124 @@ extern "C" lct_status lct_sgd_momentum_step_fused(const lct_tensor *W_in, const 
     a.g = d_g;
     a.cbw = dev_codebook(*cbW);
     a.cbm = dev_codebook(*cbM);
-    a.eta = eta;
-    a.mu = mu;
+    std::memset(a.k, 0, sizeof(a.k));
+    a.k[0] = eta;
+    a.k[1] = mu;
+    a.op = OP2_MOMENTUM;
     a.in_place = (W_out->d_sf == W_in->d_sf || M_out->d_sf == M_in->d_sf) ? 1u : 0u;
-    a.pad = 0;
     a.wait_ns = kDefaultWaitNs;
     return launch_momentum(a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? LCT_OK : LCT_ERR_CUDA;
+}
+
+namespace lct {
+namespace {
+
+// An output tensor against its own input: overflow and scratch apart from
+// every input region, the other regions either the same or disjoint.
+bool output_fits_input(const Range out[7], const Range in[7])
+{
+    for (int k = 0; k < 6; ++k)
+        if (overlap(out[5], in[k]) || overlap(out[6], in[k])) return false;
+    for (int i = 0; i < 5; ++i)
+        for (int k = 0; k < 6; ++k) {
+            const bool same = i == k && out[i].lo == in[k].lo;
+            if (!same && overlap(out[i], in[k])) return false;
+        }
+    return true;
+}
+
+}  // namespace
+}  // namespace lct
+
+extern "C" lct_status lct_adamw_step_fused(const lct_tensor *W_in, const lct_codebook *cbW, const lct_tensor *M_in,
+                                           const lct_codebook *cbM, const lct_tensor *V_in, const lct_codebook *cbV,
+                                           const uint16_t *d_g, const lct_adamw_params *p, const lct_tensor *W_out,
+                                           const lct_tensor *M_out, const lct_tensor *V_out, void *stream)
+{
+    const lct_tensor *ins[3] = {W_in, M_in, V_in}, *outs[3] = {W_out, M_out, V_out};
+    const lct_codebook *cbs[3] = {cbW, cbM, cbV};
+    lct_sizes si[3], so[3];
+    lct_status rc;
+    for (int i = 0; i < 3; ++i) {
+        if ((rc = check_tensor(ins[i], false, &si[i])) != LCT_OK) return rc;
+        if ((rc = check_tensor(outs[i], true, &so[i])) != LCT_OK) return rc;
+        if (!cbs[i] || !codebook_valid(*cbs[i])) return LCT_ERR_INVALID_ARG;
+    }
+    if (!p || !(p->step >= 1) || !(p->beta1 >= 0.0 && p->beta1 < 1.0) || !(p->beta2 >= 0.0 && p->beta2 < 1.0) ||
+        !(p->eps > 0.0) || !std::isfinite(p->lr) || !std::isfinite(p->weight_decay) || !std::isfinite(p->eps))
+        return LCT_ERR_INVALID_ARG;
+    const uint64_t n = W_in->n;
+    for (int i = 0; i < 3; ++i) {
+        if (ins[i]->n != n || outs[i]->n != n) return LCT_ERR_INVALID_ARG;
+        if (ins[i]->level != W_in->level || outs[i]->level != W_in->level) return LCT_ERR_UNSUPPORTED;
+    }
+    if (n > 0 && (!d_g || !aligned16(d_g))) return LCT_ERR_INVALID_ARG;
+    Range ri[3][7], ro[3][7];
+    for (int i = 0; i < 3; ++i) {
+        regions(ins[i], si[i], ri[i]);
+        regions(outs[i], so[i], ro[i]);
+    }
+    if (n > 0) {
+        const Range rg = range_of(d_g, 2 * n);
+        for (int o = 0; o < 3; ++o) {
+            for (int r = 0; r < 7; ++r)
+                if (overlap(ro[o][r], rg)) return LCT_ERR_INVALID_ARG;
+            // an output against the other outputs and the other inputs
+            for (int q = 0; q < 3; ++q) {
+                if (q == o) continue;
+                for (int r = 0; r < 7; ++r)
+                    for (int t = 0; t < 7; ++t) {
+                        if (overlap(ro[o][r], ro[q][t])) return LCT_ERR_INVALID_ARG;
+                        if (t < 6 && overlap(ro[o][r], ri[q][t])) return LCT_ERR_INVALID_ARG;
+                    }
+            }
+            if (!output_fits_input(ro[o], ri[o])) return LCT_ERR_INVALID_ARG;
+        }
+    }
+    // the step's constants, rounded to float once
+    const double t = static_cast<double>(p->step);
+    float k[8];
+    k[0] = static_cast<float>(p->beta1);
+    k[1] = static_cast<float>(1.0 - p->beta1);
+    k[2] = static_cast<float>(p->beta2);
+    k[3] = static_cast<float>(1.0 - p->beta2);
+    k[4] = static_cast<float>(p->lr / (1.0 - std::pow(p->beta1, t)));
+    k[5] = static_cast<float>(1.0 / std::sqrt(1.0 - std::pow(p->beta2, t)));
+    k[6] = static_cast<float>(p->eps);
+    k[7] = static_cast<float>(p->lr * p->weight_decay);
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+
+    // pass 1: the moments (M, V and the gradient in, M' and V' out)
+    MomentumArgs m;
+    m.w_in = dev_view(M_in, si[1]);
+    m.m_in = dev_view(V_in, si[2]);
+    m.w_out = dev_view(M_out, so[1]);
+    m.m_out = dev_view(V_out, so[2]);
+    m.g = d_g;
+    m.cbw = dev_codebook(*cbM);
+    m.cbm = dev_codebook(*cbV);
+    std::memcpy(m.k, k, sizeof(k));
+    m.op = OP2_ADAM_MOMENTS;
+    m.in_place = (M_out->d_sf == M_in->d_sf || V_out->d_sf == V_in->d_sf) ? 1u : 0u;
+    m.wait_ns = kDefaultWaitNs;
+    if (launch_momentum(m, st) != cudaSuccess) return LCT_ERR_CUDA;
+
+    // pass 2: the weight (W, M' and V' in, W' out)
+    UpdateArgs a;
+    std::memset(&a, 0, sizeof(a));
+    a.in[0] = dev_view(W_in, si[0]);
+    a.in[1] = dev_view(M_out, so[1]);
+    a.in[2] = dev_view(V_out, so[2]);
+    a.w_out = dev_view(W_out, so[0]);
+    a.cb[0] = dev_codebook(*cbW);
+    a.cb[1] = dev_codebook(*cbM);
+    a.cb[2] = dev_codebook(*cbV);
+    std::memcpy(a.k, k, sizeof(k));
+    a.op = OP_ADAMW;
+    a.nin = 3;
+    a.in_place = W_out->d_sf == W_in->d_sf ? 1u : 0u;
+    a.wait_ns = kDefaultWaitNs;
+    return launch_update(a, st) == cudaSuccess ? LCT_OK : LCT_ERR_CUDA;
 }
 
 // ------------------------------------------------------------ test hook

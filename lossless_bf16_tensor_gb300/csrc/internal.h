@@ -80,27 +80,38 @@ struct DecodeArgs {
     uint32_t pad;
 };
 
-struct SgdArgs {
-    DevTensor w_in, m, w_out;
-    DevCodebook cbw, cbm;
-    float eta;
-    uint32_t in_place;  // W_out's sign-fraction bytes are W_in's
+// Weight updates of the fused one-pass kernel.
+enum : uint32_t { OP_SGD = 0, OP_ADAMW = 1 };
+
+struct UpdateArgs {
+    DevTensor in[3];      // W, M, and V for AdamW
+    DevTensor w_out;
+    DevCodebook cb[3];
+    float k[8];           // the step's constants (SGD: k[0] = eta)
+    uint32_t op;          // OP_SGD or OP_ADAMW
+    uint32_t nin;         // inputs used: 2 or 3
+    uint32_t in_place;    // W_out's sign-fraction bytes are W_in's
+    uint32_t pad;
     uint64_t wait_ns;
 };
 
+// Updates of the fused two-state kernel (two compressed tensors and a dense
+// gradient in, both tensors out).
+enum : uint32_t { OP2_MOMENTUM = 0, OP2_ADAM_MOMENTS = 1 };
+
 struct MomentumArgs {
-    DevTensor w_in, m_in, w_out, m_out;
+    DevTensor w_in, m_in, w_out, m_out;  // the two states (W and M, or AdamW's M and V)
     const uint16_t *g;  // dense BF16 gradient, n values
     DevCodebook cbw, cbm;
-    float eta, mu;
+    float k[8];         // the step's constants (momentum: k[0] = eta, k[1] = mu)
+    uint32_t op;        // OP2_MOMENTUM or OP2_ADAM_MOMENTS
     uint32_t in_place;  // an output shares its input's sign-fraction bytes
-    uint32_t pad;
     uint64_t wait_ns;
 };
 
 cudaError_t launch_encode(const EncodeArgs &a, cudaStream_t s);
 cudaError_t launch_decode(const DecodeArgs &a, uint32_t nblocks, cudaStream_t s);
-cudaError_t launch_sgd(const SgdArgs &a, cudaStream_t s);
+cudaError_t launch_update(const UpdateArgs &a, cudaStream_t s);
 cudaError_t launch_momentum(const MomentumArgs &a, cudaStream_t s);
 cudaError_t launch_wait_probe(lct_header *hdr, unsigned long long *work, uint64_t wait_ns,
                               cudaStream_t s);

@@ -1,5 +1,9 @@
-// Fused compressed SGD-with-momentum step of liblct:
-//   M <- bf16(mu*M + g),  W <- bf16(W - eta*M)
+// Fused compressed two-state updates of liblct, one pass reading two
+// compressed tensors and a dense BF16 gradient and writing both tensors back:
+//   SGD with momentum:  M <- bf16(mu*M + g),  W <- bf16(W - eta*M)
+//   AdamW's moments:    M <- bf16(b1*M + (1-b1)*g),  V <- bf16(b2*V + (1-b2)*g*g)
+// (the AdamW weight update then runs in the one-pass weight kernel).  Below,
+// "W" and "M" name the first and second state.
 //
 // [EXP] "Jargon", entry "Optimizer state": the momentum buffer of SGD with
 // momentum is the optimizer state the pages have in mind; [ABS]: optimizer
@@ -30,15 +34,34 @@ constexpr int kMomRows = 16;    // rows per chunk
 constexpr int kMomRing = 2;     // chunks in flight
 constexpr int kMomSpill = 32;   // spilled new-exponent rows kept per output (out of place)
 
-// One element: w, m, g as BF16 in bits 0..15.  *mo = bf16(fl32(fl32(mu*m) +
-// g)); returns bf16(fl32(w - fl32(eta * mo))).
-__device__ __forceinline__ uint32_t momentum_one(uint32_t w, uint32_t m, uint32_t g, float eta, float mu,
-                                                 uint32_t *mo)
-{
-    const uint32_t mn = bf16_rne(__fadd_rn(__fmul_rn(mu, bf16_f(m)), bf16_f(g)));
-    *mo = mn;
-    return bf16_rne(__fsub_rn(bf16_f(w), __fmul_rn(eta, bf16_f(mn))));
-}
+// The element update of the two states a and b with the gradient g (BF16 in
+// bits 0..15): returns the new a, stores the new b in *bo.
+template <int OP>
+struct TwoStateOp;
+
+// SGD with momentum, a = w, b = m: b' = bf16(fl32(fl32(mu*m) + g)),
+// a' = bf16(fl32(w - fl32(eta*b'))), with k0 = eta, k1 = mu.
+template <>
+struct TwoStateOp<OP2_MOMENTUM> {
+    __device__ static __forceinline__ uint32_t apply(uint32_t w, uint32_t m, uint32_t g, const float *k, uint32_t *bo)
+    {
+        const uint32_t mn = bf16_rne(__fadd_rn(__fmul_rn(k[1], bf16_f(m)), bf16_f(g)));
+        *bo = mn;
+        return bf16_rne(__fsub_rn(bf16_f(w), __fmul_rn(k[0], bf16_f(mn))));
+    }
+};
+
+// AdamW's moments, a = m, b = v: a' = bf16(fl32(k0*m) + fl32(k1*g)),
+// b' = bf16(fl32(k2*v) + fl32(k3*fl32(g*g))), every operation rounded on its own.
+template <>
+struct TwoStateOp<OP2_ADAM_MOMENTS> {
+    __device__ static __forceinline__ uint32_t apply(uint32_t m, uint32_t v, uint32_t g, const float *k, uint32_t *bo)
+    {
+        const float gf = bf16_f(g);
+        *bo = bf16_rne(__fadd_rn(__fmul_rn(k[2], bf16_f(v)), __fmul_rn(k[3], __fmul_rn(gf, gf))));
+        return bf16_rne(__fadd_rn(__fmul_rn(k[0], bf16_f(m)), __fmul_rn(k[1], gf)));
+    }
+};
 
 template <int LEVEL, bool INPLACE>
 struct MomSmem {
@@ -140,9 +163,10 @@ __device__ __forceinline__ void mom_put_chunk(Writer &wo, const uint32_t (&h)[R]
     }
 }
 
-template <int LEVEL, bool INPLACE>
+template <int LEVEL, bool INPLACE, int OP>
 __global__ void __launch_bounds__(kMomThreads, INPLACE ? 1 : 2) k_momentum(const __grid_constant__ MomentumArgs a)
 {
+    using Op = TwoStateOp<OP>;
     using G = Geo<LEVEL>;
     using L = MomSmem<LEVEL, INPLACE>;
     constexpr int W = G::W, R = kMomRows, S = kMomRing, SP = L::kSpillRows;
@@ -240,7 +264,9 @@ __global__ void __launch_bounds__(kMomThreads, INPLACE ? 1 : 2) k_momentum(const
     uint32_t *colM = a.m_out.slots + (uint64_t)b * W * kStreams + j;
     uint8_t *sfWj = a.w_out.sf + base + j;
     uint8_t *sfMj = a.m_out.sf + base + j;
-    const float eta = a.eta, mu = a.mu;
+    float kc[8];  // the step's constants
+#pragma unroll
+    for (int i = 0; i < 8; ++i) kc[i] = a.k[i];
 
     for (uint32_t c = 0; c < nchunks; ++c) {
         const bool bulk = c < nbulk;
@@ -264,8 +290,8 @@ __global__ void __launch_bounds__(kMomThreads, INPLACE ? 1 : 2) k_momentum(const
                 }
 #pragma unroll
                 for (int r = 0; r < R; ++r)
-                    hW[r] = momentum_one(join_one(sfwc[r * kStreams], ew[r]), join_one(sfmc[r * kStreams], em[r]),
-                                         gc[r * kStreams], eta, mu, &hM[r]);
+                    hW[r] = Op::apply(join_one(sfwc[r * kStreams], ew[r]), join_one(sfmc[r * kStreams], em[r]),
+                                      gc[r * kStreams], kc, &hM[r]);
             }
 #pragma unroll
             for (int r = 0; r < R; ++r) {
@@ -285,7 +311,7 @@ __global__ void __launch_bounds__(kMomThreads, INPLACE ? 1 : 2) k_momentum(const
                 const uint32_t fm = bulk ? sfmc[r * kStreams] : a.m_in.sf[at];
                 const uint32_t gv = bulk ? gc[r * kStreams] : a.g[at];
                 uint32_t hMo;
-                const uint32_t hWo = momentum_one(join_one(fw, ew), join_one(fm, em), gv, eta, mu, &hMo);
+                const uint32_t hWo = Op::apply(join_one(fw, ew), join_one(fm, em), gv, kc, &hMo);
                 const uint32_t eW = exp_of(hWo), eM = exp_of(hMo);
                 sfWj[row0 + r * kStreams] = sf_of(hWo);
                 sfMj[row0 + r * kStreams] = sf_of(hMo);
@@ -373,8 +399,8 @@ __global__ void __launch_bounds__(kMomThreads, INPLACE ? 1 : 2) k_momentum(const
                 if (k < first) continue;
                 const uint64_t at = base + (uint64_t)k * kStreams + j;
                 uint32_t hMo;
-                const uint32_t hWo = momentum_one(join_one(a.w_in.sf[at], ew), join_one(a.m_in.sf[at], em), a.g[at],
-                                                  eta, mu, &hMo);
+                const uint32_t hWo = Op::apply(join_one(a.w_in.sf[at], ew), join_one(a.m_in.sf[at], em), a.g[at], kc,
+                                               &hMo);
                 if (redo_w && k >= mk_w) out_w[pre_w + (k - mk_w)] = exp_of(hWo);
                 if (redo_m && k >= mk_m) out_m[pre_m + (k - mk_m)] = exp_of(hMo);
             }
@@ -392,20 +418,27 @@ __global__ void __launch_bounds__(kMomThreads, INPLACE ? 1 : 2) k_momentum(const
     }
 }
 
-template <int LEVEL, bool INPLACE>
+template <int LEVEL, bool INPLACE, int OP>
 cudaError_t launch_level(const MomentumArgs &a, cudaStream_t s)
 {
     constexpr int smem = MomSmem<LEVEL, INPLACE>::kBytes;
     cudaError_t err =
-        cudaFuncSetAttribute(k_momentum<LEVEL, INPLACE>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        cudaFuncSetAttribute(k_momentum<LEVEL, INPLACE, OP>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (err != cudaSuccess) return err;
-    return launch_pdl(k_momentum<LEVEL, INPLACE>, dim3(a.w_out.nblocks), dim3(kMomThreads), smem, s, a);
+    return launch_pdl(k_momentum<LEVEL, INPLACE, OP>, dim3(a.w_out.nblocks), dim3(kMomThreads), smem, s, a);
+}
+
+template <int LEVEL, int OP>
+cudaError_t launch_op_level(const MomentumArgs &a, cudaStream_t s)
+{
+    return a.in_place ? launch_level<LEVEL, true, OP>(a, s) : launch_level<LEVEL, false, OP>(a, s);
 }
 
 template <int LEVEL>
 cudaError_t launch_momentum_level(const MomentumArgs &a, cudaStream_t s)
 {
-    return a.in_place ? launch_level<LEVEL, true>(a, s) : launch_level<LEVEL, false>(a, s);
+    return a.op == OP2_ADAM_MOMENTS ? launch_op_level<LEVEL, OP2_ADAM_MOMENTS>(a, s)
+                                    : launch_op_level<LEVEL, OP2_MOMENTUM>(a, s);
 }
 
 }  // namespace dev

@@ -108,6 +108,9 @@ def lib():
         l.orc_bf16_rne.restype = ctypes.c_uint16
         l.orc_sgd_step.argtypes = [P, P, P, P, ctypes.c_float, P]
         l.orc_sgd_momentum_step.argtypes = [P, P, P, P, P, ctypes.c_float, ctypes.c_float, P, P, P]
+        l.orc_adamw_constants.argtypes = [ctypes.c_double] * 5 + [ctypes.c_uint32, P]
+        l.orc_adamw_constants.restype = None
+        l.orc_adamw_step.argtypes = [P] * 7 + [P, P, P, P, P]
         _lib = l
     return _lib
 
@@ -302,6 +305,35 @@ def sgd_momentum_step(W: Compressed, cbW: Codebook, M: Compressed, cbM: Codebook
         out.delta = int(t.delta)
         out.ovf_used = int(t.ovf_used)
     return w_out, m_out
+
+
+def adamw_constants(lr: float, beta1: float, beta2: float, eps: float, weight_decay: float, t: int) -> np.ndarray:
+    """The eight float constants of one AdamW step (see orc_adamw_constants)."""
+    k = np.zeros(8, np.float32)
+    lib().orc_adamw_constants(lr, beta1, beta2, eps, weight_decay, t, _ptr(k))
+    return k
+
+
+def adamw_step(W: Compressed, cbW: Codebook, M: Compressed, cbM: Codebook, V: Compressed, cbV: Codebook,
+               g: np.ndarray, k: np.ndarray, caps=(None, None, None)):
+    """One AdamW step on compressed W, M, V with a dense BF16 gradient:
+    returns the new (W, M, V)."""
+    g = np.ascontiguousarray(g, dtype=np.uint16).reshape(-1)
+    k = np.ascontiguousarray(k, dtype=np.float32)
+    if g.size != W.n or k.size != 8:
+        raise ValueError("gradient size differs from W, or k is not 8 floats")
+    outs = [Compressed.empty(t.n, t.block, t.slot_words, cap) for t, cap in zip((W, M, V), caps)]
+    ts = [t._struct() for t in (W, M, V)]
+    tos = [o._struct() for o in outs]
+    rc = (ctypes.c_int * 3)()
+    lib().orc_adamw_step(ctypes.byref(ts[0]), ctypes.byref(cbW), ctypes.byref(ts[1]), ctypes.byref(cbM),
+                         ctypes.byref(ts[2]), ctypes.byref(cbV), _ptr(g) if g.size else None, _ptr(k),
+                         ctypes.byref(tos[0]), ctypes.byref(tos[1]), ctypes.byref(tos[2]), rc)
+    for o, t, st in zip(outs, tos, rc):
+        o.status = int(st)
+        o.delta = int(t.delta)
+        o.ovf_used = int(t.ovf_used)
+    return tuple(outs)
 
 
 if __name__ == "__main__":  # pragma: no cover

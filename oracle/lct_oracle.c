@@ -638,3 +638,91 @@ int orc_sgd_momentum_step(const orc_tensor *W, const orc_codebook *cbW, const or
     free(m);
     return st;
 }
+
+/* Constants of one AdamW step, computed once in double from the
+ * hyper-parameters and rounded to float (reading: the step size and the
+ * second-moment correction fold the bias corrections of step t). */
+void orc_adamw_constants(double lr, double beta1, double beta2, double eps, double weight_decay,
+                         uint32_t t, float k[8])
+{
+    k[0] = (float)beta1;
+    k[1] = (float)(1.0 - beta1);
+    k[2] = (float)beta2;
+    k[3] = (float)(1.0 - beta2);
+    k[4] = (float)(lr / (1.0 - pow(beta1, (double)t)));           /* step size */
+    k[5] = (float)(1.0 / sqrt(1.0 - pow(beta2, (double)t)));      /* 1/sqrt(1 - beta2^t) */
+    k[6] = (float)eps;
+    k[7] = (float)(lr * weight_decay);                            /* decoupled decay */
+}
+
+/* AdamW on compressed W, M (first moment) and V (second moment) with a
+ * dense BF16 gradient g ([EXP] "Jargon", entry "Optimizer state": optimizer
+ * states such as momentum buffers are the same size as the weights; [ABS]:
+ * optimizer states are kept compressed).  The pages print no optimizer;
+ * (reading) the AdamW update with decoupled weight decay, every float32
+ * operation rounded on its own (no fused multiply-add), k from
+ * orc_adamw_constants:
+ *   M' = bf16( k0*m + k1*g )
+ *   V' = bf16( k2*v + k3*(g*g) )
+ *   W' = bf16( (w - k7*w) - (k4*M') / (sqrt(V')*k5 + k6) )
+ * with the weight update taking M' and V' as stored (BF16); sqrt and the
+ * division are the correctly rounded IEEE operations.  Each output is coded
+ * with its input's codebook and stored shift.  rc[0..2] get the status of
+ * W', M', V'. */
+int orc_adamw_step(const orc_tensor *W, const orc_codebook *cbW, const orc_tensor *M,
+                   const orc_codebook *cbM, const orc_tensor *V, const orc_codebook *cbV,
+                   const uint16_t *g, const float k[8], orc_tensor *W_out, orc_tensor *M_out,
+                   orc_tensor *V_out, int rc[3])
+{
+    rc[0] = rc[1] = rc[2] = ORC_BAD_ARG;
+    const orc_tensor *in[3] = {W, M, V};
+    orc_tensor *out[3] = {W_out, M_out, V_out};
+    for (int i = 0; i < 3; i++)
+        if (in[i]->n != W->n || out[i]->n != W->n || out[i]->block != in[i]->block ||
+            out[i]->slot_words != in[i]->slot_words)
+            return ORC_BAD_ARG;
+    uint64_t n = W->n;
+    uint16_t *w = (uint16_t *)malloc(2 * (n > 0 ? n : 1));
+    uint16_t *m = (uint16_t *)malloc(2 * (n > 0 ? n : 1));
+    uint16_t *v = (uint16_t *)malloc(2 * (n > 0 ? n : 1));
+    int st = orc_decode(W, cbW, w);
+    if (st == ORC_OK) st = orc_decode(M, cbM, m);
+    if (st == ORC_OK) st = orc_decode(V, cbV, v);
+    if (st == ORC_OK) {
+        for (uint64_t i = 0; i < n; i++) {
+            float gf = bf16_value(g[i]);
+            float a1 = k[0] * bf16_value(m[i]);
+            float a2 = k[1] * gf;
+            float ms = a1 + a2;
+            m[i] = orc_bf16_rne(ms);
+            float b1 = k[2] * bf16_value(v[i]);
+            float gg = gf * gf;
+            float b2 = k[3] * gg;
+            float vs = b1 + b2;
+            v[i] = orc_bf16_rne(vs);
+            float root = sqrtf(bf16_value(v[i]));
+            float scaled = root * k[5];
+            float den = scaled + k[6];
+            float num = k[4] * bf16_value(m[i]);
+            float upd = num / den;
+            float wf = bf16_value(w[i]);
+            float decay = k[7] * wf;
+            float wd = wf - decay;
+            float r = wd - upd;
+            w[i] = orc_bf16_rne(r);
+        }
+        W_out->delta = W->delta;
+        M_out->delta = M->delta;
+        V_out->delta = V->delta;
+        rc[0] = orc_encode(w, cbW, W_out);
+        rc[1] = orc_encode(m, cbM, M_out);
+        rc[2] = orc_encode(v, cbV, V_out);
+        st = rc[0] != ORC_OK ? rc[0] : (rc[1] != ORC_OK ? rc[1] : rc[2]);
+    } else {
+        rc[0] = rc[1] = rc[2] = st;
+    }
+    free(w);
+    free(m);
+    free(v);
+    return st;
+}

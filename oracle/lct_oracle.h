@@ -36,6 +36,8 @@
  *   orc_sgd_step         torch CPU float32 ops + bf16 cast           (pinned)
  *   orc_sgd_momentum_step  torch CPU float32 ops + bf16 casts, one-FMA
  *                        sensitivity, the mu = 0 reduction           (pinned)
+ *   orc_adamw_step       torch CPU float32 ops + bf16 casts, FMA sensitivity,
+ *                        first step from zero moments = sign descent (pinned)
  */
 #ifndef LCT_ORACLE_H
 #define LCT_ORACLE_H
@@ -113,6 +115,12 @@ int orc_sgd_step(const orc_tensor *W, const orc_codebook *cbW, const orc_tensor 
 int orc_sgd_momentum_step(const orc_tensor *W, const orc_codebook *cbW, const orc_tensor *M,
                           const orc_codebook *cbM, const uint16_t *g, float eta, float mu,
                           orc_tensor *W_out, orc_tensor *M_out, int rc[2]);
+void orc_adamw_constants(double lr, double beta1, double beta2, double eps, double weight_decay,
+                         uint32_t t, float k[8]);
+int orc_adamw_step(const orc_tensor *W, const orc_codebook *cbW, const orc_tensor *M,
+                   const orc_codebook *cbM, const orc_tensor *V, const orc_codebook *cbV,
+                   const uint16_t *g, const float k[8], orc_tensor *W_out, orc_tensor *M_out,
+                   orc_tensor *V_out, int rc[3]);
 
 #ifdef __cplusplus
 }

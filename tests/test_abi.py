@@ -253,3 +253,48 @@ def test_decode_blocks_host_checks(lct_lib):
     assert dec(1, 1, yp=None) == E
     assert dec(1, 1, yp=t.d_sf) == E                     # overlaps the tensor
     assert dec(4, 0) == lct_lib.LCT_OK and dec(0, 0) == lct_lib.LCT_OK
+
+
+def test_adamw_host_argument_errors_never_reach_the_device(lct_lib):
+    """Host checks of lct_adamw_step_fused: parameters, sizes, levels, the
+    gradient pointer and the aliasing rules (no CUDA call is made)."""
+    lib = lct_lib.library()
+    cb = lct_lib.lct_codebook_build(0, 0.02)
+    E = lct_lib.LCT_ERR_INVALID_ARG
+    g = 0x6A000000
+    bases = [0x10000000, 0x20000000, 0x30000000, 0x40000000, 0x50000000, 0x70000000]
+
+    def six():
+        return [_fake_tensor(lct_lib, base=x) for x in bases]
+
+    def adam(ts, p=None, gp=g):
+        p = p or lct_lib.lct_adamw_params(1e-3, 0.9, 0.999, 1e-8, 0.01, 1)
+        w, m, v, ow, om, ov = ts
+        return lib.lct_adamw_step_fused(ctypes.byref(w), ctypes.byref(cb), ctypes.byref(m), ctypes.byref(cb),
+                                        ctypes.byref(v), ctypes.byref(cb), gp, ctypes.byref(p), ctypes.byref(ow),
+                                        ctypes.byref(om), ctypes.byref(ov), None)
+
+    P = lct_lib.lct_adamw_params
+    for bad in (P(1e-3, 0.9, 0.999, 1e-8, 0.0, 0), P(1e-3, 1.0, 0.999, 1e-8, 0.0, 1),
+                P(1e-3, 0.9, -0.1, 1e-8, 0.0, 1), P(1e-3, 0.9, 0.999, 0.0, 0.0, 1),
+                P(float("nan"), 0.9, 0.999, 1e-8, 0.0, 1), P(1e-3, 0.9, 0.999, 1e-8, float("inf"), 1)):
+        assert adam(six(), p=bad) == E
+    assert adam(six(), gp=None) == E
+    assert adam(six(), gp=g + 4) == E
+    ts = six()
+    assert adam(ts, gp=ts[3].d_sf) == E                   # gradient overlaps an output
+    ts = six()
+    ts[1] = _fake_tensor(lct_lib, n=999, base=bases[1])
+    assert adam(ts) == E                                  # n mismatch
+    ts = six()
+    ts[5] = _fake_tensor(lct_lib, level=2, base=bases[5])
+    assert adam(ts) == lct_lib.LCT_ERR_UNSUPPORTED
+    ts = six()
+    ts[4] = _fake_tensor(lct_lib, base=bases[2])          # M' written into V
+    assert adam(ts) == E
+    ts = six()
+    ts[3].d_ovf = ts[4].d_ovf                              # two outputs share an overflow region
+    assert adam(ts) == E
+    ts = six()
+    ts[3] = _fake_tensor(lct_lib, base=bases[0])          # W' fully aliases W, overflow included
+    assert adam(ts) == E

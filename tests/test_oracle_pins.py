@@ -665,3 +665,80 @@ def test_zero_atom_keeps_markers_under_power_of_two_scaling(orc):
         assert c.delta == d0 + k
         assert np.array_equal(c.markers, ref.markers) and c.ovf_used == ref.ovf_used
     assert ref.ovf_used < plain.ovf_used / 4
+
+
+# ------------------------------------------------------------ AdamW step
+
+def _adamw_torch(w, m, v, g, k):
+    """The AdamW step as separate torch CPU float32 ops (each rounded)."""
+    kt = [torch.tensor(float(x), dtype=torch.float32) for x in k]
+    wt, mt, vt, gt = (_bf16_tensor(a).float() for a in (w, m, v, g))
+    m_new = _bits((kt[0] * mt) + (kt[1] * gt))
+    v_new = _bits((kt[2] * vt) + (kt[3] * (gt * gt)))
+    mf, vf = _bf16_tensor(m_new).float(), _bf16_tensor(v_new).float()
+    den = (torch.sqrt(vf) * kt[5]) + kt[6]
+    upd = (kt[4] * mf) / den
+    w_new = _bits((wt - (kt[7] * wt)) - upd)
+    return w_new, m_new, v_new, (wt, mf, den, upd)
+
+
+def test_adamw_matches_torch_separate_roundings(orc):
+    """AdamW on compressed weights and moments (optimizer state, [EXP]
+    'Jargon'; [ABS]): M' = bf16(b1*m + (1-b1)*g), V' = bf16(b2*v + (1-b2)*g*g),
+    W' = bf16((w - lr*wd*w) - step*M' / (sqrt(V')*rs + eps)), every float32
+    operation rounded on its own; torch CPU runs the same ops.  A fused
+    multiply-add in the update changes the bits somewhere."""
+    n = 2 * 65536 + 3333
+    w = synth.normal(n, 0.02, 3)
+    m = synth.normal(n, 1e-4, 4)
+    v = synth.bf16_bits(np.abs(synth.bits_to_f32(synth.normal(n, 1e-8, 5))))   # a second moment is >= 0
+    g = synth.normal(n, 1e-4, 6)
+    w[:4] = [0x0000, 0x8000, 0x7F80, 0x0001]
+    m[:4] = [0x0000, 0x3F80, 0x0000, 0x8001]
+    v[:4] = [0x0000, 0x0000, 0x3F80, 0x0001]
+    g[:4] = [0x0000, 0x8000, 0x3F80, 0x0002]
+    k = orc.adamw_constants(1e-3, 0.9, 0.999, 1e-8, 0.01, 7)
+    cbw, cbm, cbv = orc.codebook_build(0, 0.02), orc.codebook_build(0, 1e-4), orc.codebook_build(1, 1e-8)
+    W, M, V = (orc.encode(x, cb, orc.CLEAN) for x, cb in ((w, cbw), (m, cbm), (v, cbv)))
+    W2, M2, V2 = orc.adamw_step(W, cbw, M, cbm, V, cbv, g, k)
+    assert W2.status == M2.status == V2.status == orc.OK
+    assert (W2.delta, M2.delta, V2.delta) == (W.delta, M.delta, V.delta)
+    got = [orc.decode(t, cb)[1] for t, cb in ((W2, cbw), (M2, cbm), (V2, cbv))]
+    w_new, m_new, v_new, (wt, mf, den, upd) = _adamw_torch(w, m, v, g, k)
+    assert np.array_equal(got[1], m_new)
+    assert np.array_equal(got[2], v_new)
+    # NaN results (inf - inf at the +inf weight) are this library's 0x7FC0;
+    # torch keeps the sign of the NaN it computed
+    nan = ((w_new & 0x7F80) == 0x7F80) & ((w_new & 0x7F) != 0)
+    assert nan.sum() == 1 and (got[0][nan] == 0x7FC0).all()
+    assert np.array_equal(got[0][~nan], w_new[~nan])
+    # the check above would catch a fused multiply-add in the moment update
+    kt = [float(x) for x in k]
+    fma_m = _bits((kt[0] * _bf16_tensor(m).double() + torch.tensor(kt[1], dtype=torch.float32).double()
+                   * _bf16_tensor(g).double()).float())
+    assert (fma_m != m_new).any()
+    # ... or the weight step without the decoupled decay
+    no_decay = _bits(wt - upd)
+    assert (no_decay != w_new).any()
+
+
+def test_adamw_first_step_from_zero_moments_is_sign_descent(orc):
+    """From zero moments, step 1 of Adam moves every weight by lr * sign(g)
+    (the bias corrections undo (1 - b1) and (1 - b2) exactly), up to the BF16
+    rounding of the stored moments."""
+    n = 65536 + 100
+    lr = 1e-3
+    w = synth.normal(n, 1e-4, 7)             # |w| small: its BF16 spacing is far below lr
+    g = synth.normal(n, 1e-2, 8)
+    g[g == 0x8000] = 0x0000
+    z = np.zeros(n, np.uint16)
+    k = orc.adamw_constants(lr, 0.9, 0.999, 1e-12, 0.0, 1)
+    cbw, cbm, cbv = orc.codebook_build(0, 1e-4), orc.codebook_build(0, 1e-3), orc.codebook_build(0, 1e-5)
+    W, M, V = orc.encode(w, cbw, orc.CLEAN), orc.encode(z, cbm, orc.CLEAN), orc.encode(z, cbv, orc.CLEAN)
+    W2, _, _ = orc.adamw_step(W, cbw, M, cbm, V, cbv, g, k)
+    _, got = orc.decode(W2, cbw)
+    step = synth.bits_to_f32(got).astype(np.float64) - synth.bits_to_f32(w).astype(np.float64)
+    sign = np.sign(synth.bits_to_f32(g).astype(np.float64))
+    nz = sign != 0
+    assert np.allclose(step[nz], -lr * sign[nz], rtol=2e-2, atol=0)
+    assert np.array_equal(got[~nz], w[~nz])   # zero gradient, zero moments: no move

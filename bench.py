@@ -46,6 +46,9 @@ WORKLOAD_TEXT = {
                      "HIGH; step = encode + decode + fused SGD (M ~ Laplace(0,1e-3))",
     "sgd_162m": "162,000,000 BF16 W ~ N(0,0.02), M ~ N(0,1e-3), Gaussian codebooks, CLEAN; step = encode + decode "
                 "+ fused SGD",
+    "adamw_162m": "162,000,000 BF16 W ~ N(0,0.02), M ~ N(0,1e-4), V = |N(0,1e-8)|, dense BF16 gradient ~ "
+                  "N(0,1e-4), CLEAN, W, M and V updated in place; step = one fused AdamW step (moments pass + "
+                  "weight pass; lr 1e-3, betas 0.9/0.999, eps 1e-8, weight decay 0.01)",
     "momentum_162m": "162,000,000 BF16 W ~ N(0,0.02), M ~ N(0,1e-3), dense BF16 gradient ~ N(0,1e-4), Gaussian "
                      "codebooks, CLEAN, W and M updated in place; step = one fused SGD-with-momentum step "
                      "(mu = 0.9, eta = 1e-3)",
@@ -172,6 +175,8 @@ def run_gpu(args):
     from lossless_bf16_tensor_gb300 import synth
 
     wl = synth.WORKLOADS[args.workload]
+    if "adamw" in wl:
+        return run_gpu_adamw(args, rank, local_rank, world)
     if "gradient" in wl:
         return run_gpu_momentum(args, rank, local_rank, world)
     n = wl["n"]
@@ -476,6 +481,117 @@ def run_gpu_momentum(args, rank, local_rank, world):
     }
 
 
+def run_gpu_adamw(args, rank, local_rank, world):
+    """One fused AdamW step per timed step on compressed W, M and V (all in
+    place, overflow regions ping-pong between steps)."""
+    import torch
+    import torch.distributed as dist
+    from lossless_bf16_tensor_gb300 import binding as B
+    from lossless_bf16_tensor_gb300 import synth
+
+    wl = synth.WORKLOADS[args.workload]
+    n = wl["n"]
+    level = B.LEVELS[wl["level"]]
+    hp = wl["adamw"]
+    cbs = [B.lct_codebook_build(wl["model"], wl["scale"], wl["shape"]),
+           B.lct_codebook_build(wl["momentum"]["model"], wl["momentum"]["scale"]),
+           B.lct_codebook_build(wl["second"]["model"], wl["second"]["scale"])]
+    stream = torch.cuda.current_stream()
+    data = [synth.generate(args.workload), synth.momentum(args.workload), synth.second_moment(args.workload)]
+    T = [B.CompressedTensor(n, level) for _ in range(3)]
+    for x, cb, t in zip(data, cbs, T):
+        B.lct_encode(torch.from_numpy(x.view(np.int16)).cuda(), cb, t, stream)
+    del data
+    grads = [torch.from_numpy(synth.gradient(args.workload, s).view(np.int16)).cuda() for s in (1, 2)]
+    bufs = [T, [B.CompressedTensor(n, level, like=t) for t in T]]
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.int32, device="cuda")
+    count = [0]
+
+    def step():
+        k = count[0]
+        cur, nxt = bufs[k % 2], bufs[(k + 1) % 2]
+        B.lct_adamw_step_fused(cur[0], cbs[0], cur[1], cbs[1], cur[2], cbs[2], grads[k % 2], hp["lr"], hp["beta1"],
+                               hp["beta2"], hp["eps"], hp["weight_decay"], k + 1, nxt[0], nxt[1], nxt[2], stream)
+        count[0] += 1
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    assert all(t.state().status == 0 for t in bufs[count[0] % 2])
+    clocks = ClockSampler(None)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.4)
+    for k in range(args.steps):
+        flush.zero_()
+        evs[k][0].record(stream)
+        step()
+        evs[k][1].record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    clk = clocks.stop()
+    per = [a.elapsed_time(b) for a, b in evs]
+    ms_step = max_over_ranks(sum(per), device="cuda") / args.steps
+    st = [t.state() for t in bufs[count[0] % 2]]
+    assert all(s_.status == 0 for s_ in st)
+    sizes = T[0].sizes
+    ab = [algorithmic_bytes(sizes, s_.ovf_used) for s_ in st]
+    # moments pass: read M, V, g, write M, V; weight pass: read W, M, V, write W
+    alg = 2 * ab[1] + 2 * ab[2] + 2 * n + 2 * ab[0] + ab[1] + ab[2]
+    peak, peak_kind = hbm_peak()
+    achieved = alg / (statistics.mean(per) * 1e-3) / 1e9
+    if rank != 0:
+        return None
+    cpu = None
+    if not (args.no_cpu_baseline or world > 1):
+        dt, nv = oracle_adamw_time(args.workload, args.cpu_blocks or 64)
+        cpu = {"value": round(nv / dt / 1e9, 5), "unit": "Gelem/s", "cores": 1, "kind": "oracle",
+               "sample": "first %d values of %s, one AdamW step; host %s, oracle single-threaded"
+                         % (nv, args.workload, cpu_model()), "seconds": round(dt, 3)}
+    return {
+        "metric": "fused AdamW step on compressed W, M and V: elements per second",
+        "value": round(replica_units(n, world) / (ms_step * 1e-3) / 1e9, 3), "unit": "Gelem/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "u32+f32", "data": "synthetic",
+        "config": {"workload": WORKLOAD_TEXT[args.workload], "name": args.workload, "n": n, "level": wl["level"],
+                   "l2": "flushed before every step (256 MiB write, outside the events)",
+                   "parallelism": "replicas" if world > 1 else "single"},
+        "roofline": {"bound": "hbm", "kernel": "adamw (moments pass + weight pass, one call)",
+                     "achieved": round(achieved, 1), "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "traffic": None, "algorithmic_bytes_per_launch": alg},
+        "breakdown": {"compression_ratio_all_in": [round(2.0 * n / (sizes.fixed_bytes + s_.ovf_used), 5) for s_ in st],
+                      "overflow_bytes": [int(s_.ovf_used) for s_ in st]},
+        "clocks": clk, "e2e": None, "gpu_launches": 4 * args.steps, "cpu_baseline": cpu,
+    }
+
+
+def oracle_adamw_time(workload: str, nblocks_sample: int):
+    """Time one oracle AdamW step on the first `nblocks_sample` blocks."""
+    import oracle
+    from lossless_bf16_tensor_gb300 import synth
+    wl = synth.WORKLOADS[workload]
+    level = {"CLEAN": 0, "MEDIUM": 1, "HIGH": 2}[wl["level"]]
+    block, _ = oracle.geometry(level)
+    k = min(wl["n"], nblocks_sample * block)
+    xs = [synth.generate(workload, k), synth.momentum(workload, k), synth.second_moment(workload, k)]
+    g = synth.gradient(workload, 1, k)
+    model = {"gaussian": 0, "laplace": 1, "powerlaw": 2}
+    cbs = [oracle.codebook_build(model[wl["model"]], wl["scale"]),
+           oracle.codebook_build(model[wl["momentum"]["model"]], wl["momentum"]["scale"]),
+           oracle.codebook_build(model[wl["second"]["model"]], wl["second"]["scale"])]
+    T = [oracle.encode(x, cb, level) for x, cb in zip(xs, cbs)]
+    hp = wl["adamw"]
+    kc = oracle.adamw_constants(hp["lr"], hp["beta1"], hp["beta2"], hp["eps"], hp["weight_decay"], 1)
+    t0 = time.perf_counter()
+    oracle.adamw_step(T[0], cbs[0], T[1], cbs[1], T[2], cbs[2], g, kc)
+    return time.perf_counter() - t0, k
+
+
 def oracle_momentum_time(workload: str, nblocks_sample: int):
     """Time one oracle momentum step on the first `nblocks_sample` blocks."""
     import oracle
@@ -569,6 +685,9 @@ def run_reference(args):
     if rank != 0:
         return None
     from lossless_bf16_tensor_gb300 import synth
+    if "adamw" in synth.WORKLOADS[args.workload]:
+        return run_reference_timed(args, world, oracle_adamw_time,
+                                   "fused AdamW step on compressed W, M and V: elements per second")
     if "gradient" in synth.WORKLOADS[args.workload]:
         return run_reference_momentum(args, world)
     times, nvals = [], 0
@@ -589,6 +708,25 @@ def run_reference(args):
             "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
                              "sample": sample},
             "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def run_reference_timed(args, world, timer, metric):
+    for _ in range(args.warmup):
+        timer(args.workload, args.cpu_blocks)
+    times, nvals = [], 0
+    for _ in range(args.steps):
+        dt, nvals = timer(args.workload, args.cpu_blocks)
+        times.append(dt)
+    s = sum(times) / len(times)
+    value = nvals / s / 1e9
+    sample = "first %d values of %s per step (%d blocks)" % (nvals, args.workload, args.cpu_blocks)
+    return {"impl": "reference", "metric": metric, "value": round(value, 5), "unit": "Gelem/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(s * 1e3, 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "u32+f32", "data": "synthetic",
+            "config": {"workload": WORKLOAD_TEXT[args.workload], "name": args.workload},
+            "cpu_baseline": {"value": round(value, 5), "unit": "Gelem/s", "cores": 1, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": round(value, 5), "unit": "Gelem/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
 def run_reference_momentum(args, world):

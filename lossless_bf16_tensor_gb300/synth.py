@@ -20,6 +20,10 @@ and activations):
 * ``momentum_162m`` the ``sgd_162m`` W and M with a dense BF16 gradient
                     g ~ N(0, 1e-4) (seed 6 on odd steps, 7 on even ones),
                     mu = 0.9, eta = 1e-3: SGD with momentum.
+* ``adamw_162m``    the ``sgd_162m`` W, a first moment M ~ N(0, 1e-4) (seed 4),
+                    a second moment V = |N(0, 1e-8)| (seed 5) and the
+                    ``momentum_162m`` gradients; AdamW with lr = 1e-3,
+                    betas (0.9, 0.999), eps = 1e-8, weight decay 0.01.
 * ``gelu_act``      [8, 4096, 3072] GELU(z), z ~ N(0, 1), seed 5, with 30% of
                     positions set to +0.0; HIGH; scaled by 2^k, k = -4..4.
 * ``gelu_act_zero`` the same activations coded with a zero-atom Gaussian(1)
@@ -31,7 +35,8 @@ import numpy as np
 import torch
 
 __all__ = ["bf16_bits", "normal", "laplace", "heavy_tail", "gelu_sparse", "scale_pow2",
-           "all_bf16_patterns", "random_bits", "generate", "momentum", "gradient", "WORKLOADS"]
+           "all_bf16_patterns", "random_bits", "generate", "momentum", "gradient", "second_moment",
+           "WORKLOADS"]
 
 
 def bf16_bits(a: np.ndarray) -> np.ndarray:
@@ -122,6 +127,12 @@ WORKLOADS = {
                           model="gaussian", scale=0.02, shape=0.0, level="CLEAN",
                           momentum=dict(sigma=1e-3, seed=4, model="gaussian", scale=1e-3),
                           gradient=dict(sigma=1e-4, seeds=(6, 7)), eta=1e-3, mu=0.9),
+    "adamw_162m": dict(n=162_000_000, gen="normal", args=dict(sigma=0.02, seed=3),
+                       model="gaussian", scale=0.02, shape=0.0, level="CLEAN",
+                       momentum=dict(sigma=1e-4, seed=4, model="gaussian", scale=1e-4),
+                       second=dict(sigma=1e-8, seed=5, model="laplace", scale=1e-8),
+                       gradient=dict(sigma=1e-4, seeds=(6, 7)),
+                       adamw=dict(lr=1e-3, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.01)),
     "gelu_act": dict(n=8 * 4096 * 3072, gen="gelu_sparse", args=dict(seed=5),
                      model="gaussian", scale=1.0, shape=0.0, level="HIGH",
                      pow2=list(range(-4, 5))),
@@ -152,3 +163,11 @@ def gradient(name: str, step: int, n: int | None = None) -> np.ndarray:
     w = WORKLOADS[name]
     g = w["gradient"]
     return normal(w["n"] if n is None else n, g["sigma"], g["seeds"][(step - 1) % 2])
+
+
+def second_moment(name: str, n: int | None = None) -> np.ndarray:
+    """A non-negative second-moment tensor: |N(0, sigma)| in BF16."""
+    w = WORKLOADS[name]
+    sm = w["second"]
+    rng = np.random.default_rng(sm["seed"])
+    return bf16_bits(np.abs(rng.normal(0.0, sm["sigma"], size=w["n"] if n is None else n)))

@@ -250,3 +250,50 @@ def test_compressed_tensor_moves_through_host_memory():
     torch.cuda.synchronize()
     assert np.array_equal(gpu_decode(back, cb), x)
     assert_same_format(back.to_host(), oracle.encode(x, ocb, lv))
+
+
+def test_more_than_two_to_the_32_values():
+    """4,294,979,641 values (past 2^32, so every 32-bit element index would
+    wrap): encode, decode checked in full on the device, fused SGD; blocks at
+    the start, across the 2^32 boundary and at the ragged end compared with
+    the oracle run on those blocks alone (blocks are independent given the
+    shift).  Values tile a seeded 2^20-value Laplace draw."""
+    n = (1 << 32) + 12345
+    period = 1 << 20
+    xb = synth.laplace(period, 0.01, seed=11)
+    mb = synth.laplace(period, 1e-3, seed=12)
+    reps = n // period + 1
+    x = torch.from_numpy(xb.view(np.int16)).cuda().repeat(reps)[:n]
+    m = torch.from_numpy(mb.view(np.int16)).cuda().repeat(reps)[:n]
+    cb, ocb = codebooks(1, 0.01)
+    cbm, ocbm = codebooks(1, 1e-3)
+    X = B.CompressedTensor(n, 0)
+    Mc = B.CompressedTensor(n, 0)
+    B.lct_encode(x, cb, X)
+    B.lct_encode(m, cbm, Mc)
+    y = torch.empty_like(x)
+    B.lct_decode(X, cb, y)
+    Wn = B.CompressedTensor(n, 0)
+    B.lct_sgd_step_fused(X, cb, Mc, cbm, float(np.float32(1e-3)), Wn)
+    torch.cuda.synchronize()
+    assert torch.equal(y, x)
+    del y
+    sx, sm_, sw = X.state(), Mc.state(), Wn.state()
+    assert sx.status == sm_.status == sw.status == 0
+    block, nb = 65536, X.nblocks
+    hx, hm, hw = (t.regions for t in (X, Mc, Wn))
+    for b in (0, (1 << 32) // block - 1, (1 << 32) // block, nb - 1):
+        lo, hi = b * block, min(n, (b + 1) * block)
+        idx = np.arange(lo, hi, dtype=np.int64) % period
+        xs, ms = xb[idx], mb[idx]
+        rx = oracle.encode(xs, ocb, 0, delta=sx.delta)
+        rm = oracle.encode(ms, ocbm, 0, delta=sm_.delta)
+        rw = oracle.sgd_step(rx, ocb, rm, ocbm, float(np.float32(1e-3)))
+        for regs, ref in ((hx, rx), (hw, rw)):
+            assert np.array_equal(regs["sf"][lo:hi].cpu().numpy(), ref.sf), b
+            sl = regs["slots"].view(torch.int32)[b * 25 * 256:(b + 1) * 25 * 256].cpu().numpy().view(np.uint32)
+            assert np.array_equal(sl, ref.slots), b
+            mk = regs["markers"].view(torch.int16)[b * 256:(b + 1) * 256].cpu().numpy().view(np.uint16)
+            assert np.array_equal(mk, ref.markers), b
+            off = regs["blk_off"].view(torch.int64)[b:b + 2].cpu().numpy()
+            assert off[1] - off[0] == ref.ovf_used, b

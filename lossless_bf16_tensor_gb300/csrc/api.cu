@@ -118,6 +118,41 @@ void regions(const lct_tensor *t, const lct_sizes &s, Range out[7])
     out[6] = range_of(t->d_work, s.work_bytes);
 }
 
+// Aliasing rules of a fused update with nout outputs and nin >= nout inputs,
+// output o being the new value of input o (inputs nout.. are read only):
+//   - an output may share its header, sign-fraction, slot, marker and offset
+//     regions with its own input (in place) but not partly overlap them, and
+//     its overflow and scratch are apart from every region of that input;
+//   - an output does not touch another input, another output or the dense
+//     gradient (grad may be null).
+bool aliasing_ok(const Range (*out)[7], int nout, const Range (*in)[7], int nin, const Range *grad)
+{
+    for (int o = 0; o < nout; ++o) {
+        for (int r = 0; r < 7; ++r)
+            if (grad && overlap(out[o][r], *grad)) return false;
+        for (int i = 0; i < nin; ++i) {
+            if (i == o) continue;
+            for (int r = 0; r < 7; ++r)
+                for (int k = 0; k < 6; ++k)
+                    if (overlap(out[o][r], in[i][k])) return false;
+        }
+        for (int q = 0; q < nout; ++q) {
+            if (q == o) continue;
+            for (int r = 0; r < 7; ++r)
+                for (int k = 0; k < 7; ++k)
+                    if (overlap(out[o][r], out[q][k])) return false;
+        }
+        for (int k = 0; k < 6; ++k)
+            if (overlap(out[o][5], in[o][k]) || overlap(out[o][6], in[o][k])) return false;
+        for (int r = 0; r < 5; ++r)
+            for (int k = 0; k < 6; ++k) {
+                const bool same = r == k && out[o][r].lo == in[o][k].lo;
+                if (!same && overlap(out[o][r], in[o][k])) return false;
+            }
+    }
+    return true;
+}
+
 }  // namespace
 }  // namespace lct
 
@@ -230,27 +265,11 @@ extern "C" lct_status lct_sgd_step_fused(const lct_tensor *W_in, const lct_codeb
     if (!cbW || !cbM || !codebook_valid(*cbW) || !codebook_valid(*cbM)) return LCT_ERR_INVALID_ARG;
     if (W_in->n != M->n || W_in->n != W_out->n) return LCT_ERR_INVALID_ARG;
     if (W_in->level != M->level || W_in->level != W_out->level) return LCT_ERR_UNSUPPORTED;
-    Range rw[7], rm[7], ro[7];
-    regions(W_in, sw, rw);
-    regions(M, sm, rm);
-    regions(W_out, so, ro);
-    if (W_out->n > 0) {
-        // W_out must not touch M at all.
-        for (int i = 0; i < 7; ++i)
-            for (int k = 0; k < 6; ++k)
-                if (overlap(ro[i], rm[k])) return LCT_ERR_INVALID_ARG;
-        // W_out's overflow and scratch must be apart from every input region;
-        // its other regions may coincide exactly with W_in's (in place) but
-        // not partly overlap them.
-        for (int k = 0; k < 6; ++k) {
-            if (overlap(ro[5], rw[k]) || overlap(ro[6], rw[k])) return LCT_ERR_INVALID_ARG;
-        }
-        for (int i = 0; i < 5; ++i)
-            for (int k = 0; k < 6; ++k) {
-                const bool same = i == k && ro[i].lo == rw[k].lo;
-                if (!same && overlap(ro[i], rw[k])) return LCT_ERR_INVALID_ARG;
-            }
-    }
+    Range ri[2][7], ro[1][7];
+    regions(W_in, sw, ri[0]);
+    regions(M, sm, ri[1]);
+    regions(W_out, so, ro[0]);
+    if (W_out->n > 0 && !aliasing_ok(ro, 1, ri, 2, nullptr)) return LCT_ERR_INVALID_ARG;
     UpdateArgs a;
     std::memset(&a, 0, sizeof(a));
     a.in[0] = dev_view(W_in, sw);
@@ -283,33 +302,14 @@ extern "C" lct_status lct_sgd_momentum_step_fused(const lct_tensor *W_in, const 
     if (M_in->level != W_in->level || W_out->level != W_in->level || M_out->level != W_in->level)
         return LCT_ERR_UNSUPPORTED;
     if (n > 0 && (!d_g || !aligned16(d_g))) return LCT_ERR_INVALID_ARG;
-    Range rw[7], rm[7], row_[7], rom[7];
-    regions(W_in, sw, rw);
-    regions(M_in, sm, rm);
-    regions(W_out, sow, row_);
-    regions(M_out, som, rom);
+    Range ri[2][7], ro[2][7];
+    regions(W_in, sw, ri[0]);
+    regions(M_in, sm, ri[1]);
+    regions(W_out, sow, ro[0]);
+    regions(M_out, som, ro[1]);
     if (n > 0) {
         const Range rg = range_of(d_g, 2 * n);
-        // an output against the other input, the other output and the gradient
-        for (int i = 0; i < 7; ++i) {
-            if (overlap(row_[i], rg) || overlap(rom[i], rg)) return LCT_ERR_INVALID_ARG;
-            for (int k = 0; k < 7; ++k) {
-                if (overlap(row_[i], rom[k])) return LCT_ERR_INVALID_ARG;
-                if (k < 6 && (overlap(row_[i], rm[k]) || overlap(rom[i], rw[k]))) return LCT_ERR_INVALID_ARG;
-            }
-        }
-        // an output against its own input: overflow and scratch apart from
-        // every input region; the others the same region or disjoint
-        const Range *outs[2] = {row_, rom}, *ins[2] = {rw, rm};
-        for (int o = 0; o < 2; ++o) {
-            for (int k = 0; k < 6; ++k)
-                if (overlap(outs[o][5], ins[o][k]) || overlap(outs[o][6], ins[o][k])) return LCT_ERR_INVALID_ARG;
-            for (int i = 0; i < 5; ++i)
-                for (int k = 0; k < 6; ++k) {
-                    const bool same = i == k && outs[o][i].lo == ins[o][k].lo;
-                    if (!same && overlap(outs[o][i], ins[o][k])) return LCT_ERR_INVALID_ARG;
-                }
-        }
+        if (!aliasing_ok(ro, 2, ri, 2, &rg)) return LCT_ERR_INVALID_ARG;
     }
     MomentumArgs a;
     a.w_in = dev_view(W_in, sw);
@@ -327,26 +327,6 @@ extern "C" lct_status lct_sgd_momentum_step_fused(const lct_tensor *W_in, const 
     a.wait_ns = kDefaultWaitNs;
     return launch_momentum(a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? LCT_OK : LCT_ERR_CUDA;
 }
-
-namespace lct {
-namespace {
-
-// An output tensor against its own input: overflow and scratch apart from
-// every input region, the other regions either the same or disjoint.
-bool output_fits_input(const Range out[7], const Range in[7])
-{
-    for (int k = 0; k < 6; ++k)
-        if (overlap(out[5], in[k]) || overlap(out[6], in[k])) return false;
-    for (int i = 0; i < 5; ++i)
-        for (int k = 0; k < 6; ++k) {
-            const bool same = i == k && out[i].lo == in[k].lo;
-            if (!same && overlap(out[i], in[k])) return false;
-        }
-    return true;
-}
-
-}  // namespace
-}  // namespace lct
 
 extern "C" lct_status lct_adamw_step_fused(const lct_tensor *W_in, const lct_codebook *cbW, const lct_tensor *M_in,
                                            const lct_codebook *cbM, const lct_tensor *V_in, const lct_codebook *cbV,
@@ -378,20 +358,7 @@ extern "C" lct_status lct_adamw_step_fused(const lct_tensor *W_in, const lct_cod
     }
     if (n > 0) {
         const Range rg = range_of(d_g, 2 * n);
-        for (int o = 0; o < 3; ++o) {
-            for (int r = 0; r < 7; ++r)
-                if (overlap(ro[o][r], rg)) return LCT_ERR_INVALID_ARG;
-            // an output against the other outputs and the other inputs
-            for (int q = 0; q < 3; ++q) {
-                if (q == o) continue;
-                for (int r = 0; r < 7; ++r)
-                    for (int t = 0; t < 7; ++t) {
-                        if (overlap(ro[o][r], ro[q][t])) return LCT_ERR_INVALID_ARG;
-                        if (t < 6 && overlap(ro[o][r], ri[q][t])) return LCT_ERR_INVALID_ARG;
-                    }
-            }
-            if (!output_fits_input(ro[o], ri[o])) return LCT_ERR_INVALID_ARG;
-        }
+        if (!aliasing_ok(ro, 3, ri, 3, &rg)) return LCT_ERR_INVALID_ARG;
     }
     // the step's constants, rounded to float once
     const double t = static_cast<double>(p->step);

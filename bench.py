@@ -11,7 +11,10 @@ value = uncompressed BF16 bytes passed through the codec per second: encode
 
 Default workload: 2^24 BF16 values ~ Laplace(0, 0.01), Laplace codebook,
 CLEAN blocks; M ~ Laplace(0, 1e-3).  L2 is flushed (256 MiB write) before
-every timed step, outside the step's events.
+every timed step, outside the step's events.  The timed steps carry events
+only at their boundaries; the per-kernel times (and the roofline of the
+dominant kernel) come from a second pass of as many steps with an event after
+every kernel.
 
 --impl reference times the CPU oracle (single thread) on the same workload.
 Under torchrun every rank runs its own replica (weak scaling, no collective
@@ -201,18 +204,20 @@ def run_gpu(args):
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.int32, device="cuda")
 
     def step(evs=None):
-        # evs: 0 step start, 1 encode end, 2 decode end, 3 fused SGD end
+        # evs: (step start, step end) or (step start, encode end, decode end,
+        # fused SGD end)
+        inner = evs is not None and len(evs) == 4
         if evs:
             evs[0].record(stream)
         B.lct_encode(x, cb, X, stream)
-        if evs:
+        if inner:
             evs[1].record(stream)
         B.lct_decode(X, cb, y, stream)
-        if evs:
+        if inner:
             evs[2].record(stream)
         B.lct_sgd_step_fused(X, cb, Mc, cbm, ETA, Wn, stream)
         if evs:
-            evs[3].record(stream)
+            evs[-1].record(stream)
 
     for _ in range(args.warmup):
         flush.zero_()
@@ -229,7 +234,13 @@ def run_gpu(args):
     except AttributeError:
         pass
     clocks = ClockSampler(None if world == 1 and bus is None else bus)
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    # The timed steps carry events at their boundaries only: an event between
+    # two kernels keeps the second from launching while the first finishes
+    # (programmatic dependent launch), which a user's back-to-back calls do
+    # not suffer.  The per-kernel times come from a second pass of as many
+    # steps with an event after every kernel.
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
+    kevs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
@@ -241,12 +252,17 @@ def run_gpu(args):
     torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
-    clk = clocks.stop()
-    enc = [e[0].elapsed_time(e[1]) for e in evs]
-    dec = [e[1].elapsed_time(e[2]) for e in evs]
-    sgd = [e[2].elapsed_time(e[3]) for e in evs]
-    total_ms = max_over_ranks(sum(e[0].elapsed_time(e[3]) for e in evs), device="cuda")
+    total_ms = max_over_ranks(sum(e[0].elapsed_time(e[1]) for e in evs), device="cuda")
     ms_step = total_ms / args.steps
+    for k in range(args.steps):
+        flush.zero_()
+        step(kevs[k])
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    enc = [e[0].elapsed_time(e[1]) for e in kevs]
+    dec = [e[1].elapsed_time(e[2]) for e in kevs]
+    sgd = [e[2].elapsed_time(e[3]) for e in kevs]
+    ms_step_kernel_events = statistics.mean(e[0].elapsed_time(e[3]) for e in kevs)
 
     sx, sm_, sw = X.state(), Mc.state(), Wn.state()
     sizes = X.sizes
@@ -305,6 +321,8 @@ def run_gpu(args):
             "decode_gbs_uncompressed": round(2 * n / (t_ms["decode"] * 1e-3) / 1e9, 1),
             "sgd_gelem_per_s": round(n / (t_ms["sgd"] * 1e-3) / 1e9, 3),
             "ms": {k: round(v, 4) for k, v in t_ms.items()},
+            "kernel_times": "second pass of the same number of steps with an event after every kernel "
+                            "(%.4f ms per step with those events)" % ms_step_kernel_events,
             "hbm_frac_of_%s" % peak_kind: {k: round(v, 4) for k, v in frac.items()},
             "compression_ratio_all_in": round(ratio_all_in, 5),
             "compression_ratio_payload": round(ratio_payload, 5),

@@ -35,8 +35,13 @@ struct EncodeSmem {
     static constexpr int kBytes = kIn + kSlot + kTbl + kSpill;
 };
 
-// Prologue (one launch per encode): CTA 0 estimates the shift and writes the
-// tensor header; every CTA zeroes its share of the look-back status words.
+// Prologue (one launch per encode, clusters of kSampleCtas CTAs): the first
+// cluster estimates the shift and CTA 0 writes the tensor header; every CTA
+// zeroes its share of the look-back status words.  The samples are spread
+// over the cluster's CTAs (one SM keeps only so many loads in flight) and
+// their counts are added up through distributed shared memory.
+constexpr int kSampleCtas = 8;
+
 __global__ void __launch_bounds__(256) k_encode_prologue(const uint16_t *__restrict__ x, DevTensor t,
                                                           int32_t median_exp, uint32_t cb_hash)
 {
@@ -45,15 +50,19 @@ __global__ void __launch_bounds__(256) k_encode_prologue(const uint16_t *__restr
     for (uint64_t i = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x; i < t.nblocks;
          i += (uint64_t)gridDim.x * blockDim.x)
         t.work[i] = 0ull;
-    if (blockIdx.x != 0) return;
+    if (blockIdx.x >= kSampleCtas) return;  // not the first cluster
 
     // Shift: m = min(n, 4096) samples at floor(k*n/m); histogram of their
-    // exponents in the normal range 1..254; lower median.
-    constexpr int kPer = LCT_SHIFT_SAMPLES / 256;
+    // exponents in the normal range 1..254; lower median.  CTA r of the
+    // cluster takes k = tid + 256*i for i in [r*kPer, (r+1)*kPer).
+    constexpr int kPer = LCT_SHIFT_SAMPLES / 256 / kSampleCtas;
+    static_assert(kPer * 256 * kSampleCtas == LCT_SHIFT_SAMPLES, "samples split evenly");
     __shared__ uint32_t hist[8][256];  // one histogram per warp
+    __shared__ uint32_t cta_hist[256];
     __shared__ uint32_t wsum[8];
     __shared__ int32_t median;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const uint32_t rank = cluster_rank();
 #pragma unroll
     for (int w = 0; w < 8; ++w) hist[w][tid] = 0;
     if (tid == 0) median = -1;
@@ -65,7 +74,7 @@ __global__ void __launch_bounds__(256) k_encode_prologue(const uint16_t *__restr
     uint16_t v[kPer];
 #pragma unroll
     for (int i = 0; i < kPer; ++i) {  // all loads in flight at once
-        const uint32_t k = tid + 256u * i;
+        const uint32_t k = tid + 256u * (rank * kPer + i);
         const uint64_t at = m == (uint32_t)LCT_SHIFT_SAMPLES ? ((uint64_t)k * n) >> 12 : (uint64_t)k;
         v[i] = k < m ? __ldg(x + at) : 0;
     }
@@ -74,7 +83,7 @@ __global__ void __launch_bounds__(256) k_encode_prologue(const uint16_t *__restr
 #pragma unroll
     for (int i = 0; i < kPer; ++i) {
         const uint32_t e = exp_of(v[i]);
-        const bool keep = tid + 256u * i < m && e >= 1 && e <= 254;
+        const bool keep = tid + 256u * (rank * kPer + i) < m && e >= 1 && e <= 254;
         const uint32_t same = __match_any_sync(kFull, keep ? e : 256u);
         if (keep && lane == __ffs(same) - 1) hist[warp][e] += __popc(same);
     }
@@ -82,42 +91,49 @@ __global__ void __launch_bounds__(256) k_encode_prologue(const uint16_t *__restr
     uint32_t c = 0;
 #pragma unroll
     for (int w = 0; w < 8; ++w) c += hist[w][tid];
-    uint32_t inc = c;
+    cta_hist[tid] = c;
+    cluster_sync();  // every CTA's counts are in its shared memory
+    if (rank == 0) {
+        c = 0;
+        for (uint32_t q = 0; q < (uint32_t)kSampleCtas; ++q) c += ld_peer_shared(&cta_hist[tid], q);
+        uint32_t inc = c;
 #pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const uint32_t u = __shfl_up_sync(kFull, inc, o);
-        if (lane >= o) inc += u;
-    }
-    if (lane == 31) wsum[warp] = inc;
-    __syncthreads();
-    uint32_t before = 0, kept = 0;
-    for (int w = 0; w < 8; ++w) {
-        if (w < warp) before += wsum[w];
-        kept += wsum[w];
-    }
-    inc += before;
-    if (kept > 0) {
-        const uint32_t rank = (kept - 1) / 2;  // lower median, 0-based
-        if (inc > rank && inc - c <= rank) median = tid;
-    }
-    __syncthreads();
-    if (tid == 0) {
-        int delta = 0;
-        if (median >= 0) {
-            delta = median - median_exp;
-            delta = delta > 127 ? 127 : (delta < -127 ? -127 : delta);
+        for (int o = 1; o < 32; o <<= 1) {
+            const uint32_t u = __shfl_up_sync(kFull, inc, o);
+            if (lane >= o) inc += u;
         }
-        lct_header *h = t.hdr;
-        h->magic = LCT_MAGIC;
-        h->version = 1;
-        h->n = n;
-        h->level = t.level;
-        h->delta = delta;
-        h->status = 0;
-        h->cb_hash = cb_hash;
-        h->ovf_used = 0;
-        h->ovf_cap = t.ovf_cap;
+        if (lane == 31) wsum[warp] = inc;
+        __syncthreads();
+        uint32_t before = 0, kept = 0;
+        for (int w = 0; w < 8; ++w) {
+            if (w < warp) before += wsum[w];
+            kept += wsum[w];
+        }
+        inc += before;
+        if (kept > 0) {
+            const uint32_t r = (kept - 1) / 2;  // lower median, 0-based
+            if (inc > r && inc - c <= r) median = tid;
+        }
+        __syncthreads();
+        if (tid == 0) {
+            int delta = 0;
+            if (median >= 0) {
+                delta = median - median_exp;
+                delta = delta > 127 ? 127 : (delta < -127 ? -127 : delta);
+            }
+            lct_header *h = t.hdr;
+            h->magic = LCT_MAGIC;
+            h->version = 1;
+            h->n = n;
+            h->level = t.level;
+            h->delta = delta;
+            h->status = 0;
+            h->cb_hash = cb_hash;
+            h->ovf_used = 0;
+            h->ovf_cap = t.ovf_cap;
+        }
     }
+    cluster_sync();  // CTA 0 has read the other CTAs' counts
 }
 
 template <int LEVEL>
@@ -248,9 +264,10 @@ __global__ void __launch_bounds__(kEncThreads, 4) k_encode(const __grid_constant
     }
     __syncthreads();
 
+    const unsigned long long excl = s_excl;
+
     // spilled exponents, raw, in (stream, symbol) order: one warp per stream
     // at a time, lanes over the stream's spilled symbols
-    const unsigned long long excl = s_excl;
     if (total > 0 && excl + total <= a.t.ovf_cap) {
         uint8_t *out = a.t.ovf + excl;
         for (int i = 0; i < 32; ++i) {
@@ -293,9 +310,11 @@ cudaError_t launch_level(const EncodeArgs &a, cudaStream_t s)
 
 cudaError_t launch_encode(const EncodeArgs &a, cudaStream_t s)
 {
-    const uint32_t zero_ctas = 1 + a.t.nblocks / 8192;
-    cudaError_t err = dev::launch_pdl(dev::k_encode_prologue, dim3(zero_ctas < 64 ? zero_ctas : 64), dim3(256), 0, s,
-                                      a.x, a.t, a.median_exp, a.cb.hash);
+    // one CTA per 8192 look-back words (at most 64), in whole clusters
+    const uint64_t zero_ctas = 1 + a.t.nblocks / 8192;
+    const uint32_t k = dev::kSampleCtas, ctas = (uint32_t)((zero_ctas < 64 ? zero_ctas : 64) + k - 1) / k * k;
+    cudaError_t err = dev::launch_pdl_cluster(dev::k_encode_prologue, dim3(ctas), dim3(256), 0, s, k, a.x, a.t,
+                                              a.median_exp, a.cb.hash);
     if (err != cudaSuccess || a.t.nblocks == 0) return err;
     switch (a.t.level) {
     case LCT_LEVEL_CLEAN: return dev::launch_level<LCT_LEVEL_CLEAN>(a, s);

@@ -383,16 +383,21 @@ constexpr unsigned long long kFlagAgg = 1ull << 62;  // block total published
 constexpr unsigned long long kFlagInc = 2ull << 62;  // inclusive prefix published
 constexpr unsigned long long kValMask = (1ull << 62) - 1;
 
-__device__ __forceinline__ unsigned long long ld_acquire(const unsigned long long *p)
+// A status word is read and written whole (one aligned 64-bit access) and
+// carries everything a successor uses from it: the flag and the count.  No
+// other data is handed over through it, so relaxed accesses at GPU scope are
+// enough; a release would first have to make every earlier global store of
+// the CTA (its sign-fraction bytes and markers) visible.
+__device__ __forceinline__ unsigned long long ld_status(const unsigned long long *p)
 {
     unsigned long long v;
-    asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
     return v;
 }
 
-__device__ __forceinline__ void st_release(unsigned long long *p, unsigned long long v)
+__device__ __forceinline__ void st_status(unsigned long long *p, unsigned long long v)
 {
-    asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+    asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
 }
 
 // One full warp of block b: publish the block's overflow byte count, then
@@ -409,17 +414,17 @@ static __device__ __noinline__ unsigned long long warp_lookback(unsigned long lo
     const int lane = threadIdx.x & 31;
     *timed_out = false;
     if (b == 0) {
-        if (lane == 0) st_release(&status[0], kFlagInc | total);
+        if (lane == 0) st_status(&status[0], kFlagInc | total);
         return 0;
     }
-    if (lane == 0) st_release(&status[b], kFlagAgg | total);
+    if (lane == 0) st_status(&status[b], kFlagAgg | total);
     unsigned long long excl = 0;
     int64_t nearest = (int64_t)b - 1;
     const uint64_t t0 = global_ns();
     uint32_t spins = 0;
     for (;;) {
         const int64_t idx = nearest - lane;
-        const unsigned long long v = idx >= 0 ? ld_acquire(&status[idx]) : kFlagInc;
+        const unsigned long long v = idx >= 0 ? ld_status(&status[idx]) : kFlagInc;
         const uint32_t flag = (uint32_t)(v >> 62);
         const uint32_t inc = __ballot_sync(kFull, flag == 2u);
         const uint32_t not_ready = __ballot_sync(kFull, flag == 0u);
@@ -440,7 +445,7 @@ static __device__ __noinline__ unsigned long long warp_lookback(unsigned long lo
         if (inc) break;
         nearest -= 32;
     }
-    if (lane == 0) st_release(&status[b], kFlagInc | ((excl + total) & kValMask));
+    if (lane == 0) st_status(&status[b], kFlagInc | ((excl + total) & kValMask));
     return excl;
 }
 
@@ -451,16 +456,16 @@ static __device__ __noinline__ unsigned long long lookback(unsigned long long *s
 {
     *timed_out = false;
     if (b == 0) {
-        st_release(&status[0], kFlagInc | total);
+        st_status(&status[0], kFlagInc | total);
         return 0;
     }
-    st_release(&status[b], kFlagAgg | total);
+    st_status(&status[b], kFlagAgg | total);
     unsigned long long excl = 0;
     const uint64_t t0 = global_ns();
     uint32_t spins = 0;
     int64_t pred = (int64_t)b - 1;
     while (pred >= 0) {
-        const unsigned long long v = ld_acquire(&status[pred]);
+        const unsigned long long v = ld_status(&status[pred]);
         const unsigned long long flag = v & ~kValMask;
         if (flag == 0) {
             ++spins;
@@ -475,7 +480,7 @@ static __device__ __noinline__ unsigned long long lookback(unsigned long long *s
         if (flag == kFlagInc) break;
         --pred;
     }
-    st_release(&status[b], kFlagInc | ((excl + total) & kValMask));
+    st_status(&status[b], kFlagInc | ((excl + total) & kValMask));
     return excl;
 }
 

@@ -278,14 +278,7 @@ def run_gpu(args):
     uncompressed_per_step = 10 * n
     value = 10 * replica_units(n, world) / (ms_step * 1e-3) / 1e9
 
-    traffic = None
-    tpath = os.path.join(ROOT, "profiles", "traffic.json")
-    if os.path.exists(tpath):
-        with open(tpath) as f:
-            tr = json.load(f)
-        entry = tr.get(args.workload, {}).get(dom)
-        if entry and entry.get("source_hash") == kernel_source_hash(dom):
-            traffic = entry["bytes_per_launch"]
+    traffic = stored_traffic(args.workload, dom)
 
     # ---- end to end through the public API with host buffers
     e2e = None
@@ -466,13 +459,7 @@ def run_gpu_momentum(args, rank, local_rank, world):
     t_ms = statistics.mean(per)
     achieved = alg / (t_ms * 1e-3) / 1e9
     value = replica_units(n, world) / (ms_step * 1e-3) / 1e9
-    traffic = None
-    tpath = os.path.join(ROOT, "profiles", "traffic.json")
-    if os.path.exists(tpath):
-        with open(tpath) as f:
-            entry = json.load(f).get(args.workload, {}).get("momentum")
-        if entry and entry.get("source_hash") == kernel_source_hash("momentum"):
-            traffic = entry["bytes_per_launch"]
+    traffic = stored_traffic(args.workload, "momentum")
     if rank != 0:
         return None
     cpu = None
@@ -581,7 +568,8 @@ def run_gpu_adamw(args, rank, local_rank, world):
                    "parallelism": "replicas" if world > 1 else "single"},
         "roofline": {"bound": "hbm", "kernel": "adamw (moments pass + weight pass, one call)",
                      "achieved": round(achieved, 1), "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
-                     "frac": round(achieved / peak, 4), "traffic": None, "algorithmic_bytes_per_launch": alg},
+                     "frac": round(achieved / peak, 4), "traffic": stored_traffic(args.workload, "adamw"),
+                     "algorithmic_bytes_per_launch": alg},
         "breakdown": {"compression_ratio_all_in": [round(2.0 * n / (sizes.fixed_bytes + s_.ovf_used), 5) for s_ in st],
                       "overflow_bytes": [int(s_.ovf_used) for s_ in st]},
         "clocks": clk, "e2e": None, "gpu_launches": 4 * args.steps, "cpu_baseline": cpu,
@@ -630,7 +618,22 @@ def oracle_momentum_time(workload: str, nblocks_sample: int):
 
 # Device source each kernel's DRAM traffic depends on (the shared device
 # header and the kernel's own file); host code does not enter the hash.
-KERNEL_SOURCES = {"encode": "encode.cu", "decode": "decode.cu", "sgd": "sgd.cu", "momentum": "momentum.cu"}
+KERNEL_SOURCES = {"encode": ("encode.cu",), "decode": ("decode.cu",), "sgd": ("sgd.cu",),
+                  "momentum": ("momentum.cu",), "adamw": ("momentum.cu", "sgd.cu")}
+
+
+def stored_traffic(workload: str, kernel: str):
+    """DRAM bytes (read + write) per launch of `kernel` on `workload` from the
+    ncu summary in profiles/traffic.json, or None when none was taken of the
+    kernel's current source."""
+    tpath = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(tpath):
+        return None
+    with open(tpath) as f:
+        entry = json.load(f).get(workload, {}).get(kernel)
+    if entry and entry.get("source_hash") == kernel_source_hash(kernel):
+        return entry["bytes_per_launch"]
+    return None
 
 
 def kernel_source_hash(kernel: str) -> str:
@@ -639,7 +642,7 @@ def kernel_source_hash(kernel: str) -> str:
     import hashlib
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "lossless_bf16_tensor_gb300", "csrc")
-    for fn in ("codec_dev.cuh", "internal.h", KERNEL_SOURCES[kernel]):
+    for fn in ("codec_dev.cuh", "internal.h") + KERNEL_SOURCES[kernel]:
         with open(os.path.join(csrc, fn), "rb") as f:
             h.update(fn.encode() + f.read())
     return h.hexdigest()[:16]

@@ -2,6 +2,7 @@
 time is the slowest rank's, the job's value counts every rank's replica, and
 the CPU reference arm runs on rank 0 only."""
 import io
+import json
 import os
 import socket
 import sys
@@ -64,3 +65,22 @@ def test_single_process_defaults():
     import bench
     assert bench.max_over_ranks(3.5) == 3.5
     assert bench.replica_units(7, 1) == 7
+
+
+def test_stored_traffic_follows_the_kernel_source():
+    """A stored ncu traffic figure is reported only for the kernel source it
+    was taken of: the AdamW call's hash covers both of its kernels' files."""
+    sys.path.insert(0, ROOT)
+    import bench
+    assert bench.stored_traffic("no_such_workload", "sgd") is None
+    hashes = {k: bench.kernel_source_hash(k) for k in bench.KERNEL_SOURCES}
+    assert len(set(hashes.values())) == len(hashes)
+    with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
+        stored = json.load(f)
+    for workload, kernels in stored.items():
+        for kernel, entry in kernels.items():
+            got = bench.stored_traffic(workload, kernel)
+            if entry["source_hash"] == hashes[kernel]:
+                assert got == entry["bytes_per_launch"] > 0
+            else:
+                assert got is None

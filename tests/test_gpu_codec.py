@@ -297,3 +297,29 @@ def test_more_than_two_to_the_32_values():
             assert np.array_equal(mk, ref.markers), b
             off = regs["blk_off"].view(torch.int64)[b:b + 2].cpu().numpy()
             assert off[1] - off[0] == ref.ovf_used, b
+
+
+def test_package_level_usage():
+    """The package-level calls a user starts from: build a codebook, encode,
+    decode, fused SGD into a new tensor; checked against the oracle's SGD."""
+    import lossless_bf16_tensor_gb300 as L
+    torch.manual_seed(0)
+    n = 4 * 65536
+    w = (torch.randn(n, device="cuda") * 0.02).to(torch.bfloat16)
+    m = (torch.randn(n, device="cuda") * 1e-3).to(torch.bfloat16)
+    cb, cbm = L.lct_codebook_build("gaussian", 0.02), L.lct_codebook_build("gaussian", 1e-3)
+    W, M, W2 = (L.CompressedTensor(n, "CLEAN") for _ in range(3))
+    L.lct_encode(w.view(torch.int16), cb, W)
+    L.lct_encode(m.view(torch.int16), cbm, M)
+    assert 1.40 < W.compression_ratio() < 1.44
+    y = torch.empty_like(w)
+    L.lct_decode(W, cb, y.view(torch.int16))
+    assert torch.equal(y, w)
+    eta = float(np.float32(1e-3))
+    L.lct_sgd_step_fused(W, cb, M, cbm, eta, W2)
+    torch.cuda.synchronize()
+    w_np, m_np = (t.view(torch.int16).cpu().numpy().view(np.uint16) for t in (w, m))
+    ocb, ocbm = oracle.codebook_build(0, 0.02), oracle.codebook_build(0, 1e-3)
+    ref = oracle.sgd_step(oracle.encode(w_np, ocb, 0), ocb, oracle.encode(m_np, ocbm, 0), ocbm, eta)
+    assert W2.state().status == B.LCT_OK
+    assert_same_format(W2.to_host(), ref)

@@ -203,21 +203,21 @@ def run_gpu(args):
     B.lct_encode(md, cbm, Mc)
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.int32, device="cuda")
 
-    def step(evs=None):
+    def step(evs=None, st=stream):
         # evs: (step start, step end) or (step start, encode end, decode end,
         # fused SGD end)
         inner = evs is not None and len(evs) == 4
         if evs:
-            evs[0].record(stream)
-        B.lct_encode(x, cb, X, stream)
+            evs[0].record(st)
+        B.lct_encode(x, cb, X, st)
         if inner:
-            evs[1].record(stream)
-        B.lct_decode(X, cb, y, stream)
+            evs[1].record(st)
+        B.lct_decode(X, cb, y, st)
         if inner:
-            evs[2].record(stream)
-        B.lct_sgd_step_fused(X, cb, Mc, cbm, ETA, Wn, stream)
+            evs[2].record(st)
+        B.lct_sgd_step_fused(X, cb, Mc, cbm, ETA, Wn, st)
         if evs:
-            evs[-1].record(stream)
+            evs[-1].record(st)
 
     for _ in range(args.warmup):
         flush.zero_()
@@ -258,6 +258,22 @@ def run_gpu(args):
         flush.zero_()
         step(kevs[k])
     torch.cuda.synchronize()
+    # The same step captured once in a CUDA graph and replayed (every call
+    # only enqueues work, so it captures); reported beside the direct step.
+    graph_ms = None
+    if world == 1:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):  # captured on torch's side stream
+            step(st=torch.cuda.current_stream())
+        gevs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
+        for k in range(args.steps):
+            flush.zero_()
+            gevs[k][0].record(stream)
+            g.replay()
+            gevs[k][1].record(stream)
+        torch.cuda.synchronize()
+        graph_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in gevs)
+        assert torch.equal(y, x), "decode(encode(x)) != x after graph replay"
     clk = clocks.stop()
     enc = [e[0].elapsed_time(e[1]) for e in kevs]
     dec = [e[1].elapsed_time(e[2]) for e in kevs]
@@ -316,6 +332,7 @@ def run_gpu(args):
             "ms": {k: round(v, 4) for k, v in t_ms.items()},
             "kernel_times": "second pass of the same number of steps with an event after every kernel "
                             "(%.4f ms per step with those events)" % ms_step_kernel_events,
+            "ms_per_step_cuda_graph": None if graph_ms is None else round(graph_ms, 4),
             "hbm_frac_of_%s" % peak_kind: {k: round(v, 4) for k, v in frac.items()},
             "compression_ratio_all_in": round(ratio_all_in, 5),
             "compression_ratio_payload": round(ratio_payload, 5),

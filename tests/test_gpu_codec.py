@@ -323,3 +323,44 @@ def test_package_level_usage():
     ref = oracle.sgd_step(oracle.encode(w_np, ocb, 0), ocb, oracle.encode(m_np, ocbm, 0), ocbm, eta)
     assert W2.state().status == B.LCT_OK
     assert_same_format(W2.to_host(), ref)
+
+
+def test_step_captured_in_a_cuda_graph():
+    """The calls enqueue work only (no host synchronisation, no allocation),
+    so a step of encode, decode and fused SGD can be captured in a CUDA graph
+    and replayed on new inputs copied into the captured buffers; every replay
+    matches the oracle."""
+    n = 2 * 65536 + 4097
+    cb, ocb = codebooks(1, 0.01, 0.0)
+    cbm, ocbm = codebooks(1, 1e-3, 0.0)
+    m = synth.laplace(n, 1e-3, seed=2)
+    M = gpu_encode(m, cbm, 0)
+    X, Wn = B.CompressedTensor(n, 0), B.CompressedTensor(n, 0)
+    x = torch.empty(n, dtype=torch.int16, device="cuda")
+    y = torch.empty_like(x)
+    eta = float(np.float32(1e-3))
+    s = torch.cuda.Stream()
+    x.copy_(to_device(synth.laplace(n, 0.01, seed=40)))
+    torch.cuda.synchronize()
+    with torch.cuda.stream(s):  # one step outside the capture (loads the kernels)
+        B.lct_encode(x, cb, X, s)
+        B.lct_decode(X, cb, y, s)
+        B.lct_sgd_step_fused(X, cb, M, cbm, eta, Wn, s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        B.lct_encode(x, cb, X, s)
+        B.lct_decode(X, cb, y, s)
+        B.lct_sgd_step_fused(X, cb, M, cbm, eta, Wn, s)
+    ref_m = oracle.encode(m, ocbm, 0)
+    for seed in (41, 42, 43):
+        xh = synth.laplace(n, 0.01, seed=seed)
+        x.copy_(to_device(xh))
+        torch.cuda.synchronize()
+        with torch.cuda.stream(s):
+            g.replay()
+        torch.cuda.synchronize()
+        ref = oracle.encode(xh, ocb, 0)
+        assert_same_format(X.to_host(), ref)
+        assert np.array_equal(from_device(y), xh)
+        assert_same_format(Wn.to_host(), oracle.sgd_step(ref, ocb, ref_m, ocbm, eta))

@@ -667,9 +667,9 @@ def kernel_source_hash(kernel: str) -> str:
 
 # ------------------------------------------------------ oracle (CPU) arm
 
-def oracle_step_time(workload: str, nblocks_sample: int | None):
-    """Time the oracle on the workload (or its first `nblocks_sample` blocks):
-    encode, decode, fused SGD, as one step.  Returns (seconds, values)."""
+def oracle_step_inputs(workload: str, nblocks_sample: int | None):
+    """The oracle's inputs for one step of the workload (or of its first
+    `nblocks_sample` blocks): x, its codebook, the encoded M and M's codebook."""
     import oracle
     from lossless_bf16_tensor_gb300 import synth
     wl = synth.WORKLOADS[workload]
@@ -687,14 +687,19 @@ def oracle_step_time(workload: str, nblocks_sample: int | None):
     else:
         cb = oracle.codebook_build(model[wl["model"]], wl["scale"], wl["shape"])
     cbm = oracle.codebook_build(model[mm], ms)
-    M = oracle.encode(m, cbm, level)
+    return x, cb, oracle.encode(m, cbm, level), cbm, level
+
+
+def oracle_step(x, cb, M, cbm, level) -> float:
+    """One timed oracle step (encode, decode, fused SGD); returns seconds."""
+    import oracle
     t0 = time.perf_counter()
     X = oracle.encode(x, cb, level)
     rc, y = oracle.decode(X, cb)
     oracle.sgd_step(X, cb, M, cbm, ETA)
     dt = time.perf_counter() - t0
     assert rc == 0 and np.array_equal(y, x)
-    return dt, x.size
+    return dt
 
 
 def cpu_model() -> str:
@@ -708,14 +713,25 @@ def cpu_model() -> str:
     return "unknown"
 
 
+CPU_BASELINE_SECONDS = 10.0
+
+
 def cpu_baseline(workload: str, nblocks_sample: int | None):
-    dt, nvals = oracle_step_time(workload, nblocks_sample)
-    return {"value": round(10 * nvals / dt / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
-            "sample": "%d values of the %s workload (%s), one step: encode + decode + fused SGD; "
+    """The oracle on one host core, stepped over the same inputs until at least
+    CPU_BASELINE_SECONDS of oracle work are timed (one step of the whole 2^24
+    workload takes about a second)."""
+    inputs = oracle_step_inputs(workload, nblocks_sample)
+    nvals = inputs[0].size
+    total, steps = 0.0, 0
+    while total < CPU_BASELINE_SECONDS:
+        total += oracle_step(*inputs)
+        steps += 1
+    return {"value": round(10 * nvals * steps / total / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": "%d steps (encode + decode + fused SGD) over %d values of the %s workload (%s); "
                       "host %s, %d logical CPUs, oracle single-threaded" % (
-                          nvals, workload, "first %d blocks" % nblocks_sample if nblocks_sample else "all",
+                          steps, nvals, workload, "first %d blocks" % nblocks_sample if nblocks_sample else "all",
                           cpu_model(), os.cpu_count() or 0),
-            "seconds": round(dt, 3)}
+            "seconds": round(total, 3)}
 
 
 def run_reference(args):
@@ -728,12 +744,11 @@ def run_reference(args):
                                    "fused AdamW step on compressed W, M and V: elements per second")
     if "gradient" in synth.WORKLOADS[args.workload]:
         return run_reference_momentum(args, world)
-    times, nvals = [], 0
+    inputs = oracle_step_inputs(args.workload, args.cpu_blocks)
+    nvals = inputs[0].size
     for _ in range(args.warmup):
-        oracle_step_time(args.workload, args.cpu_blocks)
-    for _ in range(args.steps):
-        dt, nvals = oracle_step_time(args.workload, args.cpu_blocks)
-        times.append(dt)
+        oracle_step(*inputs)
+    times = [oracle_step(*inputs) for _ in range(args.steps)]
     s = sum(times) / len(times)
     value = 10 * nvals / s / 1e9
     sample = "%d values of %s per step (%s)" % (nvals, args.workload,

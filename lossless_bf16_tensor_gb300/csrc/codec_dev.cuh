@@ -138,10 +138,12 @@ __device__ __forceinline__ void rd_take2(uint32_t &p, const uint32_t *__restrict
 
 // Appends codes most significant bit first into one stream's W-word slot
 // image (word w at col[w * 256]) until the first code that does not fit; that
-// symbol's index is the marker.  Bits not yet written sit in a 64-bit
-// accumulator (hi:lo) holding `nbits` bits; at most one word is flushed per
-// flush call.  `rem` is kept exact only on the checked path (wr_fix_rem
-// restores it after unchecked appends).
+// symbol's index is the marker.  Every append (of at most 32 bits) is
+// followed by a flush, so before an append fewer than 32 bits are pending and
+// they all sit in `hi`; an append ORs the code's head into `hi` and leaves the
+// bits that run past the word in `lo`, which a flush moves up.  `rem` is kept
+// exact only on the checked path (wr_fix_rem restores it after unchecked
+// appends).
 struct Writer {
     uint32_t hi, lo, nbits, wi, rem, marker;
     bool alive;
@@ -159,13 +161,11 @@ __device__ __forceinline__ void wr_init(Writer &w, uint32_t nj)
     w.alive = true;
 }
 
-// Append one code (left-aligned in ent.x, ent.y bits) without flushing; the
-// accumulator must have room (nbits + ent.y <= 64).
+// Append one code (left-aligned in ent.x, ent.y <= 32 bits); nbits < 32.
 __device__ __forceinline__ void wr_add(Writer &w, const uint2 ent)
 {
-    const uint64_t v = ((uint64_t)ent.x << 32) >> w.nbits;
-    w.hi |= (uint32_t)(v >> 32);
-    w.lo |= (uint32_t)v;
+    w.hi |= ent.x >> w.nbits;
+    w.lo = __funnelshift_r(0u, ent.x, w.nbits);  // low word of (ent.x : 0) >> nbits; 0 when nbits = 0
     w.nbits += ent.y;
 }
 
@@ -176,15 +176,13 @@ __device__ __forceinline__ void wr_add2(Writer &w, const uint2 a, const uint2 b)
     wr_add(w, make_uint2(a.x | (b.x >> a.y), a.y + b.y));
 }
 
-// Write out the accumulator's first word if it is complete (leaves nbits < 32
-// when nbits was below 64).
+// Write out the current word if it is complete (leaves nbits < 32).
 __device__ __forceinline__ void wr_flush(Writer &w, uint32_t *__restrict__ col)
 {
     if (w.nbits >= 32u) {
         col[w.wi * kStreams] = w.hi;
         ++w.wi;
         w.hi = w.lo;
-        w.lo = 0;
         w.nbits -= 32u;
     }
 }

@@ -72,6 +72,14 @@ __device__ __forceinline__ uint2 enc_entry(const DevCodebook &cb, int delta, int
     return make_uint2(code << (32u - len), len);
 }
 
+// The encode-table entry of a BF16 value h (bits 0..15, higher bits zero):
+// entry exp_of(h), addressed by its byte offset ((h >> 7) & 0xFF) * 8 in one
+// shift and one mask.
+__device__ __forceinline__ uint2 code_of(const uint2 *__restrict__ tbl, uint32_t h)
+{
+    return *reinterpret_cast<const uint2 *>(reinterpret_cast<const uint8_t *>(tbl) + ((h >> 4) & 0x7F8u));
+}
+
 // Decode table for shift delta, indexed by the next 8 bits of the stream:
 //   bits  0..4   s: a left funnel shift of (0 : window) by s brings the
 //                escape literal to bits 7..14 (s = 15 + escape length); 0

@@ -198,7 +198,7 @@ __global__ void __launch_bounds__(kEncThreads, 4) k_encode(const __grid_constant
             for (int r = 0; r < R; ++r) h[r] = xc[r * kStreams];
 #pragma unroll
             for (int r = 0; r < R; ++r) {
-                ent[r] = tbl[exp_of(h[r])];
+                ent[r] = code_of(tbl, h[r]);
                 need += ent[r].y;
             }
 #pragma unroll

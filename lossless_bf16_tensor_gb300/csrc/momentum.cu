@@ -144,7 +144,7 @@ __device__ __forceinline__ void mom_put_chunk(Writer &wo, const uint32_t (&h)[R]
     uint32_t need = 0;
 #pragma unroll
     for (int r = 0; r < R; ++r) {
-        ent[r] = tbl[exp_of(h[r])];
+        ent[r] = code_of(tbl, h[r]);
         need += ent[r].y;
     }
     if (__all_sync(kFull, wo.alive && need <= wo.rem)) {

@@ -258,7 +258,7 @@ __global__ void __launch_bounds__(kSgdThreads, SgdSmem<LEVEL, INPLACE, UpdateOp<
             }
 #pragma unroll
             for (int r = 0; r < R; ++r) {
-                ent[r] = tbl[exp_of(h[r])];
+                ent[r] = code_of(tbl, h[r]);
                 need += ent[r].y;
             }
 #pragma unroll

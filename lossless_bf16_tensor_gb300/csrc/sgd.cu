@@ -16,12 +16,12 @@
 // straight to global memory.  The slot images of the inputs come in by TMA
 // bulk copy; their sign-fraction bytes stream through a ring of row chunks.
 // A chunk in which no stream of a warp reaches a spill marker and every new
-// slot has room takes a fast path with no per-value checks.  Spilled new
-// exponents are kept for 32 rows out of place (three CTAs per SM for the
-// SGD); an out-of-place step whose stream spills more than that re-decodes
-// the older rows of that stream at the end.  In place every spilled exponent
-// is kept: a code is at most 16 bits, so a stream holds at least 2W symbols
-// of its slot and spills at most NJ - 2W.
+// slot has room takes a fast path with no per-value checks.  A code is at
+// most 16 bits, so a stream holds at least 2W symbols of its slot and spills
+// at most NJ - 2W.  That many spilled new exponents are kept in place and for
+// the 128-row levels (MEDIUM, HIGH).  Out of place in CLEAN 32 rows are kept
+// (three CTAs per SM for the SGD), and a stream that spills more than that
+// re-decodes its older rows at the end.
 #include "codec_dev.cuh"
 
 namespace lct {
@@ -61,16 +61,25 @@ struct UpdateOp<OP_ADAMW> {
 template <int LEVEL, bool INPLACE, int NIN>
 struct SgdSmem {
     static constexpr int W = Geo<LEVEL>::W, NJ = Geo<LEVEL>::NJ;
-    static constexpr int kSpillRows = INPLACE ? NJ - 2 * W : kSgdSpill;
+    // Every spilled new exponent stays staged (at most NJ - 2W per stream, a
+    // code being at most 16 bits) in place, where nothing can be recomputed,
+    // and for the 128-row levels, where that is 88 or 96 rows; otherwise a
+    // 32-row ring, and a stream that spills more is recomputed at the end.
+    static constexpr bool kKeepAll = INPLACE || NJ <= 128;
+    static constexpr int kSpillRows = kKeepAll ? NJ - 2 * W : kSgdSpill;
     static constexpr int kStages = INPLACE ? 3 : 2;  // chunks in flight
     static constexpr int kSlotIn = (W + 1) * kStreams * 4;  // + zero guard row
     static constexpr int kRing = kStages * kSgdRows * kStreams;  // per input
     static constexpr int kLuts = NIN * 256 * 4 + 256 * 8;
     static constexpr int kSpill = (kSpillRows * kRow + 127) / 128 * 128;
     static constexpr int kBytes = NIN * kSlotIn + NIN * kRing + kLuts + kSpill;
-    static constexpr int kCtas = INPLACE ? 1 : (NIN == 2 ? 3 : 2);  // CTAs per SM the launch bounds ask for
-    static_assert(INPLACE || (kSgdSpill & (kSgdSpill - 1)) == 0, "ring index uses a mask");
-    static_assert(kBytes <= 227 * 1024, "shared memory of one CTA");
+    // CTAs per SM the launch bounds ask for: as many as fit the SM's 228 KB
+    // (1 KB of it reserved per CTA), at most 3 for the SGD and 2 for AdamW
+    static constexpr int kFit = 228 * 1024 / (kBytes + 1024 + 256);
+    static constexpr int kWant = INPLACE ? 1 : (NIN == 2 ? 3 : 2);
+    static constexpr int kCtas = kFit < kWant ? kFit : kWant;
+    static_assert(kKeepAll || (kSgdSpill & (kSgdSpill - 1)) == 0, "ring index uses a mask");
+    static_assert(kBytes <= 227 * 1024 && kCtas >= 1, "shared memory of one CTA");
 };
 
 // Prologue: the new W's header (shift and codebook carried over from W,
@@ -125,11 +134,11 @@ __device__ __forceinline__ uint32_t in_take(InStream &s, uint32_t k, const uint3
 }
 
 // Slot of a spilled new exponent in the staging rows: t = k - marker counts
-// the stream's spilled symbols; out of place the rows are a ring.
-template <bool INPLACE, int SP>
+// the stream's spilled symbols; unless every one is kept the rows are a ring.
+template <bool KEEP_ALL, int SP>
 __device__ __forceinline__ uint32_t stage_row(uint32_t t)
 {
-    return INPLACE ? t : (t & (SP - 1));
+    return KEEP_ALL ? t : (t & (SP - 1));
 }
 
 template <int LEVEL, bool INPLACE, int OP>
@@ -276,7 +285,7 @@ __global__ void __launch_bounds__(kSgdThreads, SgdSmem<LEVEL, INPLACE, UpdateOp<
                 for (int r = 0; r < R; ++r) {
                     const uint32_t kk = c * R + r;
                     if (wr_put_checked(wo, ent[r], kk, colO))
-                        ringj[stage_row<INPLACE, SP>(kk - wo.marker) * kRow] = (uint8_t)exp_of(h[r]);
+                        ringj[stage_row<L::kKeepAll, SP>(kk - wo.marker) * kRow] = (uint8_t)exp_of(h[r]);
                 }
             }
         } else {
@@ -294,7 +303,8 @@ __global__ void __launch_bounds__(kSgdThreads, SgdSmem<LEVEL, INPLACE, UpdateOp<
                 const uint32_t hv = Op::apply(x, k);
                 const uint32_t ev = exp_of(hv);
                 sfo[r * kStreams] = sf_of(hv);
-                if (wr_put_checked(wo, tbl[ev], kk, colO)) ringj[stage_row<INPLACE, SP>(kk - wo.marker) * kRow] = (uint8_t)ev;
+                if (wr_put_checked(wo, tbl[ev], kk, colO))
+                    ringj[stage_row<L::kKeepAll, SP>(kk - wo.marker) * kRow] = (uint8_t)ev;
             }
         }
         __syncthreads();  // every thread is done with this chunk's ring slot
@@ -334,12 +344,12 @@ __global__ void __launch_bounds__(kSgdThreads, SgdSmem<LEVEL, INPLACE, UpdateOp<
             const uint32_t ssp = __shfl_sync(kFull, spill, i);
             const uint32_t spr = __shfl_sync(kFull, pre, i);
             const uint32_t sj = (uint32_t)(warp * 32 + i);
-            const uint32_t kept_from = INPLACE || ssp <= (uint32_t)SP ? 0u : ssp - SP;  // older ones were overwritten
+            const uint32_t kept_from = L::kKeepAll || ssp <= (uint32_t)SP ? 0u : ssp - SP;  // older ones were overwritten
             for (uint32_t l = lane; l < ssp; l += 32)
-                if (INPLACE || l >= kept_from) out[spr + l] = ring[stage_row<INPLACE, SP>(l) * kRow + sj];
+                if (L::kKeepAll || l >= kept_from) out[spr + l] = ring[stage_row<L::kKeepAll, SP>(l) * kRow + sj];
         }
         const uint32_t kept_from = nj > (uint32_t)SP ? nj - SP : 0u;
-        if (!INPLACE && marker < kept_from) {
+        if (!L::kKeepAll && marker < kept_from) {
             // This stream spilled past the kept rows: decode its inputs again
             // from the slot images (still in shared memory) and recompute the
             // older spilled exponents.  W's sign-fraction bytes are intact

@@ -160,9 +160,10 @@ class ClockSampler:
 # ------------------------------------------------------------ GPU arm
 
 def algorithmic_bytes(sizes, ovf_used: int) -> int:
-    """Bytes a codec pass must move for one tensor: compressed form
-    (sign-fraction + slots + markers + offsets + overflow) plus 2 bytes per
-    value on the uncompressed side."""
+    """Bytes of one compressed tensor that a pass over it moves: sign-fraction
+    bytes, full fixed slots, markers, block offsets and the overflow used.
+    Callers add the 2 bytes per value of the uncompressed side where there is
+    one (encode reads it, decode writes it)."""
     return int(sizes.sf_bytes + sizes.slot_bytes + sizes.marker_bytes + sizes.blk_off_bytes + ovf_used)
 
 

@@ -298,3 +298,21 @@ def test_adamw_host_argument_errors_never_reach_the_device(lct_lib):
     ts = six()
     ts[3] = _fake_tensor(lct_lib, base=bases[0])          # W' fully aliases W, overflow included
     assert adam(ts) == E
+
+
+@pytest.mark.parametrize("level,per_value", [(0, 3.3985), (1, 3.5157), (2, 3.6407)])
+def test_roofline_bytes_are_the_format_bytes(lct_lib, level, per_value):
+    """bench.py's roofline numerator: an encode or decode of n values moves the
+    2n uncompressed bytes plus the compressed form (sign-fraction bytes, full
+    fixed slots, markers, block offsets, used overflow), 3.3985 / 3.5157 /
+    3.6407 bytes per value for CLEAN / MEDIUM / HIGH before overflow."""
+    import sys
+    sys.path.insert(0, ROOT)
+    import bench
+    n = 1 << 24
+    sizes = lct_lib.lct_compressed_size(n, level)
+    one = bench.algorithmic_bytes(sizes, 0)
+    assert abs((2 * n + one) / n - per_value) < 3e-4  # the figures are rounded to 4 places
+    assert bench.algorithmic_bytes(sizes, 12345) == one + 12345
+    # the fused SGD reads two compressed tensors and writes one
+    assert 3 * one / n == pytest.approx(3 * (per_value - 2), abs=3e-4)

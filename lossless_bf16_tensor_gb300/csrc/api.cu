@@ -201,6 +201,7 @@ extern "C" lct_status lct_encode(const uint16_t *d_x, const lct_codebook *cb, co
     a.median_exp = cb->median_exp;
     a.pad = 0;
     a.wait_ns = kDefaultWaitNs;
+    set_multipliers(a);
     return launch_encode(a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? LCT_OK : LCT_ERR_CUDA;
 }
 
@@ -220,6 +221,7 @@ extern "C" lct_status lct_decode(const lct_tensor *t, const lct_codebook *cb, ui
     a.y = d_y;
     a.cb = dev_codebook(*cb);
     a.wait_ns = kDefaultWaitNs;
+    set_multipliers(a);
     a.first_block = 0;
     a.pad = 0;
     return launch_decode(a, a.t.nblocks, static_cast<cudaStream_t>(stream)) == cudaSuccess ? LCT_OK : LCT_ERR_CUDA;
@@ -246,6 +248,7 @@ extern "C" lct_status lct_decode_blocks(const lct_tensor *t, const lct_codebook 
     a.y = d_y;
     a.cb = dev_codebook(*cb);
     a.wait_ns = kDefaultWaitNs;
+    set_multipliers(a);
     a.first_block = static_cast<uint32_t>(first_block);
     a.pad = 0;
     return launch_decode(a, static_cast<uint32_t>(nblocks), static_cast<cudaStream_t>(stream)) == cudaSuccess
@@ -282,6 +285,7 @@ extern "C" lct_status lct_sgd_step_fused(const lct_tensor *W_in, const lct_codeb
     a.nin = 2;
     a.in_place = W_out->d_sf == W_in->d_sf ? 1u : 0u;
     a.wait_ns = kDefaultWaitNs;
+    set_multipliers(a);
     return launch_update(a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? LCT_OK : LCT_ERR_CUDA;
 }
 
@@ -325,6 +329,7 @@ extern "C" lct_status lct_sgd_momentum_step_fused(const lct_tensor *W_in, const 
     a.op = OP2_MOMENTUM;
     a.in_place = (W_out->d_sf == W_in->d_sf || M_out->d_sf == M_in->d_sf) ? 1u : 0u;
     a.wait_ns = kDefaultWaitNs;
+    set_multipliers(a);
     return launch_momentum(a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? LCT_OK : LCT_ERR_CUDA;
 }
 
@@ -386,6 +391,7 @@ extern "C" lct_status lct_adamw_step_fused(const lct_tensor *W_in, const lct_cod
     m.op = OP2_ADAM_MOMENTS;
     m.in_place = (M_out->d_sf == M_in->d_sf || V_out->d_sf == V_in->d_sf) ? 1u : 0u;
     m.wait_ns = kDefaultWaitNs;
+    set_multipliers(m);
     if (launch_momentum(m, st) != cudaSuccess) return LCT_ERR_CUDA;
 
     // pass 2: the weight (W, M' and V' in, W' out)
@@ -403,6 +409,7 @@ extern "C" lct_status lct_adamw_step_fused(const lct_tensor *W_in, const lct_cod
     a.nin = 3;
     a.in_place = W_out->d_sf == W_in->d_sf ? 1u : 0u;
     a.wait_ns = kDefaultWaitNs;
+    set_multipliers(a);
     return launch_update(a, st) == cudaSuccess ? LCT_OK : LCT_ERR_CUDA;
 }
 

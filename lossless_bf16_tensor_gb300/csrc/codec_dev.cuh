@@ -142,6 +142,84 @@ __device__ __forceinline__ void rd_take2(uint32_t &p, const uint32_t *__restrict
     p += l0 + (ent1 >> 27);
 }
 
+// ------------------------------------------- pair reader, deferred literal
+
+// Shared-memory loads by 32-bit shared address.
+__device__ __forceinline__ uint32_t lds32(uint32_t addr)
+{
+    uint32_t v;
+    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(addr));
+    return v;
+}
+
+// a * b + c on the FMA pipe.  The multipliers below are powers of two that
+// the kernels receive as launch arguments: a constant one would be folded
+// into a shift on the integer ALU pipe, which is the busiest pipe of the
+// decoders.
+__device__ __forceinline__ uint32_t imad(uint32_t a, uint32_t b, uint32_t c)
+{
+    uint32_t d;
+    asm("mad.lo.u32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+
+// Runtime multipliers: x = 32 (bit position -> byte offset of a slot word
+// row, (p & 0x3E0) * 32 = (p >> 5) * 1024), y = 4 (table index -> byte
+// offset).
+struct Mul {
+    uint32_t x, y;
+};
+
+// One input stream for the pair reader: bit position and the shared address
+// of the stream's column in the slot image (word w at col + 1024 * w).
+struct Rd {
+    uint32_t p, col;
+};
+
+// Two symbols at bit p, with the escape literals left out: ent0 and ent1 are
+// the decode-table entries (exponent in bits 7..14 for a coded symbol, 0 for
+// an escape, whose literal shift is in bits 0..4) and w0, w1 the 32-bit
+// windows at each symbol, from which lit_fix recovers a literal.  A warp
+// pays for the literals only when one of its lanes met an escape.  The word
+// index is taken modulo 32: a position past the slot only arises from
+// corrupt data, whose reads then stay inside the CTA's shared memory (every
+// kernel keeps 33 KB from each slot image on), and the final position check
+// reports it.
+__device__ __forceinline__ void rd_pair(Rd &r, uint32_t lut, const Mul m, uint32_t &w0, uint32_t &w1, uint32_t &ent0,
+                                        uint32_t &ent1)
+{
+    const uint32_t a = imad(r.p & 0x3E0u, m.x, r.col);
+    const uint32_t hi = lds32(a), lo = lds32(a + kStreams * 4);
+    w0 = __funnelshift_l(lo, hi, r.p);  // the next 32 bits
+    ent0 = lds32(imad(w0 >> 24, m.y, lut));
+    const uint32_t l0 = ent0 >> 27;
+    w1 = w0 << l0;
+    ent1 = lds32(imad(w1 >> 24, m.y, lut));
+    r.p += l0 + (ent1 >> 27);
+}
+
+// A decode-table entry with its escape literal added (exponent in bits 7..14).
+__device__ __forceinline__ uint32_t lit_fix(uint32_t w, uint32_t ent) { return ent | esc_literal(w, ent); }
+
+// Nonzero when an entry decodes an escape (its literal shift is not 0).
+__device__ __forceinline__ uint32_t esc_bits(uint32_t ent_or) { return ent_or & 31u; }
+
+// Two float32 results -> two BF16 (round to nearest even, subnormals kept)
+// packed lo | hi << 16; a NaN half becomes this library's NaN 0x7FC0 (the
+// conversion writes 0x7FFF; the NaN test sets a half to 0xFFFF, and 0x7FFF
+// exclusive-or 0x003F is 0x7FC0).
+__device__ __forceinline__ uint32_t bf16x2_rne(float lo, float hi)
+{
+    uint32_t d, nan;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi), "f"(lo));
+    asm("set.nan.u32.bf16x2 %0, %1, %1;" : "=r"(nan) : "r"(d));
+    return d ^ (nan & 0x003F003Fu);
+}
+
+// Sign-fraction bytes of two packed BF16 values, in byte 0 and byte 2 (the
+// other bytes are to be ignored).
+__device__ __forceinline__ uint32_t sf_of2(uint32_t p) { return ((p >> 8) & 0x00800080u) | (p & 0xFF7FFF7Fu); }
+
 // ------------------------------------------------------- stream coding
 
 // Appends codes most significant bit first into one stream's W-word slot
@@ -252,9 +330,22 @@ __device__ __forceinline__ float bf16_f(uint32_t h) { return __uint_as_float(h <
 
 // ------------------------------------------------------------- scans
 
+// Barrier over the CTA (BAR = 0) or over the first NT threads of the CTA on
+// named barrier BAR (the consumer warps of a warp-specialised kernel, whose
+// producer warp does not take part).
+template <int BAR = 0, int NT = 0>
+__device__ __forceinline__ void cta_sync()
+{
+    if constexpr (BAR == 0)
+        __syncthreads();
+    else
+        asm volatile("bar.sync %0, %1;" ::"n"(BAR), "n"(NT) : "memory");
+}
+
 // Exclusive scan of one value per thread over `group_warps` warps starting at
-// warp `first_warp`; *total gets the group's sum.  Contains __syncthreads(),
-// so every thread of the CTA must call it.
+// warp `first_warp`; *total gets the group's sum.  Contains two barriers
+// (cta_sync<BAR, NT>), so every thread taking part in them must call it.
+template <int BAR = 0, int NT = 0>
 __device__ __forceinline__ uint32_t group_exclusive_scan(uint32_t v, uint32_t *warp_tot, int group_warps,
                                                          int first_warp, uint32_t *total)
 {
@@ -266,7 +357,7 @@ __device__ __forceinline__ uint32_t group_exclusive_scan(uint32_t v, uint32_t *w
         if (lane >= o) inc += t;
     }
     if (lane == 31) warp_tot[warp] = inc;
-    __syncthreads();
+    cta_sync<BAR, NT>();
     uint32_t before = 0, sum = 0;
     for (int w = 0; w < group_warps; ++w) {
         const uint32_t t = warp_tot[first_warp + w];
@@ -274,7 +365,7 @@ __device__ __forceinline__ uint32_t group_exclusive_scan(uint32_t v, uint32_t *w
         sum += t;
     }
     *total = sum;
-    __syncthreads();
+    cta_sync<BAR, NT>();
     return before + inc - v;
 }
 

@@ -27,6 +27,8 @@ struct DecodeSmem {
     static constexpr int kRing = kDecRing * kDecRows * kStreams;
     static constexpr int kLut = 256 * 4;
     static constexpr int kBytes = kSlot + kRing + kLut;
+    static_assert(kBytes >= 33 * 1024, "the pair reader's reads stay inside the CTA");
+    static_assert(kDecRows % 8 == 0, "eight-row groups");
 };
 
 template <int LEVEL>
@@ -89,6 +91,8 @@ __global__ void __launch_bounds__(kDecThreads, 4) k_decode(const __grid_constant
 
     if (!mbar_wait(&bar_slot, 0, limit)) s_timeout = 1;
     const uint32_t *col = slot_s + j;
+    const uint32_t col_s = smem_addr(col), lut_s = smem_addr(lut);
+    const Mul mul{a.mul_row, a.mul_ent};
     uint32_t pos = 0;  // bit position in the slot
     uint16_t *yj = a.y + (base - (uint64_t)a.first_block * G::B) + j;
 
@@ -99,15 +103,29 @@ __global__ void __launch_bounds__(kDecThreads, 4) k_decode(const __grid_constant
         const uint8_t *sfc = sf_s + slot * R * kStreams + j;
         uint16_t *yc = yj + (uint64_t)c * R * kStreams;
         if (bulk && __all_sync(kFull, marker >= (c + 1) * R)) {
-            // loads first (the decode chain and the chunk's sign-fraction
-            // bytes), stores last, so nothing orders a load behind a store
-            uint32_t e[R], sf[R];
+            // eight rows at a time: the symbols two by two with the escape
+            // literals deferred (added only when a lane of the warp met an
+            // escape), then the sign-fraction bytes and the joined values
 #pragma unroll
-            for (int r = 0; r < R; r += 2) rd_take2<W>(pos, col, lut, e[r], e[r + 1]);
+            for (int g = 0; g < R / 8; ++g) {
+                uint32_t wv[8], ev[8], esc = 0;
 #pragma unroll
-            for (int r = 0; r < R; ++r) sf[r] = sfc[r * kStreams];
+                for (int q = 0; q < 4; ++q) {
+                    Rd r{pos, col_s};
+                    rd_pair(r, lut_s, mul, wv[2 * q], wv[2 * q + 1], ev[2 * q], ev[2 * q + 1]);
+                    pos = r.p;
+                    esc |= ev[2 * q] | ev[2 * q + 1];
+                }
+                if (__any_sync(kFull, esc_bits(esc))) {
 #pragma unroll
-            for (int r = 0; r < R; ++r) yc[r * kStreams] = (uint16_t)join_one(sf[r], e[r]);
+                    for (int t = 0; t < 8; ++t) ev[t] = lit_fix(wv[t], ev[t]);
+                }
+                uint32_t sf[8];
+#pragma unroll
+                for (int t = 0; t < 8; ++t) sf[t] = sfc[(g * 8 + t) * kStreams];
+#pragma unroll
+                for (int t = 0; t < 8; ++t) yc[(g * 8 + t) * kStreams] = (uint16_t)join_one(sf[t], ev[t]);
+            }
         } else {
             for (int r = 0; r < R; ++r) {
                 const uint32_t k = c * R + r;

@@ -62,6 +62,10 @@ struct DevTensor {
     int32_t level;
 };
 
+// Every argument block carries two multipliers, 32 and 4, that the decoders
+// use for address arithmetic: as launch arguments they are not compile-time
+// constants, so the multiply-adds stay on the FMA pipe instead of becoming
+// shifts on the integer ALU pipe.
 struct EncodeArgs {
     const uint16_t *x;
     DevTensor t;
@@ -69,6 +73,7 @@ struct EncodeArgs {
     int32_t median_exp;
     uint32_t pad;
     uint64_t wait_ns;
+    uint32_t mul_row, mul_ent;  // 32 and 4 (set_multipliers)
 };
 
 struct DecodeArgs {
@@ -78,6 +83,7 @@ struct DecodeArgs {
     uint64_t wait_ns;
     uint32_t first_block;  // the launch decodes blocks first_block .. + grid size
     uint32_t pad;
+    uint32_t mul_row, mul_ent;  // 32 and 4 (set_multipliers)
 };
 
 // Weight updates of the fused one-pass kernel.
@@ -93,6 +99,7 @@ struct UpdateArgs {
     uint32_t in_place;    // W_out's sign-fraction bytes are W_in's
     uint32_t pad;
     uint64_t wait_ns;
+    uint32_t mul_row, mul_ent;  // 32 and 4 (set_multipliers)
 };
 
 // Updates of the fused two-state kernel (two compressed tensors and a dense
@@ -107,7 +114,15 @@ struct MomentumArgs {
     uint32_t op;        // OP2_MOMENTUM or OP2_ADAM_MOMENTS
     uint32_t in_place;  // an output shares its input's sign-fraction bytes
     uint64_t wait_ns;
+    uint32_t mul_row, mul_ent;  // 32 and 4 (set_multipliers)
 };
+
+template <typename Args>
+inline void set_multipliers(Args &a)
+{
+    a.mul_row = 32;
+    a.mul_ent = 4;
+}
 
 cudaError_t launch_encode(const EncodeArgs &a, cudaStream_t s);
 cudaError_t launch_decode(const DecodeArgs &a, uint32_t nblocks, cudaStream_t s);

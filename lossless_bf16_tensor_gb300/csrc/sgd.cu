@@ -27,20 +27,23 @@
 namespace lct {
 namespace dev {
 
-constexpr int kSgdThreads = 256;
-constexpr int kSgdRows = 8;    // rows per sign-fraction chunk
-constexpr int kSgdSpill = 32;  // spilled new-exponent rows kept (out of place; a power of two)
+constexpr int kSgdThreads = 256;                 // consumer threads: one per stream
+constexpr int kSgdBlock = kSgdThreads + 32;      // and one producer warp
+constexpr int kSgdRows = 8;        // rows per sign-fraction chunk
+constexpr int kSgdRowsClean = 8;   // rows per chunk out of place in CLEAN
+constexpr int kSgdSpill = 32;      // spilled new-exponent rows kept (out of place in CLEAN; 0 or a power of two)
 
 template <int OP>
 struct UpdateOp;
 
-// W' = bf16(fl32(w - fl32(k0*m))): product and difference rounded separately.
+// W' = bf16(fl32(w - fl32(k0*m))): product and difference rounded separately
+// (apply returns the float32 result; the caller rounds it to BF16).
 template <>
 struct UpdateOp<OP_SGD> {
     static constexpr int kInputs = 2;
-    __device__ static __forceinline__ uint32_t apply(const uint32_t (&x)[2], const float *k)
+    __device__ static __forceinline__ float apply(const uint32_t (&x)[2], const float *k)
     {
-        return bf16_rne(__fsub_rn(bf16_f(x[0]), __fmul_rn(k[0], bf16_f(x[1]))));
+        return __fsub_rn(bf16_f(x[0]), __fmul_rn(k[0], bf16_f(x[1])));
     }
 };
 
@@ -49,12 +52,12 @@ struct UpdateOp<OP_SGD> {
 template <>
 struct UpdateOp<OP_ADAMW> {
     static constexpr int kInputs = 3;
-    __device__ static __forceinline__ uint32_t apply(const uint32_t (&x)[3], const float *k)
+    __device__ static __forceinline__ float apply(const uint32_t (&x)[3], const float *k)
     {
         const float w = bf16_f(x[0]);
         const float den = __fadd_rn(__fmul_rn(__fsqrt_rn(bf16_f(x[2])), k[5]), k[6]);
         const float upd = __fdiv_rn(__fmul_rn(k[4], bf16_f(x[1])), den);
-        return bf16_rne(__fsub_rn(__fsub_rn(w, __fmul_rn(k[7], w)), upd));
+        return __fsub_rn(__fsub_rn(w, __fmul_rn(k[7], w)), upd);
     }
 };
 
@@ -69,7 +72,8 @@ struct SgdSmem {
     static constexpr int kSpillRows = kKeepAll ? NJ - 2 * W : kSgdSpill;
     static constexpr int kStages = INPLACE ? 3 : 2;  // chunks in flight
     static constexpr int kSlotIn = (W + 1) * kStreams * 4;  // + zero guard row
-    static constexpr int kRing = kStages * kSgdRows * kStreams;  // per input
+    static constexpr int kRows = kKeepAll ? kSgdRows : kSgdRowsClean;  // rows per chunk
+    static constexpr int kRing = kStages * kRows * kStreams;  // per input
     static constexpr int kLuts = NIN * 256 * 4 + 256 * 8;
     static constexpr int kSpill = (kSpillRows * kRow + 127) / 128 * 128;
     static constexpr int kBytes = NIN * kSlotIn + NIN * kRing + kLuts + kSpill;
@@ -79,7 +83,10 @@ struct SgdSmem {
     static constexpr int kWant = INPLACE ? 1 : (NIN == 2 ? 3 : 2);
     static constexpr int kCtas = kFit < kWant ? kFit : kWant;
     static_assert(kKeepAll || (kSgdSpill & (kSgdSpill - 1)) == 0, "ring index uses a mask");
+    static_assert(kRows % 4 == 0, "four-row groups");
     static_assert(kBytes <= 227 * 1024 && kCtas >= 1, "shared memory of one CTA");
+    // the pair reader's reads from the last slot image stay inside the CTA
+    static_assert((NIN - 1) * kSlotIn + 33 * 1024 <= kBytes, "33 KB after every slot image");
 };
 
 // Prologue: the new W's header (shift and codebook carried over from W,
@@ -141,15 +148,99 @@ __device__ __forceinline__ uint32_t stage_row(uint32_t t)
     return KEEP_ALL ? t : (t & (SP - 1));
 }
 
+// Four rows of every stream on the fast path (every input symbol of the rows
+// lies in its slot).  The inputs' symbols are decoded two at a time with the
+// escape literals deferred (a warp fixes them up only when one of its lanes
+// met an escape), the four values are updated and rounded two at a time, and
+// their sign-fraction bytes written.  When no new exponent of the warp's
+// streams differs from the old weight's, the new codes are the old weight's
+// codes bit for bit (same codebook, same stored shift), so the rows' bits are
+// appended straight from the old weight's stream window.  Otherwise the new
+// codes are looked up and appended, with the fit check per value only when
+// some stream of the warp may not keep all four.
+template <int W, int NIN, typename Op, bool KEEP_ALL, int SP>
+__device__ __forceinline__ void update_group(InStream (&in)[NIN], const uint32_t (&col_s)[NIN],
+                                             const uint32_t (&lut_s)[NIN], const Mul mul,
+                                             uint8_t *const (&sf_s)[NIN], uint32_t sf_at, const float *k,
+                                             const uint2 *tbl, Writer &wo, uint32_t *colO, uint8_t *sfo,
+                                             uint8_t *ringj, uint32_t k0)
+{
+    uint32_t wv[NIN][4], ev[NIN][4], esc = 0;
+    const uint32_t p0 = in[0].pos;
+#pragma unroll
+    for (int q = 0; q < 2; ++q)
+#pragma unroll
+        for (int i = 0; i < NIN; ++i) {
+            Rd r{in[i].pos, col_s[i]};
+            rd_pair(r, lut_s[i], mul, wv[i][2 * q], wv[i][2 * q + 1], ev[i][2 * q], ev[i][2 * q + 1]);
+            in[i].pos = r.p;
+            esc |= ev[i][2 * q] | ev[i][2 * q + 1];
+        }
+    if (__any_sync(kFull, esc_bits(esc))) {
+#pragma unroll
+        for (int i = 0; i < NIN; ++i)
+#pragma unroll
+            for (int t = 0; t < 4; ++t) ev[i][t] = lit_fix(wv[i][t], ev[i][t]);
+    }
+    const uint32_t bc = in[0].pos - p0;  // the old weight's bits of these rows
+    uint32_t P[2], same = 0;
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+        float r[2];
+        uint32_t xw[2];
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+            uint32_t x[NIN];
+#pragma unroll
+            for (int i = 0; i < NIN; ++i) x[i] = join_one(sf_s[i][sf_at + (2 * q + t) * kStreams], ev[i][2 * q + t]);
+            xw[t] = x[0];
+            r[t] = Op::apply(x, k);
+        }
+        P[q] = bf16x2_rne(r[0], r[1]);
+        same |= P[q] ^ __byte_perm(xw[0], xw[1], 0x5410);  // old weight values, packed the same way
+        const uint32_t sfp = sf_of2(P[q]);
+        sfo[(2 * q) * kStreams] = (uint8_t)sfp;
+        sfo[(2 * q + 1) * kStreams] = (uint8_t)(sfp >> 16);
+    }
+    if (__all_sync(kFull, wo.alive && !(same & 0x7F807F80u) && bc <= 32u && bc <= wo.rem)) {
+        wr_add(wo, make_uint2(wv[0][0] & ~(0xFFFFFFFFu >> bc), bc));
+        wr_flush(wo, colO);
+        wo.rem -= bc;
+        return;
+    }
+    const uint32_t h[4] = {P[0], P[0] >> 16, P[1], P[1] >> 16};
+    uint2 ent[4];
+    uint32_t need = 0;
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+        ent[t] = code_of(tbl, h[t]);
+        need += ent[t].y;
+    }
+    if (__all_sync(kFull, wo.alive && need <= wo.rem)) {
+        wr_add2(wo, ent[0], ent[1]);
+        wr_flush(wo, colO);
+        wr_add2(wo, ent[2], ent[3]);
+        wr_flush(wo, colO);
+        wo.rem -= need;
+    } else {
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+            const uint32_t kk = k0 + t;
+            if (wr_put_checked(wo, ent[t], kk, colO) && SP > 0)
+                ringj[stage_row<KEEP_ALL, SP>(kk - wo.marker) * kRow] = (uint8_t)exp_of(h[t]);
+        }
+    }
+}
+
 template <int LEVEL, bool INPLACE, int OP>
-__global__ void __launch_bounds__(kSgdThreads, SgdSmem<LEVEL, INPLACE, UpdateOp<OP>::kInputs>::kCtas)
+__global__ void __launch_bounds__(kSgdBlock, SgdSmem<LEVEL, INPLACE, UpdateOp<OP>::kInputs>::kCtas)
     k_update(const __grid_constant__ UpdateArgs a)
 {
     using G = Geo<LEVEL>;
     using Op = UpdateOp<OP>;
     constexpr int NIN = Op::kInputs;
     using L = SgdSmem<LEVEL, INPLACE, NIN>;
-    constexpr int W = G::W, R = kSgdRows, S = L::kStages, SP = L::kSpillRows;
+    constexpr int W = G::W, R = L::kRows, S = L::kStages, SP = L::kSpillRows;
     constexpr int NW = kSgdThreads / 32;
     extern __shared__ __align__(128) uint8_t smem[];
     uint32_t *slot[NIN];
@@ -163,7 +254,16 @@ __global__ void __launch_bounds__(kSgdThreads, SgdSmem<LEVEL, INPLACE, UpdateOp<
     }
     uint2 *tbl = reinterpret_cast<uint2 *>(lut[0] + NIN * 256);
     uint8_t *ring = reinterpret_cast<uint8_t *>(tbl + 256);
-    __shared__ __align__(8) uint64_t bar_slot, bar_sf[S];
+    uint32_t col_s[NIN], lut_s[NIN];
+#pragma unroll
+    for (int i = 0; i < NIN; ++i) {
+        col_s[i] = smem_addr(slot[i] + threadIdx.x);
+        lut_s[i] = smem_addr(lut[i]);
+    }
+    const Mul mul{a.mul_row, a.mul_ent};
+    // bar_sf[s]: stage s of the ring has landed; bar_free[s]: every consumer
+    // warp is done with stage s (the producer may refill it)
+    __shared__ __align__(8) uint64_t bar_slot, bar_sf[S], bar_free[S];
     __shared__ uint32_t warp_tot[NW];
     __shared__ unsigned long long s_excl;
     __shared__ uint32_t s_flags;  // bit 0: a wait gave up, bit 1: corrupt input
@@ -177,7 +277,10 @@ __global__ void __launch_bounds__(kSgdThreads, SgdSmem<LEVEL, INPLACE, UpdateOp<
 
     if (j == 0) {
         mbar_init(&bar_slot, 1);
-        for (int s = 0; s < S; ++s) mbar_init(&bar_sf[s], 1);
+        for (int s = 0; s < S; ++s) {
+            mbar_init(&bar_sf[s], 1);
+            mbar_init(&bar_free[s], NW);
+        }
         fence_mbar_init();
         s_flags = 0;
     }
@@ -185,28 +288,39 @@ __global__ void __launch_bounds__(kSgdThreads, SgdSmem<LEVEL, INPLACE, UpdateOp<
     pdl_wait();
     bool bad = false;
     const int delta_w = a.w_out.hdr->delta;  // the prologue copied W's shift
+    if (j < kSgdThreads) {
 #pragma unroll
-    for (int i = 0; i < NIN; ++i) {
-        const lct_header *h = a.in[i].hdr;
-        bad |= !(h->magic == LCT_MAGIC && h->n == a.in[i].n && h->level == LEVEL && h->cb_hash == a.cb[i].hash);
-        lut[i][j] = dec_entry(a.cb[i], i == 0 ? delta_w : h->delta, j);
-        slot[i][W * kStreams + j] = 0u;
+        for (int i = 0; i < NIN; ++i) {
+            const lct_header *h = a.in[i].hdr;
+            bad |= !(h->magic == LCT_MAGIC && h->n == a.in[i].n && h->level == LEVEL && h->cb_hash == a.cb[i].hash);
+            lut[i][j] = dec_entry(a.cb[i], i == 0 ? delta_w : h->delta, j);
+            slot[i][W * kStreams + j] = 0u;
+        }
+        tbl[j] = enc_entry(a.cb[0], delta_w, j);
     }
-    tbl[j] = enc_entry(a.cb[0], delta_w, j);
-    __syncthreads();  // barriers initialised
-    auto issue = [&](uint32_t c) {
-        mbar_expect_tx(&bar_sf[c % S], NIN * R * kStreams);
+    __syncthreads();  // barriers initialised, tables built
+    if (warp == NW) {
+        // Producer warp: the slot images, then every chunk of the ring, each
+        // stage refilled as soon as all consumer warps have released it.
+        if (lane == 0) {
+            mbar_expect_tx(&bar_slot, NIN * W * kStreams * 4);
 #pragma unroll
-        for (int i = 0; i < NIN; ++i)
-            bulk_load(sf_s[i] + (c % S) * R * kStreams, a.in[i].sf + base + (uint64_t)c * R * kStreams,
-                      R * kStreams, &bar_sf[c % S]);
-    };
-    if (j == 0) {
-        mbar_expect_tx(&bar_slot, NIN * W * kStreams * 4);
+            for (int i = 0; i < NIN; ++i)
+                bulk_load(slot[i], a.in[i].slots + (uint64_t)b * W * kStreams, W * kStreams * 4, &bar_slot);
+            bool gave_up = false;
+            for (uint32_t c = 0; c < nbulk; ++c) {
+                const uint32_t st = c % S;
+                if (c >= (uint32_t)S && !mbar_wait(&bar_free[st], (c / S - 1) & 1u, gave_up ? 1000000ull : limit))
+                    gave_up = true;
+                mbar_expect_tx(&bar_sf[st], NIN * R * kStreams);
 #pragma unroll
-        for (int i = 0; i < NIN; ++i)
-            bulk_load(slot[i], a.in[i].slots + (uint64_t)b * W * kStreams, W * kStreams * 4, &bar_slot);
-        for (uint32_t c = 0; c < (uint32_t)S && c < nbulk; ++c) issue(c);
+                for (int i = 0; i < NIN; ++i)
+                    bulk_load(sf_s[i] + st * R * kStreams, a.in[i].sf + base + (uint64_t)c * R * kStreams,
+                              R * kStreams, &bar_sf[st]);
+            }
+            if (gave_up) atomicOr(&s_flags, 1u);
+        }
+        return;
     }
 
     // input markers, spill prefixes and overflow ranges
@@ -220,7 +334,7 @@ __global__ void __launch_bounds__(kSgdThreads, SgdSmem<LEVEL, INPLACE, UpdateOp<
         bad |= mk > nj;
         in[i].marker = min(mk, nj);
         uint32_t tot;
-        const uint32_t pre = group_exclusive_scan(nj - in[i].marker, warp_tot, NW, 0, &tot);
+        const uint32_t pre = group_exclusive_scan<1, kSgdThreads>(nj - in[i].marker, warp_tot, NW, 0, &tot);
         const uint64_t o0 = a.in[i].blk_off[b], o1 = a.in[i].blk_off[b + 1];
         ovf_ok[i] = o1 <= a.in[i].ovf_cap && o0 <= o1 && o1 - o0 == tot;
         in[i].ovf_at = o0 + pre - in[i].marker;
@@ -248,46 +362,12 @@ __global__ void __launch_bounds__(kSgdThreads, SgdSmem<LEVEL, INPLACE, UpdateOp<
 #pragma unroll
         for (int i = 0; i < NIN; ++i) in_slot = in_slot && in[i].marker >= kend;
         if (bulk && __all_sync(kFull, in_slot)) {
-            // loads first (the decode chains, the sign-fraction bytes, the
-            // new values' code-table entries), stores last, so nothing orders
-            // a load behind a store
-            uint32_t e[NIN][R], h[R], need = 0;
-            uint2 ent[R];
+            const uint32_t sf_at = slot_c * R * kStreams;
 #pragma unroll
-            for (int r = 0; r < R; r += 2) {
-#pragma unroll
-                for (int i = 0; i < NIN; ++i) rd_take2<W>(in[i].pos, in[i].col, lut[i], e[i][r], e[i][r + 1]);
-            }
-#pragma unroll
-            for (int r = 0; r < R; ++r) {
-                uint32_t x[NIN];
-#pragma unroll
-                for (int i = 0; i < NIN; ++i) x[i] = join_one(sf_s[i][slot_c * R * kStreams + r * kStreams + j], e[i][r]);
-                h[r] = Op::apply(x, k);
-            }
-#pragma unroll
-            for (int r = 0; r < R; ++r) {
-                ent[r] = code_of(tbl, h[r]);
-                need += ent[r].y;
-            }
-#pragma unroll
-            for (int r = 0; r < R; ++r) sfo[r * kStreams] = sf_of(h[r]);
-            if (__all_sync(kFull, wo.alive && need <= wo.rem)) {
-                // every new stream of the warp keeps the whole chunk in its slot
-#pragma unroll
-                for (int r = 0; r < R; r += 2) {  // two codes fit the accumulator, then one flush
-                    wr_add2(wo, ent[r], ent[r + 1]);
-                    wr_flush(wo, colO);
-                }
-                wo.rem -= need;
-            } else {
-#pragma unroll
-                for (int r = 0; r < R; ++r) {
-                    const uint32_t kk = c * R + r;
-                    if (wr_put_checked(wo, ent[r], kk, colO))
-                        ringj[stage_row<L::kKeepAll, SP>(kk - wo.marker) * kRow] = (uint8_t)exp_of(h[r]);
-                }
-            }
+            for (int g = 0; g < R / 4; ++g)
+                update_group<W, NIN, Op, L::kKeepAll, SP>(in, col_s, lut_s, mul, sf_s, sf_at + g * 4 * kStreams + j,
+                                                          k, tbl, wo, colO, sfo + g * 4 * kStreams, ringj,
+                                                          c * R + g * 4);
         } else {
             for (int r = 0; r < R; ++r) {
                 const uint32_t kk = c * R + r;
@@ -300,15 +380,17 @@ __global__ void __launch_bounds__(kSgdThreads, SgdSmem<LEVEL, INPLACE, UpdateOp<
                     const uint32_t fi = bulk ? sf_s[i][slot_c * R * kStreams + r * kStreams + j] : a.in[i].sf[at];
                     x[i] = join_one(fi, ei);
                 }
-                const uint32_t hv = Op::apply(x, k);
+                const uint32_t hv = bf16_rne(Op::apply(x, k));
                 const uint32_t ev = exp_of(hv);
                 sfo[r * kStreams] = sf_of(hv);
-                if (wr_put_checked(wo, tbl[ev], kk, colO))
+                if (wr_put_checked(wo, tbl[ev], kk, colO) && SP > 0)
                     ringj[stage_row<L::kKeepAll, SP>(kk - wo.marker) * kRow] = (uint8_t)ev;
             }
         }
-        __syncthreads();  // every thread is done with this chunk's ring slot
-        if (j == 0 && c + S < nbulk) issue(c + S);
+        if (bulk) {  // this warp is done with the chunk's ring stage
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bar_free[slot_c]);
+        }
     }
 #pragma unroll
     for (int i = 0; i < NIN; ++i) bad |= in[i].pos > 32u * W;
@@ -316,7 +398,7 @@ __global__ void __launch_bounds__(kSgdThreads, SgdSmem<LEVEL, INPLACE, UpdateOp<
     wr_finish<W>(wo, colO);
     const uint32_t marker = wo.marker, spill = nj - marker;
     uint32_t total;
-    const uint32_t pre = group_exclusive_scan(spill, warp_tot, NW, 0, &total);
+    const uint32_t pre = group_exclusive_scan<1, kSgdThreads>(spill, warp_tot, NW, 0, &total);
     a.w_out.markers[(uint64_t)b * kStreams + j] = (uint16_t)marker;
 
     if (warp == 0) {
@@ -334,7 +416,7 @@ __global__ void __launch_bounds__(kSgdThreads, SgdSmem<LEVEL, INPLACE, UpdateOp<
             s_excl = excl;
         }
     }
-    __syncthreads();
+    cta_sync<1, kSgdThreads>();
 
     const unsigned long long excl = s_excl;
     if (total > 0 && excl + total <= a.w_out.ovf_cap) {
@@ -366,7 +448,7 @@ __global__ void __launch_bounds__(kSgdThreads, SgdSmem<LEVEL, INPLACE, UpdateOp<
 #pragma unroll
                 for (int i = 0; i < NIN; ++i)
                     x[i] = join_one(a.in[i].sf[at], in_take<W>(re[i], kk, lut[i], a.in[i].ovf, ovf_ok[i]));
-                const uint32_t hv = Op::apply(x, k);
+                const uint32_t hv = bf16_rne(Op::apply(x, k));
                 if (kk >= marker) out[pre + (kk - marker)] = exp_of(hv);
             }
         }
@@ -390,7 +472,7 @@ cudaError_t launch_level(const UpdateArgs &a, cudaStream_t s)
     cudaError_t err =
         cudaFuncSetAttribute(k_update<LEVEL, INPLACE, OP>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (err != cudaSuccess) return err;
-    return launch_pdl(k_update<LEVEL, INPLACE, OP>, dim3(a.w_out.nblocks), dim3(kSgdThreads), smem, s, a);
+    return launch_pdl(k_update<LEVEL, INPLACE, OP>, dim3(a.w_out.nblocks), dim3(kSgdBlock), smem, s, a);
 }
 
 template <int LEVEL, int OP>

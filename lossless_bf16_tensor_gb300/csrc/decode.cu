@@ -58,18 +58,10 @@ __global__ void __launch_bounds__(kDecThreads, 4) k_decode(const __grid_constant
         fence_mbar_init();
         s_timeout = 0;
     }
-    // Everything below reads what earlier work in the stream wrote.
+    // Everything below reads what earlier work in the stream wrote.  The
+    // copies and every global read of the block's start are issued before the
+    // first barrier so that their latencies overlap.
     pdl_wait();
-    lct_header *hdr = a.t.hdr;
-    const bool hdr_ok = hdr->magic == LCT_MAGIC && hdr->n == a.t.n && hdr->level == LEVEL &&
-                        hdr->cb_hash == a.cb.hash;
-    if (!hdr_ok) {
-        if (j == 0) latch(hdr, LCT_ERR_CORRUPT);
-        return;  // no copy has been issued yet
-    }
-    lut[j] = dec_entry(a.cb, hdr->delta, j);
-    slot_s[W * kStreams + j] = 0u;
-    __syncthreads();  // barriers initialised
     if (j == 0) {
         mbar_expect_tx(&bar_slot, W * kStreams * 4);
         bulk_load(slot_s, a.t.slots + (uint64_t)b * W * kStreams, W * kStreams * 4, &bar_slot);
@@ -78,14 +70,30 @@ __global__ void __launch_bounds__(kDecThreads, 4) k_decode(const __grid_constant
             bulk_load(sf_s + c * R * kStreams, a.t.sf + base + (uint64_t)c * R * kStreams, R * kStreams, &bar_sf[c]);
         }
     }
-
+    lct_header *hdr = a.t.hdr;
+    const bool hdr_ok = hdr->magic == LCT_MAGIC && hdr->n == a.t.n && hdr->level == LEVEL &&
+                        hdr->cb_hash == a.cb.hash;
+    const int delta = hdr->delta;
     const uint32_t nj = nb > (uint32_t)j ? (nb - j + 255) / 256 : 0;
     uint32_t marker = a.t.markers[(uint64_t)b * kStreams + j];
+    const uint64_t off0 = a.t.blk_off[b], off1 = a.t.blk_off[b + 1];
+    if (!hdr_ok) {
+        if (j == 0) {
+            latch(hdr, LCT_ERR_CORRUPT);
+            // let the copies issued above land before the CTA goes away
+            mbar_wait(&bar_slot, 0, limit);
+            for (uint32_t c = 0; c < (uint32_t)S && c < nbulk; ++c) mbar_wait(&bar_sf[c], 0, limit);
+        }
+        return;
+    }
+    lut[j] = dec_entry(a.cb, delta, j);
+    slot_s[W * kStreams + j] = 0u;
+    __syncthreads();  // table built
+
     bool bad = marker > nj;
     marker = min(marker, nj);
     uint32_t total;
     const uint32_t pre = group_exclusive_scan(nj - marker, warp_tot, kDecThreads / 32, 0, &total);
-    const uint64_t off0 = a.t.blk_off[b], off1 = a.t.blk_off[b + 1];
     const bool ovf_ok = off1 <= a.t.ovf_cap && off0 <= off1 && off1 - off0 == total;
     const uint64_t ovf_at = off0 + pre - marker;  // overflow index of spilled symbol k is ovf_at + k
 

@@ -275,69 +275,85 @@ __global__ void __launch_bounds__(kSgdBlock, SgdSmem<LEVEL, INPLACE, UpdateOp<OP
     const uint32_t nrows = (nb + 255) >> 8, nbulk = (nb >> 8) / R, nchunks = (nrows + R - 1) / R;
     const uint64_t limit = a.wait_ns;
 
-    if (j == 0) {
-        mbar_init(&bar_slot, 1);
-        for (int s = 0; s < S; ++s) {
-            mbar_init(&bar_sf[s], 1);
-            mbar_init(&bar_free[s], NW);
-        }
-        fence_mbar_init();
-        s_flags = 0;
-    }
-    // inputs, the new header and the cleared look-back words are all ready
-    pdl_wait();
-    bool bad = false;
-    const int delta_w = a.w_out.hdr->delta;  // the prologue copied W's shift
-    if (j < kSgdThreads) {
-#pragma unroll
-        for (int i = 0; i < NIN; ++i) {
-            const lct_header *h = a.in[i].hdr;
-            bad |= !(h->magic == LCT_MAGIC && h->n == a.in[i].n && h->level == LEVEL && h->cb_hash == a.cb[i].hash);
-            lut[i][j] = dec_entry(a.cb[i], i == 0 ? delta_w : h->delta, j);
-            slot[i][W * kStreams + j] = 0u;
-        }
-        tbl[j] = enc_entry(a.cb[0], delta_w, j);
-    }
-    __syncthreads();  // barriers initialised, tables built
     if (warp == NW) {
-        // Producer warp: the slot images, then every chunk of the ring, each
-        // stage refilled as soon as all consumer warps have released it.
+        // Producer warp: initialise the barriers, issue the slot images and
+        // the first stages of the ring at once, then refill each stage as soon
+        // as all consumer warps have released it.
+        if (lane == 0) {
+            mbar_init(&bar_slot, 1);
+            for (int s = 0; s < S; ++s) {
+                mbar_init(&bar_sf[s], 1);
+                mbar_init(&bar_free[s], NW);
+            }
+            fence_mbar_init();
+            s_flags = 0;
+        }
+        pdl_wait();  // the inputs are complete
+        auto issue = [&](uint32_t c) {
+            const uint32_t st = c % S;
+            mbar_expect_tx(&bar_sf[st], NIN * R * kStreams);
+#pragma unroll
+            for (int i = 0; i < NIN; ++i)
+                bulk_load(sf_s[i] + st * R * kStreams, a.in[i].sf + base + (uint64_t)c * R * kStreams, R * kStreams,
+                          &bar_sf[st]);
+        };
         if (lane == 0) {
             mbar_expect_tx(&bar_slot, NIN * W * kStreams * 4);
 #pragma unroll
             for (int i = 0; i < NIN; ++i)
                 bulk_load(slot[i], a.in[i].slots + (uint64_t)b * W * kStreams, W * kStreams * 4, &bar_slot);
+            for (uint32_t c = 0; c < (uint32_t)S && c < nbulk; ++c) issue(c);
+        }
+        __syncthreads();  // barriers initialised, tables built
+        if (lane == 0) {
             bool gave_up = false;
-            for (uint32_t c = 0; c < nbulk; ++c) {
-                const uint32_t st = c % S;
-                if (c >= (uint32_t)S && !mbar_wait(&bar_free[st], (c / S - 1) & 1u, gave_up ? 1000000ull : limit))
-                    gave_up = true;
-                mbar_expect_tx(&bar_sf[st], NIN * R * kStreams);
-#pragma unroll
-                for (int i = 0; i < NIN; ++i)
-                    bulk_load(sf_s[i] + st * R * kStreams, a.in[i].sf + base + (uint64_t)c * R * kStreams,
-                              R * kStreams, &bar_sf[st]);
+            for (uint32_t c = S; c < nbulk; ++c) {
+                if (!mbar_wait(&bar_free[c % S], (c / S - 1) & 1u, gave_up ? 1000000ull : limit)) gave_up = true;
+                issue(c);
             }
             if (gave_up) atomicOr(&s_flags, 1u);
         }
         return;
     }
 
-    // input markers, spill prefixes and overflow ranges
+    // Consumer warps, thread j = stream j.  Every global read of the block's
+    // start is issued before the first barrier so that their latencies overlap.
+    pdl_wait();  // inputs, the new header and the cleared look-back words are all ready
     const uint32_t nj = nb > (uint32_t)j ? (nb - j + 255) / 256 : 0;
+    const int delta_w = a.w_out.hdr->delta;  // the prologue copied W's shift
+    uint32_t mk[NIN];
+    uint64_t o0[NIN], o1[NIN];
+    bool bad = false;
+    int delta_in[NIN];
+#pragma unroll
+    for (int i = 0; i < NIN; ++i) {
+        mk[i] = a.in[i].markers[(uint64_t)b * kStreams + j];
+        o0[i] = a.in[i].blk_off[b];
+        o1[i] = a.in[i].blk_off[b + 1];
+        const lct_header *h = a.in[i].hdr;
+        bad |= !(h->magic == LCT_MAGIC && h->n == a.in[i].n && h->level == LEVEL && h->cb_hash == a.cb[i].hash);
+        delta_in[i] = h->delta;
+    }
+#pragma unroll
+    for (int i = 0; i < NIN; ++i) {
+        lut[i][j] = dec_entry(a.cb[i], i == 0 ? delta_w : delta_in[i], j);
+        slot[i][W * kStreams + j] = 0u;
+    }
+    tbl[j] = enc_entry(a.cb[0], delta_w, j);
+    __syncthreads();  // barriers initialised, tables built
+
+    // input markers, spill prefixes and overflow ranges
     InStream in[NIN];
     bool ovf_ok[NIN];
 #pragma unroll
     for (int i = 0; i < NIN; ++i) {
         in[i].col = slot[i] + j;
-        const uint32_t mk = a.in[i].markers[(uint64_t)b * kStreams + j];
-        bad |= mk > nj;
-        in[i].marker = min(mk, nj);
+        bad |= mk[i] > nj;
+        in[i].marker = min(mk[i], nj);
         uint32_t tot;
         const uint32_t pre = group_exclusive_scan<1, kSgdThreads>(nj - in[i].marker, warp_tot, NW, 0, &tot);
-        const uint64_t o0 = a.in[i].blk_off[b], o1 = a.in[i].blk_off[b + 1];
-        ovf_ok[i] = o1 <= a.in[i].ovf_cap && o0 <= o1 && o1 - o0 == tot;
-        in[i].ovf_at = o0 + pre - in[i].marker;
+        ovf_ok[i] = o1[i] <= a.in[i].ovf_cap && o0[i] <= o1[i] && o1[i] - o0[i] == tot;
+        in[i].ovf_at = o0[i] + pre - in[i].marker;
         bad |= !ovf_ok[i];
         in[i].pos = 0;
     }

@@ -6,25 +6,31 @@ A step is one pass of the whole hot path over one synthetic batch:
   2. lct_decode         streams -> BF16
   3. lct_sgd_step_fused W <- W - eta*M on the compressed W (the tensor just
                         encoded) and a compressed momentum M
-value = uncompressed BF16 bytes passed through the codec per second: encode
-2N + decode 2N + fused SGD 6N (decodes W and M, encodes W) per step.
+value = uncompressed BF16 GB/s through the codec: 2N bytes encoded plus 2N
+bytes decoded per step, over the time from the step's start to the end of its
+decode (an event between the decode and the fused SGD; the fused SGD's own
+time and rate are reported beside it, and ms_per_step covers the whole step).
 
 Default workload: 2^24 BF16 values ~ Laplace(0, 0.01), Laplace codebook,
 CLEAN blocks; M ~ Laplace(0, 1e-3).  L2 is flushed (256 MiB write) before
-every timed step, outside the step's events.  The timed steps carry events
-only at their boundaries; the per-kernel times (and the roofline of the
-dominant kernel) come from a second pass of as many steps with an event after
-every kernel.
+every timed step, outside the step's events.  The per-kernel times (and the
+roofline of the dominant kernel) come from a second pass with the L2 flushed
+before every kernel.  breakdown.configs holds the five workload
+configurations (one block of N(0,0.02); 2^24 Laplace; 2^26 heavy-tailed
+MEDIUM; 162M fused SGD; GELU activations at 9 scales, HIGH), each with the
+oracle timed on a block sample of it.
 
 --impl reference times the CPU oracle (single thread) on the same workload.
-Under torchrun every rank runs its own replica (weak scaling, no collective
-on the data path); timing is the max over ranks.
+--gpus N runs one replica per GPU (weak scaling, no collective on the data
+path); under torchrun the ranks come from the environment, otherwise bench.py
+starts its N ranks itself.  Timing is the max over ranks.
 """
 from __future__ import annotations
 
 import argparse
 import json
 import os
+import socket
 import statistics
 import subprocess
 import sys
@@ -80,6 +86,10 @@ def dist_env():
     return int(os.environ.get("RANK", "0")), int(os.environ.get("LOCAL_RANK", "0")), ws
 
 
+def dist_backend() -> str:
+    return os.environ.get("LCT_DIST_BACKEND", "nccl")
+
+
 def max_over_ranks(value: float, device=None) -> float:
     """The largest `value` over all ranks (the job's time is its slowest
     rank's); `value` itself when no process group is running."""
@@ -96,6 +106,47 @@ def replica_units(n_per_rank: int, world: int) -> int:
     """Values the whole job processes per step: every rank runs its own
     replica of the workload (weak scaling, no collective on the data path)."""
     return n_per_rank * world
+
+
+# ----------------------------------------------------------- rank launch
+
+def _free_port() -> int:
+    with socket.socket() as sk:
+        sk.bind(("127.0.0.1", 0))
+        return sk.getsockname()[1]
+
+
+def _rank_entry(rank, world, port, backend, target, targs, q):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank), LOCAL_RANK=str(rank),
+                      WORLD_SIZE=str(world), LCT_DIST_BACKEND=backend)
+    q.put((rank, target(*targs)))
+
+
+def spawn_ranks(world: int, target, targs=(), backend: str = "nccl", timeout: float = 1800.0) -> dict:
+    """Run target(*targs) in `world` fresh processes, one rank each (RANK,
+    LOCAL_RANK, WORLD_SIZE and a 127.0.0.1 rendezvous in the environment, as
+    torchrun would set them); returns {rank: target's return value}.  A rank
+    that fails makes this raise."""
+    import torch.multiprocessing as mp
+    ctx = mp.get_context("spawn")
+    q = ctx.SimpleQueue()
+    port = _free_port()
+    procs = [ctx.Process(target=_rank_entry, args=(r, world, port, backend, target, targs, q)) for r in range(world)]
+    for p in procs:
+        p.start()
+    for p in procs:
+        p.join(timeout=timeout)
+    bad = [r for r, p in enumerate(procs) if p.exitcode != 0]
+    for p in procs:
+        if p.is_alive():
+            p.kill()
+    if bad:
+        raise RuntimeError("ranks %s failed" % bad)
+    out = {}
+    while not q.empty():
+        r, v = q.get()
+        out[r] = v
+    return out
 
 
 # ----------------------------------------------------------------- clocks
@@ -167,13 +218,42 @@ def algorithmic_bytes(sizes, ovf_used: int) -> int:
     return int(sizes.sf_bytes + sizes.slot_bytes + sizes.marker_bytes + sizes.blk_off_bytes + ovf_used)
 
 
+class KernelTimer:
+    """Device time of one call with the L2 flushed (a 256 MiB write) before
+    it: events on the launching stream around the call only."""
+
+    def __init__(self, torch, stream):
+        self.torch = torch
+        self.stream = stream
+        self.flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.int32, device="cuda")
+
+    def __call__(self, fn, reps: int) -> float:
+        torch = self.torch
+        ts = []
+        for _ in range(reps):
+            self.flush.zero_()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(self.stream)
+            fn()
+            e1.record(self.stream)
+            torch.cuda.synchronize()
+            ts.append(e0.elapsed_time(e1))
+        return statistics.mean(ts)
+
+
+def codebooks_for(B, wl):
+    if "zero_frac" in wl:
+        return B.lct_codebook_build_zero_atom(wl["model"], wl["scale"], wl["shape"], wl["zero_frac"])
+    return B.lct_codebook_build(wl["model"], wl["scale"], wl["shape"])
+
+
 def run_gpu(args):
     import torch
     import torch.distributed as dist
 
     rank, local_rank, world = dist_env()
     if world > 1:
-        dist.init_process_group("nccl")
+        dist.init_process_group(dist_backend())
     torch.cuda.set_device(local_rank)
     from lossless_bf16_tensor_gb300 import binding as B
     from lossless_bf16_tensor_gb300 import synth
@@ -188,10 +268,7 @@ def run_gpu(args):
     x_np = synth.generate(args.workload)
     mm, ms = SGD_MOMENTUM[args.workload]
     m_np = synth.laplace(n, ms, seed=2) if mm == "laplace" else synth.momentum(args.workload)
-    if "zero_frac" in wl:
-        cb = B.lct_codebook_build_zero_atom(wl["model"], wl["scale"], wl["shape"], wl["zero_frac"])
-    else:
-        cb = B.lct_codebook_build(wl["model"], wl["scale"], wl["shape"])
+    cb = codebooks_for(B, wl)
     cbm = B.lct_codebook_build(mm, ms)
 
     stream = torch.cuda.current_stream()
@@ -205,20 +282,16 @@ def run_gpu(args):
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.int32, device="cuda")
 
     def step(evs=None, st=stream):
-        # evs: (step start, step end) or (step start, encode end, decode end,
-        # fused SGD end)
-        inner = evs is not None and len(evs) == 4
+        # evs: (step start, decode end, step end)
         if evs:
             evs[0].record(st)
         B.lct_encode(x, cb, X, st)
-        if inner:
-            evs[1].record(st)
         B.lct_decode(X, cb, y, st)
-        if inner:
-            evs[2].record(st)
+        if evs:
+            evs[1].record(st)
         B.lct_sgd_step_fused(X, cb, Mc, cbm, ETA, Wn, st)
         if evs:
-            evs[-1].record(st)
+            evs[2].record(st)
 
     for _ in range(args.warmup):
         flush.zero_()
@@ -235,13 +308,9 @@ def run_gpu(args):
     except AttributeError:
         pass
     clocks = ClockSampler(None if world == 1 and bus is None else bus)
-    # The timed steps carry events at their boundaries only: an event between
-    # two kernels keeps the second from launching while the first finishes
-    # (programmatic dependent launch), which a user's back-to-back calls do
-    # not suffer.  The per-kernel times come from a second pass of as many
-    # steps with an event after every kernel.
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
-    kevs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    # The timed steps carry one event between the decode and the fused SGD
+    # (the encode -> decode hand-over keeps its programmatic early launch).
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
@@ -253,12 +322,14 @@ def run_gpu(args):
     torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
-    total_ms = max_over_ranks(sum(e[0].elapsed_time(e[1]) for e in evs), device="cuda")
-    ms_step = total_ms / args.steps
-    for k in range(args.steps):
-        flush.zero_()
-        step(kevs[k])
-    torch.cuda.synchronize()
+    ed_ms = max_over_ranks(sum(e[0].elapsed_time(e[1]) for e in evs), device="cuda") / args.steps
+    ms_step = max_over_ranks(sum(e[0].elapsed_time(e[2]) for e in evs), device="cuda") / args.steps
+    # Per-kernel device times, the L2 flushed before every kernel.
+    timer = KernelTimer(torch, stream)
+    reps = max(3, args.steps // 2)
+    t_ms = {"encode": timer(lambda: B.lct_encode(x, cb, X, stream), reps),
+            "decode": timer(lambda: B.lct_decode(X, cb, y, stream), reps),
+            "sgd": timer(lambda: B.lct_sgd_step_fused(X, cb, Mc, cbm, ETA, Wn, stream), reps)}
     # The same step captured once in a CUDA graph and replayed (every call
     # only enqueues work, so it captures); reported beside the direct step.
     graph_ms = None
@@ -276,10 +347,6 @@ def run_gpu(args):
         graph_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in gevs)
         assert torch.equal(y, x), "decode(encode(x)) != x after graph replay"
     clk = clocks.stop()
-    enc = [e[0].elapsed_time(e[1]) for e in kevs]
-    dec = [e[1].elapsed_time(e[2]) for e in kevs]
-    sgd = [e[2].elapsed_time(e[3]) for e in kevs]
-    ms_step_kernel_events = statistics.mean(e[0].elapsed_time(e[3]) for e in kevs)
 
     sx, sm_, sw = X.state(), Mc.state(), Wn.state()
     sizes = X.sizes
@@ -287,20 +354,22 @@ def run_gpu(args):
     bytes_m = algorithmic_bytes(sizes, sm_.ovf_used)
     bytes_w = algorithmic_bytes(sizes, sw.ovf_used)
     alg = {"encode": 2 * n + bytes_x, "decode": 2 * n + bytes_x, "sgd": bytes_x + bytes_m + bytes_w}
-    t_ms = {"encode": statistics.mean(enc), "decode": statistics.mean(dec), "sgd": statistics.mean(sgd)}
     peak, peak_kind = hbm_peak()
     frac = {k: alg[k] / (t_ms[k] * 1e-3) / 1e9 / peak for k in alg}
     dom = max(t_ms, key=t_ms.get)
     achieved = alg[dom] / (t_ms[dom] * 1e-3) / 1e9
-    uncompressed_per_step = 10 * n
-    value = 10 * replica_units(n, world) / (ms_step * 1e-3) / 1e9
+    value = 4 * replica_units(n, world) / (ed_ms * 1e-3) / 1e9
 
     traffic = stored_traffic(args.workload, dom)
 
     # ---- end to end through the public API with host buffers
     e2e = None
     if not args.no_e2e:
-        e2e = run_e2e(args, B, x_np, n, level, cb, cbm, Mc, world)
+        e2e = run_e2e(args, B, x_np, n, level, cb, world)
+
+    configs = None
+    if world == 1 and not args.no_configs:
+        configs = run_configs(B, synth, timer, stream, peak)
 
     if rank != 0:
         return None
@@ -321,7 +390,10 @@ def run_gpu(args):
         "dtype": "u32+f32",
         "data": "synthetic",
         "config": {"workload": WORKLOAD_TEXT[args.workload], "name": args.workload, "n": n,
-                   "level": wl["level"], "l2": "flushed before every step (256 MiB write, outside the events)",
+                   "level": wl["level"], "l2": "flushed before every step (256 MiB write, outside the events); "
+                   "per-kernel times flushed before every kernel",
+                   "value": "4N uncompressed bytes (encode 2N + decode 2N) per step / time from step start to "
+                            "decode end; the fused SGD runs in every step after the decode",
                    "parallelism": "replicas" if world > 1 else "single"},
         "roofline": {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 1), "peak": peak,
                      "peak_kind": peak_kind, "unit": "GB/s", "frac": round(achieved / peak, 4),
@@ -331,8 +403,8 @@ def run_gpu(args):
             "decode_gbs_uncompressed": round(2 * n / (t_ms["decode"] * 1e-3) / 1e9, 1),
             "sgd_gelem_per_s": round(n / (t_ms["sgd"] * 1e-3) / 1e9, 3),
             "ms": {k: round(v, 4) for k, v in t_ms.items()},
-            "kernel_times": "second pass of the same number of steps with an event after every kernel "
-                            "(%.4f ms per step with those events)" % ms_step_kernel_events,
+            "ms_encode_decode_in_step": round(ed_ms, 4),
+            "kernel_times": "each kernel alone, L2 flushed before it, mean of %d" % reps,
             "ms_per_step_cuda_graph": None if graph_ms is None else round(graph_ms, 4),
             "hbm_frac_of_%s" % peak_kind: {k: round(v, 4) for k, v in frac.items()},
             "compression_ratio_all_in": round(ratio_all_in, 5),
@@ -340,6 +412,7 @@ def run_gpu(args):
             "overflow_bytes": int(sx.ovf_used),
             "spill_fraction": round(sx.ovf_used / n, 6),
             "allocated_bits_per_exponent": round(8.0 * sizes.slot_bytes / n, 4),
+            "configs": configs,
         },
         "clocks": clk,
         "e2e": e2e,
@@ -349,33 +422,30 @@ def run_gpu(args):
     return line
 
 
-def run_e2e(args, B, x_np, n, level, cb, cbm, Mc, world):
-    """The headline step through the public API with host buffers: every
-    step uploads its input from pinned host memory, encodes, decodes,
-    downloads the decoded values, runs the fused SGD on the new tensor and
-    downloads the new tensor's header (its status).  Steps are pipelined as a
-    user streaming tensors would: uploads, compute and downloads run on three
-    streams with two buffer sets, so step k+1's upload overlaps step k's
-    compute and step k-1's download.  Timed from the first upload to the last
-    download; the working set (two buffer sets, ~115 MB each) exceeds L2."""
+def run_e2e(args, B, x_np, n, level, cb, world):
+    """Encode and decode through the public API with host buffers: every step
+    uploads its input from pinned host memory, encodes, decodes and downloads
+    the decoded values.  Steps are pipelined as a user streaming tensors
+    would: uploads, compute and downloads run on three streams with two buffer
+    sets, so step k+1's upload overlaps step k's compute and step k-1's
+    download.  Timed from the first upload to the last download; the working
+    set (two buffer sets, ~115 MB each at 2^24) exceeds L2."""
     import torch
     dev = torch.device("cuda")
     hx = torch.from_numpy(x_np.view(np.int16)).pin_memory()
     hy = [torch.empty(n, dtype=torch.int16).pin_memory() for _ in range(2)]
-    hh = [torch.empty(64, dtype=torch.uint8).pin_memory() for _ in range(2)]
     xs = [torch.empty(n, dtype=torch.int16, device=dev) for _ in range(2)]
     ys = [torch.empty(n, dtype=torch.int16, device=dev) for _ in range(2)]
     Xs = [B.CompressedTensor(n, level) for _ in range(2)]
-    Ws = [B.CompressedTensor(n, level) for _ in range(2)]
     s_up, s_run, s_down = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
-    ev = {k: [torch.cuda.Event() for _ in range(2)] for k in ("up", "dec", "run", "down")}
+    ev = {k: [torch.cuda.Event() for _ in range(2)] for k in ("up", "run", "down")}
     started = [False, False]
 
     def step(k):
         i = k % 2
         if started[i]:
             s_up.wait_event(ev["run"][i])     # step k-2's encode has read xs[i]
-            s_run.wait_event(ev["down"][i])   # step k-2's downloads have read ys[i] and Ws[i]
+            s_run.wait_event(ev["down"][i])   # step k-2's download has read ys[i]
         started[i] = True
         with torch.cuda.stream(s_up):
             xs[i].copy_(hx, non_blocking=True)
@@ -383,14 +453,10 @@ def run_e2e(args, B, x_np, n, level, cb, cbm, Mc, world):
         s_run.wait_event(ev["up"][i])
         B.lct_encode(xs[i], cb, Xs[i], s_run)
         B.lct_decode(Xs[i], cb, ys[i], s_run)
-        ev["dec"][i].record(s_run)
-        B.lct_sgd_step_fused(Xs[i], cb, Mc, cbm, ETA, Ws[i], s_run)
         ev["run"][i].record(s_run)
-        s_down.wait_event(ev["dec"][i])
+        s_down.wait_event(ev["run"][i])
         with torch.cuda.stream(s_down):
             hy[i].copy_(ys[i], non_blocking=True)
-            s_down.wait_event(ev["run"][i])
-            hh[i].copy_(Ws[i].regions["header"], non_blocking=True)
             ev["down"][i].record(s_down)
 
     torch.cuda.synchronize()
@@ -406,11 +472,129 @@ def run_e2e(args, B, x_np, n, level, cb, cbm, Mc, world):
     torch.cuda.synchronize()
     for i in range(2):
         assert torch.equal(hy[i], hx), "decoded values differ from the input"
-        assert int(hh[i][24:28].view(torch.int32).item()) == 0, "a status was latched"
+        assert Xs[i].state().status == 0, "a status was latched"
     e_ms = max_over_ranks(t0.elapsed_time(t1) / args.steps, device="cuda")
-    return {"value": round(10 * replica_units(n, world) / (e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
-            "ms_per_step": round(e_ms, 4), "h2d_bytes_per_step": 2 * n, "d2h_bytes_per_step": 2 * n + 64,
-            "pipelined": "upload / compute / download on three streams, two buffer sets"}
+    return {"value": round(4 * replica_units(n, world) / (e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+            "ms_per_step": round(e_ms, 4), "h2d_bytes_per_step": 2 * n, "d2h_bytes_per_step": 2 * n,
+            "pipelined": "upload / encode + decode / download on three streams, two buffer sets"}
+
+
+# ------------------------------------------------- the five configurations
+
+def oracle_codec_sample(x, cb_args, level, nblocks):
+    """The oracle's encode and decode of the first `nblocks` blocks of x on
+    one host core: (values, encode seconds, decode seconds)."""
+    import oracle
+    block, _ = oracle.geometry(level)
+    k = min(x.size, nblocks * block)
+    xs = np.ascontiguousarray(x[:k])
+    model, scale, shape, zf = cb_args
+    cb = oracle.codebook_build_zero_atom(model, scale, shape, zf) if zf else oracle.codebook_build(model, scale, shape)
+    t0 = time.perf_counter()
+    c = oracle.encode(xs, cb, level)
+    t1 = time.perf_counter()
+    rc, y = oracle.decode(c, cb)
+    t2 = time.perf_counter()
+    assert rc == 0 and np.array_equal(y, xs)
+    return k, t1 - t0, t2 - t1
+
+
+def run_configs(B, synth, timer, stream, peak):
+    """encode / decode GB/s, fused-SGD rate, HBM fractions and ratios for the
+    five workload configurations, each beside the oracle on a block sample."""
+    import torch
+    reps = 5
+    model_id = {"gaussian": 0, "laplace": 1, "powerlaw": 2}
+    out = {}
+
+    def codec_record(name, x_np, wl, n, level, rounds=None, sample_blocks=8):
+        cb = codebooks_for(B, wl)
+        x = torch.from_numpy(x_np.view(np.int16)).cuda()
+        X = B.CompressedTensor(n, level)
+        y = torch.empty_like(x)
+        xs = [x] if rounds is None else [
+            (x.view(torch.bfloat16).float() * (2.0 ** k)).to(torch.bfloat16).view(torch.int16) for k in rounds]
+        te, td, ratios = [], [], []
+        for xr in xs:
+            B.lct_encode(xr, cb, X, stream)
+            B.lct_decode(X, cb, y, stream)
+            torch.cuda.synchronize()
+            assert torch.equal(y, xr), name + ": decode(encode(x)) != x"
+            st = X.state()
+            assert st.status == 0, name
+            te.append(timer(lambda: B.lct_encode(xr, cb, X, stream), reps))
+            td.append(timer(lambda: B.lct_decode(X, cb, y, stream), reps))
+            ratios.append((2.0 * n / (X.sizes.fixed_bytes + st.ovf_used),
+                           2.0 * n / (X.sizes.sf_bytes + X.sizes.slot_bytes + st.ovf_used), st.ovf_used))
+        sizes = X.sizes
+        ovf = statistics.mean(r[2] for r in ratios)
+        alg = 2 * n + algorithmic_bytes(sizes, int(ovf))
+        t_e, t_d = statistics.mean(te), statistics.mean(td)
+        ocb = (model_id[wl["model"]], wl["scale"], wl["shape"], wl.get("zero_frac", 0.0))
+        on, oe, od = oracle_codec_sample(x_np, ocb, level, sample_blocks)
+        rec = {"n": n, "level": wl["level"], "encode_gbs_uncompressed": round(2 * n / (t_e * 1e-3) / 1e9, 1),
+               "decode_gbs_uncompressed": round(2 * n / (t_d * 1e-3) / 1e9, 1), "ms": {"encode": round(t_e, 4),
+               "decode": round(t_d, 4)}, "hbm_frac": {"encode": round(alg / (t_e * 1e-3) / 1e9 / peak, 4),
+               "decode": round(alg / (t_d * 1e-3) / 1e9 / peak, 4)},
+               "compression_ratio_all_in": round(statistics.mean(r[0] for r in ratios), 5),
+               "compression_ratio_payload": round(statistics.mean(r[1] for r in ratios), 5),
+               "spill_fraction": round(ovf / n, 6),
+               "oracle": {"values": on, "encode_s": round(oe, 4), "decode_s": round(od, 4),
+                          "encode_gbs": round(2 * on / oe / 1e9, 5), "decode_gbs": round(2 * on / od / 1e9, 5),
+                          "cores": 1, "host_cpus": os.cpu_count() or 0,
+                          "sample": "first %d block(s), oracle single-threaded" % -(-on // sizes.block)}}
+        if rounds is not None:
+            rec["rounds"] = "x * 2^k for k = %d..%d, shift re-estimated by every encode" % (rounds[0], rounds[-1])
+            rec["per_round_gbs"] = {"encode": [round(2 * n / (t * 1e-3) / 1e9, 1) for t in te],
+                                    "decode": [round(2 * n / (t * 1e-3) / 1e9, 1) for t in td]}
+        del X, x, y, xs
+        torch.cuda.empty_cache()
+        return rec
+
+    for name in ("gauss_block", "laplace_16m", "heavy_64m", "sgd_162m", "gelu_act"):
+        wl = synth.WORKLOADS[name]
+        n, level = wl["n"], B.LEVELS[wl["level"]]
+        x_np = synth.generate(name)
+        rec = codec_record(name, x_np, wl, n, level, rounds=wl.get("pow2"), sample_blocks=8)
+        if name == "sgd_162m":
+            rec["sgd"] = run_sgd_config(B, synth, timer, stream, peak, x_np, wl, n, level)
+        rec["workload"] = WORKLOAD_TEXT[name]
+        out[name] = rec
+        del x_np
+    return out
+
+
+def run_sgd_config(B, synth, timer, stream, peak, w_np, wl, n, level):
+    """Fused SGD steps W <- W - eta*M on compressed W and M (out of place,
+    two W tensors used in turn), the codebook and shift fixed."""
+    import torch
+    cbw = B.lct_codebook_build(wl["model"], wl["scale"], wl["shape"])
+    cbm = B.lct_codebook_build(wl["momentum"]["model"], wl["momentum"]["scale"])
+    Ws = [B.CompressedTensor(n, level), B.CompressedTensor(n, level)]
+    M = B.CompressedTensor(n, level)
+    B.lct_encode(torch.from_numpy(w_np.view(np.int16)).cuda(), cbw, Ws[0], stream)
+    B.lct_encode(torch.from_numpy(synth.momentum("sgd_162m").view(np.int16)).cuda(), cbm, M, stream)
+    eta = float(np.float32(wl["eta"]))
+    steps = 10
+    k = [0]
+
+    def one():
+        B.lct_sgd_step_fused(Ws[k[0] % 2], cbw, M, cbm, eta, Ws[(k[0] + 1) % 2], stream)
+        k[0] += 1
+    t = timer(one, steps)
+    torch.cuda.synchronize()
+    cur = Ws[k[0] % 2]
+    st, sm_ = cur.state(), M.state()
+    assert st.status == 0
+    sizes = cur.sizes
+    alg = 2 * algorithmic_bytes(sizes, st.ovf_used) + algorithmic_bytes(sizes, sm_.ovf_used)
+    res = {"steps": steps, "ms_per_step": round(t, 4), "gelem_per_s": round(n / (t * 1e-3) / 1e9, 3),
+           "hbm_frac": round(alg / (t * 1e-3) / 1e9 / peak, 4),
+           "compression_ratio_all_in_after": round(2.0 * n / (sizes.fixed_bytes + st.ovf_used), 5),
+           "eta": eta, "l2": "flushed before every step"}
+    del Ws, M
+    torch.cuda.empty_cache()
+    return res
 
 
 def run_gpu_momentum(args, rank, local_rank, world):
@@ -692,12 +876,12 @@ def oracle_step_inputs(workload: str, nblocks_sample: int | None):
 
 
 def oracle_step(x, cb, M, cbm, level) -> float:
-    """One timed oracle step (encode, decode, fused SGD); returns seconds."""
+    """One timed oracle encode + decode (the metric's two passes); returns
+    seconds.  M and cbm are unused (kept so the inputs match the GPU step)."""
     import oracle
     t0 = time.perf_counter()
     X = oracle.encode(x, cb, level)
     rc, y = oracle.decode(X, cb)
-    oracle.sgd_step(X, cb, M, cbm, ETA)
     dt = time.perf_counter() - t0
     assert rc == 0 and np.array_equal(y, x)
     return dt
@@ -718,17 +902,16 @@ CPU_BASELINE_SECONDS = 10.0
 
 
 def cpu_baseline(workload: str, nblocks_sample: int | None):
-    """The oracle on one host core, stepped over the same inputs until at least
-    CPU_BASELINE_SECONDS of oracle work are timed (one step of the whole 2^24
-    workload takes about a second)."""
+    """The oracle on one host core, stepped (encode + decode) over the same
+    inputs until at least CPU_BASELINE_SECONDS of oracle work are timed."""
     inputs = oracle_step_inputs(workload, nblocks_sample)
     nvals = inputs[0].size
     total, steps = 0.0, 0
     while total < CPU_BASELINE_SECONDS:
         total += oracle_step(*inputs)
         steps += 1
-    return {"value": round(10 * nvals * steps / total / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
-            "sample": "%d steps (encode + decode + fused SGD) over %d values of the %s workload (%s); "
+    return {"value": round(4 * nvals * steps / total / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": "%d steps (encode + decode) over %d values of the %s workload (%s); "
                       "host %s, %d logical CPUs, oracle single-threaded" % (
                           steps, nvals, workload, "first %d blocks" % nblocks_sample if nblocks_sample else "all",
                           cpu_model(), os.cpu_count() or 0),
@@ -751,7 +934,7 @@ def run_reference(args):
         oracle_step(*inputs)
     times = [oracle_step(*inputs) for _ in range(args.steps)]
     s = sum(times) / len(times)
-    value = 10 * nvals / s / 1e9
+    value = 4 * nvals / s / 1e9
     sample = "%d values of %s per step (%s)" % (nvals, args.workload,
                                                "first %d blocks" % args.cpu_blocks if args.cpu_blocks else "all")
     return {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
@@ -813,6 +996,7 @@ def main():
     ap.add_argument("--cpu-blocks", type=int, default=0, help="oracle sample: first N blocks (0 = whole workload)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-configs", action="store_true", help="skip the five-configuration breakdown")
     args = ap.parse_args()
     if args.impl == "reference":
         # each oracle step is a bounded sample of the workload (32 blocks
@@ -820,9 +1004,10 @@ def main():
         if not args.cpu_blocks:
             args.cpu_blocks = 32
         line = run_reference(args)
+    elif args.gpus > 1 and int(os.environ.get("WORLD_SIZE", "1")) == 1:
+        # not under torchrun: start one process per GPU here
+        line = spawn_ranks(args.gpus, run_gpu, (args,)).get(0)
     else:
-        if args.gpus > 1 and int(os.environ.get("WORLD_SIZE", "1")) == 1:
-            raise SystemExit("--gpus > 1 runs under torchrun (one process per GPU)")
         line = run_gpu(args)
     if line is not None:
         print(json.dumps(line), flush=True)

@@ -60,6 +60,32 @@ def test_two_rank_timing_and_reference_arm():
     assert [g[3] for g in got] == [True, False]       # only rank 0 runs the reference arm
 
 
+def _spawned_rank():
+    """What bench.py's self-started ranks see: the torchrun environment on a
+    127.0.0.1 rendezvous, and a working process group across the ranks."""
+    sys.path.insert(0, ROOT)
+    import bench
+    rank, local_rank, world = bench.dist_env()
+    dist.init_process_group(bench.dist_backend(), rank=rank, world_size=world)
+    try:
+        return (rank, local_rank, world, bench.max_over_ranks(5.0 + rank), bench.replica_units(100, world),
+                os.environ["MASTER_ADDR"])
+    finally:
+        dist.destroy_process_group()
+
+
+def test_bench_starts_its_own_ranks_without_torchrun():
+    """`bench.py --gpus N` outside torchrun starts N ranks itself (gloo on
+    CPU here, NCCL on GPUs): each rank gets RANK = LOCAL_RANK, WORLD_SIZE = N,
+    the job's time is the slowest rank's and its value counts every replica."""
+    sys.path.insert(0, ROOT)
+    import bench
+    out = bench.spawn_ranks(2, _spawned_rank, (), backend="gloo", timeout=300)
+    assert sorted(out) == [0, 1]
+    for r, v in out.items():
+        assert v == (r, r, 2, 6.0, 200, "127.0.0.1")
+
+
 def test_single_process_defaults():
     sys.path.insert(0, ROOT)
     import bench

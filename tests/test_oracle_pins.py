@@ -219,6 +219,135 @@ def test_codebook_from_flat_weights(orc):
     assert cb.k == 4 and set(np.nonzero(cb.lengths())[0]) == {10, 11, 12, 13}
 
 
+# ------------------------------------------------- escape-set choice
+
+def _exact_capped_cost(weights, L=8):
+    """Least sum(w * len) over prefix codes with every length <= L, by
+    exhaustive search over how many leaves take each length 1..L (the
+    heaviest leaves take the shortest lengths, which is optimal by
+    rearrangement); no Huffman or package-merge step is used."""
+    ws = sorted(weights, reverse=True)
+    m = len(ws)
+    pre = [0]
+    for w in ws:
+        pre.append(pre[-1] + w)
+    best = [None]
+
+    def rec(length, start, room, cost):  # room: Kraft budget in units of 2^-L
+        if start == m:
+            if best[0] is None or cost < best[0]:
+                best[0] = cost
+            return
+        if length > L or (best[0] is not None and cost + length * (pre[m] - pre[start]) >= best[0]):
+            return
+        unit = 1 << (L - length)
+        for c in range(min(m - start, room // unit), -1, -1):
+            rec(length + 1, start + c, room - c * unit, cost + length * (pre[start + c] - pre[start]))
+
+    rec(1, 0, 1 << L, 0)
+    return best[0]
+
+
+def _escape_cost(coded_weights, escaped_weights, L=8):
+    """The code over the coded symbols plus one escape leaf whose weight is
+    the escaped symbols' total (at least 1); every escape also pays the
+    8-bit raw exponent ([EXP] 'In bits')."""
+    w_esc = max(1, sum(escaped_weights))
+    return _exact_capped_cost(list(coded_weights) + [w_esc], L) + 8 * w_esc
+
+
+def _oracle_cost(cb, w):
+    lens = cb.lengths()
+    coded = lens > 0
+    w_esc = max(1, int(w[~coded].sum()))
+    return int((w[coded].astype(object) * lens[coded].astype(object)).sum()) + w_esc * (int(cb.esc_len) + 8)
+
+
+def _skewed_weights(rng, nsym):
+    """nsym nonzero exponents with a fast-decaying tail, so that the 8-bit
+    cap binds and escaping the rarest exponents can pay."""
+    w = np.zeros(256, np.uint64)
+    exps = rng.choice(np.arange(1, 255), size=nsym, replace=False)
+    ratio = rng.uniform(1.6, 3.5)
+    vals = [max(1, int(rng.integers(1, 1 << 20) * ratio ** -i * (1 << 20))) for i in range(nsym)]
+    rng.shuffle(vals)
+    w[exps] = vals
+    return w
+
+
+def test_escape_set_is_optimal_over_every_subset(orc):
+    """[EXP] 'In bits': rare exponents share one escape prefix.  Over every
+    subset of 9-11 exponents that could be escaped and every length vector,
+    no codebook is cheaper than the oracle's, and the oracle's cost is
+    reached: this pins the escape weight, its 8-bit literal and the choice
+    of how many exponents get codes."""
+    rng = np.random.default_rng(31)
+    escaped_somewhere = 0
+    for trial in range(12):
+        nsym = int(rng.integers(9, 12))
+        w = _skewed_weights(rng, nsym)
+        cb = orc.codebook_from_weights(w)
+        nz = [int(v) for v in w[w > 0]]
+        best = None
+        for r in range(1, nsym + 1):
+            for coded in itertools.combinations(range(nsym), r):
+                rest = [nz[i] for i in range(nsym) if i not in coded]
+                c = _escape_cost([nz[i] for i in coded], rest)
+                best = c if best is None else min(best, c)
+        assert _oracle_cost(cb, w) == best, (trial, nz)
+        escaped_somewhere += int(cb.k < nsym)
+    assert escaped_somewhere >= 3  # the cases do exercise the escape
+
+
+def test_escape_set_is_the_smallest_optimal_prefix_of_the_ranking(orc):
+    """The coded exponents are the k heaviest (weight descending, exponent
+    ascending), and k is the smallest count reaching the least cost (the
+    reading on ties), over alphabets of up to 16 exponents."""
+    rng = np.random.default_rng(32)
+    for trial in range(20):
+        nsym = int(rng.integers(9, 17))
+        w = _skewed_weights(rng, nsym)
+        if trial % 4 == 0:  # equal weights in the tail: ties between prefixes
+            tail = np.argsort(w)[-nsym:][: nsym // 2]
+            w[tail] = w[tail].min()
+        cb = orc.codebook_from_weights(w)
+        order = sorted(np.nonzero(w)[0], key=lambda e: (-int(w[e]), int(e)))
+        costs = [_escape_cost([int(w[e]) for e in order[:k]], [int(w[e]) for e in order[k:]])
+                 for k in range(1, nsym + 1)]
+        k_best = 1 + costs.index(min(costs))
+        assert cb.k == k_best, (trial, costs)
+        assert set(np.nonzero(cb.lengths())[0]) == set(order[:k_best])
+        assert _oracle_cost(cb, w) == min(costs)
+
+
+# Exponent weights for which coding k or k+1 (or k+2) exponents costs exactly
+# the same (found by a search over power-of-two-like weights; the tied counts
+# are recomputed by the reference below, not taken from the oracle).
+TIED_WEIGHTS = [
+    [131072, 65536, 8192, 4096, 512, 256, 32, 8, 4, 1],
+    [16777216, 4194304, 524288, 131072, 32768, 8192, 2048, 512, 256, 64, 8, 2, 1],
+    [1024, 1024, 512, 128, 128, 32, 16, 16, 8, 2, 1, 1],
+    [2048, 2048, 1024, 512, 128, 64, 32, 32, 16, 4, 4, 2, 1],
+    [1024, 512, 512, 256, 128, 32, 16, 16, 8, 4, 2, 1],
+]
+
+
+@pytest.mark.parametrize("vals", TIED_WEIGHTS)
+def test_escape_set_ties_go_to_the_fewest_codes(orc, vals):
+    """When several counts of coded exponents reach the least cost, the
+    oracle codes the fewest of them (the reading on ties)."""
+    w = np.zeros(256, np.uint64)
+    exps = np.arange(40, 40 + len(vals))
+    w[exps] = vals
+    order = sorted(np.nonzero(w)[0], key=lambda e: (-int(w[e]), int(e)))
+    costs = [_escape_cost([int(w[e]) for e in order[:k]], [int(w[e]) for e in order[k:]])
+             for k in range(1, len(vals) + 1)]
+    tied = [k + 1 for k, c in enumerate(costs) if c == min(costs)]
+    assert len(tied) >= 2
+    cb = orc.codebook_from_weights(w)
+    assert cb.k == tied[0] and _oracle_cost(cb, w) == min(costs)
+
+
 # ---------------------------------------------------------------- shift
 
 def _with_exponents(exps, sf=0):

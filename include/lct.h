@@ -235,9 +235,10 @@ lct_status lct_encode(const uint16_t *d_x, const lct_codebook *cb, const lct_ten
  *   - Tensors needing more than LCT_STATIC_SCRATCH_BLOCKS blocks (n above
  *     2^30 values in CLEAN, 2^29 in MEDIUM and HIGH) are rejected with
  *     LCT_ERR_UNSUPPORTED before anything is enqueued.
- *   - The first call on a device looks up the array's device address (with
- *     that device current) and keeps it; make that first call before any
- *     stream capture.
+ *   - Every call looks up the array's device address on the current device
+ *     (nothing is cached, so the address stays right after cudaDeviceReset).
+ *     The first call on a device may load the library's device code there;
+ *     make that first call before any stream capture.
  *   - All calls share the one array.  Each call clears the words it uses
  *     before using them, but calls whose GPU work overlaps -- on different
  *     streams, or from different threads -- race on the array and may produce

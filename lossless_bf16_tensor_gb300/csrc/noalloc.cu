@@ -11,7 +11,6 @@
 // in the library's own device image instead; the caller still passes the
 // input and the compressed tensor's regions, exactly as for lct_encode.
 #include <cstdint>
-#include <mutex>
 
 #include "../../include/lct.h"
 #include "internal.h"
@@ -21,24 +20,16 @@ namespace {
 // Every GPU that loads this library holds this array until the process exits.
 static __device__ __align__(256) unsigned long long g_static_scan_words[LCT_STATIC_SCRATCH_BLOCKS];
 
-constexpr int kMaxDevices = 128;
-std::mutex g_setup_mutex;
-void *g_scan_words_ptr[kMaxDevices] = {};
-
-// Device address of the array on the current device (looked up once per
-// device).  In host code the array's name is only a host-side stand-in, so a
-// kernel must be given this address, never the name itself.
+// Device address of the array on the current device, looked up on every
+// call: in host code the array's name is only a host-side stand-in, so a
+// kernel must be given this address, never the name itself.  Not caching it
+// keeps it right after cudaDeviceReset or a new primary context.  The first
+// lookup on a device may load the library's device code there.
 lct_status scan_words_on_current_device(void **out)
 {
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return LCT_ERR_CUDA;
-    std::lock_guard<std::mutex> lock(g_setup_mutex);
-    if (!g_scan_words_ptr[dev]) {
-        void *p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_static_scan_words) != cudaSuccess || !p) return LCT_ERR_CUDA;
-        g_scan_words_ptr[dev] = p;
-    }
-    *out = g_scan_words_ptr[dev];
+    void *p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_static_scan_words) != cudaSuccess || !p) return LCT_ERR_CUDA;
+    *out = p;
     return LCT_OK;
 }
 

@@ -29,7 +29,8 @@
 namespace lct {
 namespace dev {
 
-constexpr int kMomThreads = 256;
+constexpr int kMomThreads = 256;               // consumer threads: one per stream
+constexpr int kMomBlock = kMomThreads + 32;    // and one producer warp
 constexpr int kMomRows = 16;    // rows per chunk
 constexpr int kMomRing = 2;     // chunks in flight
 constexpr int kMomSpill = 32;   // spilled new-exponent rows kept per output (out of place)
@@ -63,6 +64,38 @@ struct TwoStateOp<OP2_ADAM_MOMENTS> {
     }
 };
 
+// The same updates for two values at once (xa, xb: the two states as BF16 in
+// bits 0..15, g: gradients), each result rounded to BF16 and packed
+// value 0 | value 1 << 16 (pa: new first state, pb: new second state).
+template <int OP>
+struct TwoStateOp2;
+
+template <>
+struct TwoStateOp2<OP2_MOMENTUM> {
+    __device__ static __forceinline__ void apply(const uint32_t (&w)[2], const uint32_t (&m)[2],
+                                                 const uint32_t (&g)[2], const float *k, uint32_t &pa, uint32_t &pb)
+    {
+        pb = bf16x2_rne(__fadd_rn(__fmul_rn(k[1], bf16_f(m[0])), bf16_f(g[0])),
+                        __fadd_rn(__fmul_rn(k[1], bf16_f(m[1])), bf16_f(g[1])));
+        // the weight step takes the new momentum as stored (BF16)
+        const float m0 = __uint_as_float(pb << 16), m1 = __uint_as_float(pb & 0xFFFF0000u);
+        pa = bf16x2_rne(__fsub_rn(bf16_f(w[0]), __fmul_rn(k[0], m0)), __fsub_rn(bf16_f(w[1]), __fmul_rn(k[0], m1)));
+    }
+};
+
+template <>
+struct TwoStateOp2<OP2_ADAM_MOMENTS> {
+    __device__ static __forceinline__ void apply(const uint32_t (&m)[2], const uint32_t (&v)[2],
+                                                 const uint32_t (&g)[2], const float *k, uint32_t &pa, uint32_t &pb)
+    {
+        const float g0 = bf16_f(g[0]), g1 = bf16_f(g[1]);
+        pb = bf16x2_rne(__fadd_rn(__fmul_rn(k[2], bf16_f(v[0])), __fmul_rn(k[3], __fmul_rn(g0, g0))),
+                        __fadd_rn(__fmul_rn(k[2], bf16_f(v[1])), __fmul_rn(k[3], __fmul_rn(g1, g1))));
+        pa = bf16x2_rne(__fadd_rn(__fmul_rn(k[0], bf16_f(m[0])), __fmul_rn(k[1], g0)),
+                        __fadd_rn(__fmul_rn(k[0], bf16_f(m[1])), __fmul_rn(k[1], g1)));
+    }
+};
+
 template <int LEVEL, bool INPLACE>
 struct MomSmem {
     static constexpr int W = Geo<LEVEL>::W, NJ = Geo<LEVEL>::NJ;
@@ -74,6 +107,8 @@ struct MomSmem {
     static constexpr int kSpill = (kSpillRows * kRow + 127) / 128 * 128;  // per output
     static constexpr int kBytes = 2 * kSlotIn + kRing + kLuts + 2 * kSpill;
     static_assert(kBytes <= 227 * 1024, "shared memory of one CTA");
+    static_assert(kSlotIn + 33 * 1024 <= kBytes, "the pair reader's reads stay inside the CTA");
+    static_assert(kMomRows % 4 == 0, "four-row groups");
 };
 
 // Prologue: both output headers (shift and codebook carried over from the
@@ -163,8 +198,108 @@ __device__ __forceinline__ void mom_put_chunk(Writer &wo, const uint32_t (&h)[R]
     }
 }
 
+// Appends four new exponents of one output (packed two BF16 values per
+// word in p[0], p[1]) to its stream: without per-code checks when every
+// stream of the warp has room for all four, else one checked append per code
+// (a spilled exponent goes to the staging ring).
+template <int SP>
+__device__ __forceinline__ void mom_put4(Writer &wo, const uint32_t (&p)[2], const uint2 *__restrict__ tbl,
+                                         uint32_t k0, uint32_t *__restrict__ col, uint8_t *__restrict__ stage)
+{
+    const uint32_t h[4] = {p[0], p[0] >> 16, p[1], p[1] >> 16};
+    uint2 ent[4];
+    uint32_t need = 0;
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+        ent[t] = code_of(tbl, h[t]);
+        need += ent[t].y;
+    }
+    if (__all_sync(kFull, wo.alive && need <= wo.rem)) {
+        wr_add2(wo, ent[0], ent[1]);
+        wr_flush(wo, col);
+        wr_add2(wo, ent[2], ent[3]);
+        wr_flush(wo, col);
+        wo.rem -= need;
+    } else {
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+            const uint32_t k = k0 + t;
+            if (wr_put_checked(wo, ent[t], k, col)) stage[(k % SP) * kRow] = (uint8_t)exp_of(h[t]);
+        }
+    }
+}
+
+// Four rows of every stream on the fast path (every symbol of both inputs in
+// its slot): both inputs decoded two symbols at a time with the escape
+// literals deferred, both new states rounded two values at a time, their
+// sign-fraction bytes written and their codes appended.  The first state's
+// new codes are its old ones bit for bit when no new exponent of the warp's
+// streams differs (same codebook, same stored shift): then its rows' bits
+// are appended straight from the old stream window.
+template <int OP, int SP>
+__device__ __forceinline__ void mom_group(MomIn &sw, MomIn &sm, const uint32_t colw_s, const uint32_t colm_s,
+                                          const uint32_t lutw_s, const uint32_t lutm_s, const Mul mul,
+                                          const uint8_t *sfwc, const uint8_t *sfmc, const uint16_t *gc, const float *kc,
+                                          Writer &ow, Writer &om, const uint2 *tblW, const uint2 *tblM,
+                                          uint32_t *colW, uint32_t *colM, uint8_t *sfWo, uint8_t *sfMo,
+                                          uint8_t *stageW, uint8_t *stageM, uint32_t k0)
+{
+    using Op2 = TwoStateOp2<OP>;
+    uint32_t fw[4], fm[4], gv[4];
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+        fw[t] = sfwc[t * kStreams];
+        fm[t] = sfmc[t * kStreams];
+        gv[t] = gc[t * kStreams];
+    }
+    uint32_t wvw[4], evw[4], wvm[4], evm[4], esc = 0;
+    const uint32_t p0 = sw.pos;
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+        Rd rw{sw.pos, colw_s}, rm{sm.pos, colm_s};
+        rd_pair(rw, lutw_s, mul, wvw[2 * q], wvw[2 * q + 1], evw[2 * q], evw[2 * q + 1]);
+        rd_pair(rm, lutm_s, mul, wvm[2 * q], wvm[2 * q + 1], evm[2 * q], evm[2 * q + 1]);
+        sw.pos = rw.p;
+        sm.pos = rm.p;
+        esc |= evw[2 * q] | evw[2 * q + 1] | evm[2 * q] | evm[2 * q + 1];
+    }
+    if (__any_sync(kFull, esc_bits(esc))) {
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+            evw[t] = lit_fix(wvw[t], evw[t]);
+            evm[t] = lit_fix(wvm[t], evm[t]);
+        }
+    }
+    const uint32_t bc = sw.pos - p0;  // the first state's old bits of these rows
+    uint32_t pa[2], pb[2], same = 0;
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+        const uint32_t xa[2] = {join_one(fw[2 * q], evw[2 * q]), join_one(fw[2 * q + 1], evw[2 * q + 1])};
+        const uint32_t xb[2] = {join_one(fm[2 * q], evm[2 * q]), join_one(fm[2 * q + 1], evm[2 * q + 1])};
+        const uint32_t g2[2] = {gv[2 * q], gv[2 * q + 1]};
+        Op2::apply(xa, xb, g2, kc, pa[q], pb[q]);
+        if (OP == OP2_MOMENTUM) same |= pa[q] ^ __byte_perm(xa[0], xa[1], 0x5410);
+        const uint32_t sa = sf_of2(pa[q]), sb = sf_of2(pb[q]);
+        sfWo[(2 * q) * kStreams] = (uint8_t)sa;
+        sfWo[(2 * q + 1) * kStreams] = (uint8_t)(sa >> 16);
+        sfMo[(2 * q) * kStreams] = (uint8_t)sb;
+        sfMo[(2 * q + 1) * kStreams] = (uint8_t)(sb >> 16);
+    }
+    // A weight moves by a small step, so its exponents mostly stay; AdamW's
+    // first moment is re-weighted every step and nearly always changes.
+    constexpr bool kTryCopy = OP == OP2_MOMENTUM;
+    if (kTryCopy && __all_sync(kFull, ow.alive && !(same & 0x7F807F80u) && bc <= 32u && bc <= ow.rem)) {
+        wr_add(ow, make_uint2(wvw[0] & ~(0xFFFFFFFFu >> bc), bc));
+        wr_flush(ow, colW);
+        ow.rem -= bc;
+    } else {
+        mom_put4<SP>(ow, pa, tblW, k0, colW, stageW);
+    }
+    mom_put4<SP>(om, pb, tblM, k0, colM, stageM);
+}
+
 template <int LEVEL, bool INPLACE, int OP>
-__global__ void __launch_bounds__(kMomThreads, INPLACE ? 1 : 2) k_momentum(const __grid_constant__ MomentumArgs a)
+__global__ void __launch_bounds__(kMomBlock, INPLACE ? 1 : 2) k_momentum(const __grid_constant__ MomentumArgs a)
 {
     using Op = TwoStateOp<OP>;
     using G = Geo<LEVEL>;
@@ -182,7 +317,9 @@ __global__ void __launch_bounds__(kMomThreads, INPLACE ? 1 : 2) k_momentum(const
     uint2 *tblM = tblW + 256;
     uint8_t *stageW = reinterpret_cast<uint8_t *>(tblM + 256);
     uint8_t *stageM = stageW + L::kSpill;
-    __shared__ __align__(8) uint64_t bar_slot, bar_in[S];
+    // bar_in[s]: stage s of the ring has landed; bar_free[s]: every consumer
+    // warp is done with stage s (the producer may refill it)
+    __shared__ __align__(8) uint64_t bar_slot, bar_in[S], bar_free[S];
     __shared__ uint32_t warp_tot[NW];
     __shared__ unsigned long long s_excl[2];
     __shared__ uint32_t s_flags;  // bit 0: a wait gave up, bit 1: corrupt input
@@ -194,14 +331,53 @@ __global__ void __launch_bounds__(kMomThreads, INPLACE ? 1 : 2) k_momentum(const
     const uint32_t nrows = (nb + 255) >> 8, nbulk = (nb >> 8) / R, nchunks = (nrows + R - 1) / R;
     const uint64_t limit = a.wait_ns;
 
-    if (j == 0) {
-        mbar_init(&bar_slot, 1);
-        for (int s = 0; s < S; ++s) mbar_init(&bar_in[s], 1);
-        fence_mbar_init();
-        s_flags = 0;
+    auto issue = [&](uint32_t c) {
+        uint8_t *dst = ring + (c % S) * L::kChunk;
+        const uint64_t at = base + (uint64_t)c * kRowsB;
+        mbar_expect_tx(&bar_in[c % S], L::kChunk);
+        bulk_load(dst, a.w_in.sf + at, kRowsB, &bar_in[c % S]);
+        bulk_load(dst + kRowsB, a.m_in.sf + at, kRowsB, &bar_in[c % S]);
+        bulk_load(dst + 2 * kRowsB, a.g + at, 2 * kRowsB, &bar_in[c % S]);
+    };
+    if (warp == NW) {
+        // Producer warp: initialise the barriers, issue the slot images and
+        // the first stages of the ring at once, then refill each stage as soon
+        // as all consumer warps have released it.
+        if (lane == 0) {
+            mbar_init(&bar_slot, 1);
+            for (int s = 0; s < S; ++s) {
+                mbar_init(&bar_in[s], 1);
+                mbar_init(&bar_free[s], NW);
+            }
+            fence_mbar_init();
+            s_flags = 0;
+        }
+        pdl_wait();  // the inputs are complete
+        if (lane == 0) {
+            mbar_expect_tx(&bar_slot, 2 * W * kStreams * 4);
+            bulk_load(slotW, a.w_in.slots + (uint64_t)b * W * kStreams, W * kStreams * 4, &bar_slot);
+            bulk_load(slotM, a.m_in.slots + (uint64_t)b * W * kStreams, W * kStreams * 4, &bar_slot);
+            for (uint32_t c = 0; c < (uint32_t)S && c < nbulk; ++c) issue(c);
+        }
+        __syncthreads();  // barriers initialised, tables built
+        if (lane == 0) {
+            bool gave_up = false;
+            for (uint32_t c = S; c < nbulk; ++c) {
+                if (!mbar_wait(&bar_free[c % S], (c / S - 1) & 1u, gave_up ? 1000000ull : limit)) gave_up = true;
+                issue(c);
+            }
+            if (gave_up) atomicOr(&s_flags, 1u);
+        }
+        return;
     }
-    // inputs, the new headers and the cleared look-back words are all ready
-    pdl_wait();
+
+    // Consumer warps, thread j = stream j.  Every global read of the block's
+    // start is issued before the first barrier so that their latencies overlap.
+    pdl_wait();  // inputs, the new headers and the cleared look-back words are all ready
+    const uint32_t nj = nb > (uint32_t)j ? (nb - j + 255) / 256 : 0;
+    const uint32_t mw = a.w_in.markers[(uint64_t)b * kStreams + j], mm = a.m_in.markers[(uint64_t)b * kStreams + j];
+    const uint64_t a0 = a.w_in.blk_off[b], a1 = a.w_in.blk_off[b + 1];
+    const uint64_t c0 = a.m_in.blk_off[b], c1 = a.m_in.blk_off[b + 1];
     const lct_header *hw = a.w_in.hdr, *hm = a.m_in.hdr;
     bool bad = !(hw->magic == LCT_MAGIC && hw->n == a.w_in.n && hw->level == LEVEL && hw->cb_hash == a.cbw.hash) ||
                !(hm->magic == LCT_MAGIC && hm->n == a.m_in.n && hm->level == LEVEL && hm->cb_hash == a.cbm.hash);
@@ -212,46 +388,29 @@ __global__ void __launch_bounds__(kMomThreads, INPLACE ? 1 : 2) k_momentum(const
     tblM[j] = enc_entry(a.cbm, delta_m, j);
     slotW[W * kStreams + j] = 0u;
     slotM[W * kStreams + j] = 0u;
-    __syncthreads();  // barriers initialised
-    auto issue = [&](uint32_t c) {
-        uint8_t *dst = ring + (c % S) * L::kChunk;
-        const uint64_t at = base + (uint64_t)c * kRowsB;
-        mbar_expect_tx(&bar_in[c % S], L::kChunk);
-        bulk_load(dst, a.w_in.sf + at, kRowsB, &bar_in[c % S]);
-        bulk_load(dst + kRowsB, a.m_in.sf + at, kRowsB, &bar_in[c % S]);
-        bulk_load(dst + 2 * kRowsB, a.g + at, 2 * kRowsB, &bar_in[c % S]);
-    };
-    if (j == 0) {
-        mbar_expect_tx(&bar_slot, 2 * W * kStreams * 4);
-        bulk_load(slotW, a.w_in.slots + (uint64_t)b * W * kStreams, W * kStreams * 4, &bar_slot);
-        bulk_load(slotM, a.m_in.slots + (uint64_t)b * W * kStreams, W * kStreams * 4, &bar_slot);
-        for (uint32_t c = 0; c < (uint32_t)S && c < nbulk; ++c) issue(c);
-    }
+    __syncthreads();  // barriers initialised, tables built
 
     // input markers, spill prefixes and overflow ranges
-    const uint32_t nj = nb > (uint32_t)j ? (nb - j + 255) / 256 : 0;
     MomIn sw, sm;
     sw.col = slotW + j;
     sm.col = slotM + j;
-    {
-        const uint32_t mw = a.w_in.markers[(uint64_t)b * kStreams + j], mm = a.m_in.markers[(uint64_t)b * kStreams + j];
-        bad |= mw > nj || mm > nj;
-        sw.marker = min(mw, nj);
-        sm.marker = min(mm, nj);
-    }
+    bad |= mw > nj || mm > nj;
+    sw.marker = min(mw, nj);
+    sm.marker = min(mm, nj);
     bool ovf_ok_w, ovf_ok_m;
     {
         uint32_t tot_w, tot_m;
-        const uint32_t pre_w = group_exclusive_scan(nj - sw.marker, warp_tot, NW, 0, &tot_w);
-        const uint32_t pre_m = group_exclusive_scan(nj - sm.marker, warp_tot, NW, 0, &tot_m);
-        const uint64_t a0 = a.w_in.blk_off[b], a1 = a.w_in.blk_off[b + 1];
-        const uint64_t c0 = a.m_in.blk_off[b], c1 = a.m_in.blk_off[b + 1];
+        const uint32_t pre_w = group_exclusive_scan<1, kMomThreads>(nj - sw.marker, warp_tot, NW, 0, &tot_w);
+        const uint32_t pre_m = group_exclusive_scan<1, kMomThreads>(nj - sm.marker, warp_tot, NW, 0, &tot_m);
         ovf_ok_w = a1 <= a.w_in.ovf_cap && a0 <= a1 && a1 - a0 == tot_w;
         ovf_ok_m = c1 <= a.m_in.ovf_cap && c0 <= c1 && c1 - c0 == tot_m;
         sw.ovf_at = a0 + pre_w - sw.marker;
         sm.ovf_at = c0 + pre_m - sm.marker;
         bad |= !ovf_ok_w || !ovf_ok_m;
     }
+    const uint32_t colw_s = smem_addr(slotW + j), colm_s = smem_addr(slotM + j);
+    const uint32_t lutw_s = smem_addr(lutW), lutm_s = smem_addr(lutM);
+    const Mul mul{a.mul_row, a.mul_ent};
     const uint8_t *ovf_w = a.w_in.ovf, *ovf_m = a.m_in.ovf;
 
     if (!mbar_wait(&bar_slot, 0, limit)) s_flags = 1;
@@ -279,27 +438,12 @@ __global__ void __launch_bounds__(kMomThreads, INPLACE ? 1 : 2) k_momentum(const
         const uint64_t row0 = (uint64_t)c * kRowsB;
         const uint32_t k0 = c * R, kend = k0 + R;
         if (bulk && __all_sync(kFull, sw.marker >= kend && sm.marker >= kend)) {
-            // loads first (both decode chains, the chunk's bytes), stores last
-            uint32_t hW[R], hM[R];
-            {
-                uint32_t ew[R], em[R];
 #pragma unroll
-                for (int r = 0; r < R; r += 2) {
-                    rd_take2<W>(sw.pos, sw.col, lutW, ew[r], ew[r + 1]);
-                    rd_take2<W>(sm.pos, sm.col, lutM, em[r], em[r + 1]);
-                }
-#pragma unroll
-                for (int r = 0; r < R; ++r)
-                    hW[r] = Op::apply(join_one(sfwc[r * kStreams], ew[r]), join_one(sfmc[r * kStreams], em[r]),
-                                      gc[r * kStreams], kc, &hM[r]);
-            }
-#pragma unroll
-            for (int r = 0; r < R; ++r) {
-                sfWj[row0 + r * kStreams] = sf_of(hW[r]);
-                sfMj[row0 + r * kStreams] = sf_of(hM[r]);
-            }
-            mom_put_chunk<R, SP>(ow, hW, tblW, k0, colW, stageW + j);
-            mom_put_chunk<R, SP>(om, hM, tblM, k0, colM, stageM + j);
+            for (int g = 0; g < R / 4; ++g)
+                mom_group<OP, SP>(sw, sm, colw_s, colm_s, lutw_s, lutm_s, mul, sfwc + g * 4 * kStreams,
+                                  sfmc + g * 4 * kStreams, gc + g * 4 * kStreams, kc, ow, om, tblW, tblM, colW, colM,
+                                  sfWj + row0 + g * 4 * kStreams, sfMj + row0 + g * 4 * kStreams, stageW + j,
+                                  stageM + j, k0 + g * 4);
         } else {
             for (int r = 0; r < R; ++r) {
                 const uint32_t k = k0 + r;
@@ -319,8 +463,10 @@ __global__ void __launch_bounds__(kMomThreads, INPLACE ? 1 : 2) k_momentum(const
                 if (wr_put_checked(om, tblM[eM], k, colM)) stageM[(k % SP) * kRow + j] = (uint8_t)eM;
             }
         }
-        __syncthreads();  // every thread is done with this chunk's ring slot
-        if (j == 0 && c + S < nbulk) issue(c + S);
+        if (bulk) {  // this warp is done with the chunk's ring stage
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bar_free[slot]);
+        }
     }
     bad |= sw.pos > 32u * W || sm.pos > 32u * W;
     if (bad) atomicOr(&s_flags, 2u);
@@ -329,8 +475,8 @@ __global__ void __launch_bounds__(kMomThreads, INPLACE ? 1 : 2) k_momentum(const
     const uint32_t mk_w = ow.marker, sp_w = nj - mk_w;
     const uint32_t mk_m = om.marker, sp_m = nj - mk_m;
     uint32_t tot_w, tot_m;
-    const uint32_t pre_w = group_exclusive_scan(sp_w, warp_tot, NW, 0, &tot_w);
-    const uint32_t pre_m = group_exclusive_scan(sp_m, warp_tot, NW, 0, &tot_m);
+    const uint32_t pre_w = group_exclusive_scan<1, kMomThreads>(sp_w, warp_tot, NW, 0, &tot_w);
+    const uint32_t pre_m = group_exclusive_scan<1, kMomThreads>(sp_m, warp_tot, NW, 0, &tot_m);
     a.w_out.markers[(uint64_t)b * kStreams + j] = (uint16_t)mk_w;
     a.m_out.markers[(uint64_t)b * kStreams + j] = (uint16_t)mk_m;
 
@@ -352,7 +498,7 @@ __global__ void __launch_bounds__(kMomThreads, INPLACE ? 1 : 2) k_momentum(const
             s_excl[warp] = excl;
         }
     }
-    __syncthreads();
+    cta_sync<1, kMomThreads>();
 
     const unsigned long long excl_w = s_excl[0], excl_m = s_excl[1];
     const bool room_w = tot_w > 0 && excl_w + tot_w <= a.w_out.ovf_cap;
@@ -425,7 +571,7 @@ cudaError_t launch_level(const MomentumArgs &a, cudaStream_t s)
     cudaError_t err =
         cudaFuncSetAttribute(k_momentum<LEVEL, INPLACE, OP>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (err != cudaSuccess) return err;
-    return launch_pdl(k_momentum<LEVEL, INPLACE, OP>, dim3(a.w_out.nblocks), dim3(kMomThreads), smem, s, a);
+    return launch_pdl(k_momentum<LEVEL, INPLACE, OP>, dim3(a.w_out.nblocks), dim3(kMomBlock), smem, s, a);
 }
 
 template <int LEVEL, int OP>

@@ -41,6 +41,7 @@ struct UpdateOp;
 template <>
 struct UpdateOp<OP_SGD> {
     static constexpr int kInputs = 2;
+    static constexpr bool kTryCopy = true;  // a small step: the exponents mostly stay
     __device__ static __forceinline__ float apply(const uint32_t (&x)[2], const float *k)
     {
         return __fsub_rn(bf16_f(x[0]), __fmul_rn(k[0], bf16_f(x[1])));
@@ -52,6 +53,7 @@ struct UpdateOp<OP_SGD> {
 template <>
 struct UpdateOp<OP_ADAMW> {
     static constexpr int kInputs = 3;
+    static constexpr bool kTryCopy = false;  // steps of about lr: exponents change too often to try
     __device__ static __forceinline__ float apply(const uint32_t (&x)[3], const float *k)
     {
         const float w = bf16_f(x[0]);
@@ -197,12 +199,12 @@ __device__ __forceinline__ void update_group(InStream (&in)[NIN], const uint32_t
             r[t] = Op::apply(x, k);
         }
         P[q] = bf16x2_rne(r[0], r[1]);
-        same |= P[q] ^ __byte_perm(xw[0], xw[1], 0x5410);  // old weight values, packed the same way
+        if (Op::kTryCopy) same |= P[q] ^ __byte_perm(xw[0], xw[1], 0x5410);  // old weight values, packed the same way
         const uint32_t sfp = sf_of2(P[q]);
         sfo[(2 * q) * kStreams] = (uint8_t)sfp;
         sfo[(2 * q + 1) * kStreams] = (uint8_t)(sfp >> 16);
     }
-    if (__all_sync(kFull, wo.alive && !(same & 0x7F807F80u) && bc <= 32u && bc <= wo.rem)) {
+    if (Op::kTryCopy && __all_sync(kFull, wo.alive && !(same & 0x7F807F80u) && bc <= 32u && bc <= wo.rem)) {
         wr_add(wo, make_uint2(wv[0][0] & ~(0xFFFFFFFFu >> bc), bc));
         wr_flush(wo, colO);
         wo.rem -= bc;

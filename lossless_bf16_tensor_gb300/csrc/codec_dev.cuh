@@ -165,9 +165,9 @@ __device__ __forceinline__ uint32_t imad(uint32_t a, uint32_t b, uint32_t c)
 
 // Runtime multipliers: x = 32 (bit position -> byte offset of a slot word
 // row, (p & 0x3E0) * 32 = (p >> 5) * 1024), y = 4 (table index -> byte
-// offset).
+// offset), z = 0x01010000 (a sign-fraction byte into bytes 2 and 3).
 struct Mul {
-    uint32_t x, y;
+    uint32_t x, y, z;
 };
 
 // One input stream for the pair reader: bit position and the shared address
@@ -212,6 +212,98 @@ __device__ __forceinline__ uint32_t bf16x2_rne(float lo, float hi)
 {
     uint32_t d, nan;
     asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi), "f"(lo));
+    asm("set.nan.u32.bf16x2 %0, %1, %1;" : "=r"(nan) : "r"(d));
+    return d ^ (nan & 0x003F003Fu);
+}
+
+// ------------------------------ float-ready decode table (update kernels)
+
+// A second decode-table layout for the kernels that compute on the values,
+// indexed like dec_entry by the next 8 bits of the stream:
+//   bits  0..4   L: bits consumed (code length, or escape length + 8)
+//   bits  5..9   zero
+//   bits 10..14  literal shift: escape length - 1 for an escape (a left
+//                shift of the window by it brings the literal to bits
+//                23..30), 31 for a coded symbol (the shifted window then
+//                keeps nothing below bit 31)
+//   bit  15      an escape, or a coded exponent of 255 (the warp takes the
+//                path that adds literals and canonicalises NaN)
+//   bits 23..30  the exponent, for a symbol with its own code (0 for escape)
+// Every field the position update does not want sits at bit 10 or above, so
+// the position may be advanced by the raw entries: its low 10 bits (all the
+// reader uses: word index and shift) stay exact, and the true advance over a
+// few symbols is (p_after - p_before) & 0x3FF.  The exponent sits where a
+// float32 has it, so joining it with its sign-fraction byte gives the
+// float32 bits of the BF16 value in one logic operation (join_f).
+constexpr uint32_t kEntFlag = 0x8000u;
+
+__device__ __forceinline__ uint32_t dec_entry_f(const DevCodebook &cb, int delta, int v)
+{
+    const uint32_t d = cb.dec[v], sym = d & 0x1FF, l = d >> 12;
+    if (sym == 256) return kEntFlag | (((l - 1u) & 31u) << 10) | (l + 8u);
+    const uint32_t e = cb.zero_atom && sym == 0 ? 0u : (sym + (uint32_t)delta) & 0xFFu;
+    return (e << 23) | (e == 255u ? kEntFlag : 0u) | (31u << 10) | l;
+}
+
+// Two symbols at bit p with raw entries (see dec_entry_f); w0, w1 are the
+// windows at each symbol for lit_fix_f.  The second window is the first one
+// shifted by the first symbol's length, taken from the entry's low 5 bits by
+// the funnel shift itself; the position is advanced by the raw entries.  Word
+// indices are taken modulo 32 as in rd_pair.
+__device__ __forceinline__ void rd_pair_f(Rd &r, uint32_t lut, const Mul m, uint32_t &w0, uint32_t &w1, uint32_t &ent0,
+                                          uint32_t &ent1)
+{
+    const uint32_t a = imad(r.p & 0x3E0u, m.x, r.col);
+    const uint32_t hi = lds32(a), lo = lds32(a + kStreams * 4);
+    w0 = __funnelshift_l(lo, hi, r.p);  // the next 32 bits
+    ent0 = lds32(imad(w0 >> 24, m.y, lut));
+    w1 = __funnelshift_l(0u, w0, ent0);  // w0 << L0
+    ent1 = lds32(imad(w1 >> 24, m.y, lut));
+    r.p = r.p + ent0 + ent1;
+}
+
+// One symbol at exact bit p of a slot image column (word w at col[w * 256]),
+// for the checked paths: the entry with its literal added; p advanced
+// exactly.  The word index is clamped to the slot (zero guard row after it).
+template <int W>
+__device__ __forceinline__ uint32_t rd_take_f(uint32_t &p, const uint32_t *__restrict__ col,
+                                              const uint32_t *__restrict__ lut)
+{
+    const uint32_t w = min(p >> 5, (uint32_t)(W - 1));
+    const uint32_t hi = col[w * kStreams], lo = col[(w + 1) * kStreams];
+    const uint32_t win = __funnelshift_l(lo, hi, p);
+    const uint32_t ent = lut[win >> 24];
+    p += ent & 31u;
+    return ent | __funnelshift_l(0u, win, ent >> 10);
+}
+
+// The entry with its escape literal added in bits 23..30 (a coded symbol's
+// shift of 31 only touches bit 31, which join_f ignores).
+__device__ __forceinline__ uint32_t lit_fix_f(uint32_t w, uint32_t ent)
+{
+    return ent | __funnelshift_l(0u, w, ent >> 10);
+}
+
+// float32 bits of the BF16 value with sign-fraction byte sf and the entry's
+// exponent: sf * 0x01010000 (mz) puts the sign at bit 31 and the fraction at
+// bits 16..22, and one logic operation takes bits 23..30 from the entry.
+__device__ __forceinline__ uint32_t join_f(uint32_t sf, uint32_t ent, uint32_t mz)
+{
+    return (ent & 0x7F800000u) | (imad(sf, mz, 0u) & 0x807FFFFFu);
+}
+
+// Two float32 results -> two BF16 (round to nearest even, subnormals kept)
+// packed lo | hi << 16, with NaN left as the conversion writes it (0x7FFF);
+// nan_canon2 turns such halves into this library's 0x7FC0.
+__device__ __forceinline__ uint32_t bf16x2_rn(float lo, float hi)
+{
+    uint32_t d;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi), "f"(lo));
+    return d;
+}
+__device__ __forceinline__ uint32_t nan_canon2(uint32_t d)
+{
+    uint32_t nan;
     asm("set.nan.u32.bf16x2 %0, %1, %1;" : "=r"(nan) : "r"(d));
     return d ^ (nan & 0x003F003Fu);
 }

@@ -100,7 +100,7 @@ __global__ void __launch_bounds__(kDecThreads, 4) k_decode(const __grid_constant
     if (!mbar_wait(&bar_slot, 0, limit)) s_timeout = 1;
     const uint32_t *col = slot_s + j;
     const uint32_t col_s = smem_addr(col), lut_s = smem_addr(lut);
-    const Mul mul{a.mul_row, a.mul_ent};
+    const Mul mul{a.mul_row, a.mul_ent, a.mul_sf};
     uint32_t pos = 0;  // bit position in the slot
     uint16_t *yj = a.y + (base - (uint64_t)a.first_block * G::B) + j;
 

@@ -73,7 +73,7 @@ struct EncodeArgs {
     int32_t median_exp;
     uint32_t pad;
     uint64_t wait_ns;
-    uint32_t mul_row, mul_ent;  // 32 and 4 (set_multipliers)
+    uint32_t mul_row, mul_ent, mul_sf, pad_mul;  // 32, 4 and 0x01010000 (set_multipliers)
 };
 
 struct DecodeArgs {
@@ -83,7 +83,7 @@ struct DecodeArgs {
     uint64_t wait_ns;
     uint32_t first_block;  // the launch decodes blocks first_block .. + grid size
     uint32_t pad;
-    uint32_t mul_row, mul_ent;  // 32 and 4 (set_multipliers)
+    uint32_t mul_row, mul_ent, mul_sf, pad_mul;  // 32, 4 and 0x01010000 (set_multipliers)
 };
 
 // Weight updates of the fused one-pass kernel.
@@ -99,7 +99,7 @@ struct UpdateArgs {
     uint32_t in_place;    // W_out's sign-fraction bytes are W_in's
     uint32_t pad;
     uint64_t wait_ns;
-    uint32_t mul_row, mul_ent;  // 32 and 4 (set_multipliers)
+    uint32_t mul_row, mul_ent, mul_sf, pad_mul;  // 32, 4 and 0x01010000 (set_multipliers)
 };
 
 // Updates of the fused two-state kernel (two compressed tensors and a dense
@@ -114,7 +114,7 @@ struct MomentumArgs {
     uint32_t op;        // OP2_MOMENTUM or OP2_ADAM_MOMENTS
     uint32_t in_place;  // an output shares its input's sign-fraction bytes
     uint64_t wait_ns;
-    uint32_t mul_row, mul_ent;  // 32 and 4 (set_multipliers)
+    uint32_t mul_row, mul_ent, mul_sf, pad_mul;  // 32, 4 and 0x01010000 (set_multipliers)
 };
 
 template <typename Args>
@@ -122,6 +122,8 @@ inline void set_multipliers(Args &a)
 {
     a.mul_row = 32;
     a.mul_ent = 4;
+    a.mul_sf = 0x01010000u;
+    a.pad_mul = 0;
 }
 
 cudaError_t launch_encode(const EncodeArgs &a, cudaStream_t s);

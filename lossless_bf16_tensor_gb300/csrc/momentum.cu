@@ -410,7 +410,7 @@ __global__ void __launch_bounds__(kMomBlock, INPLACE ? 1 : 2) k_momentum(const _
     }
     const uint32_t colw_s = smem_addr(slotW + j), colm_s = smem_addr(slotM + j);
     const uint32_t lutw_s = smem_addr(lutW), lutm_s = smem_addr(lutM);
-    const Mul mul{a.mul_row, a.mul_ent};
+    const Mul mul{a.mul_row, a.mul_ent, a.mul_sf};
     const uint8_t *ovf_w = a.w_in.ovf, *ovf_m = a.m_in.ovf;
 
     if (!mbar_wait(&bar_slot, 0, limit)) s_flags = 1;

@@ -37,14 +37,17 @@ template <int OP>
 struct UpdateOp;
 
 // W' = bf16(fl32(w - fl32(k0*m))): product and difference rounded separately
-// (apply returns the float32 result; the caller rounds it to BF16).
+// (apply takes the inputs as float32 and returns the float32 result; the
+// caller rounds it to BF16).  With finite inputs and a finite eta the result
+// is never NaN (an overflowing product gives an infinity, not inf - inf).
 template <>
 struct UpdateOp<OP_SGD> {
     static constexpr int kInputs = 2;
     static constexpr bool kTryCopy = true;  // a small step: the exponents mostly stay
-    __device__ static __forceinline__ float apply(const uint32_t (&x)[2], const float *k)
+    static constexpr bool kNanFree = true;  // given finite inputs and a finite k[0]
+    __device__ static __forceinline__ float apply(const float (&x)[2], const float *k)
     {
-        return __fsub_rn(bf16_f(x[0]), __fmul_rn(k[0], bf16_f(x[1])));
+        return __fsub_rn(x[0], __fmul_rn(k[0], x[1]));
     }
 };
 
@@ -54,11 +57,12 @@ template <>
 struct UpdateOp<OP_ADAMW> {
     static constexpr int kInputs = 3;
     static constexpr bool kTryCopy = false;  // steps of about lr: exponents change too often to try
-    __device__ static __forceinline__ float apply(const uint32_t (&x)[3], const float *k)
+    static constexpr bool kNanFree = false;  // sqrt of a negative input, 0/0
+    __device__ static __forceinline__ float apply(const float (&x)[3], const float *k)
     {
-        const float w = bf16_f(x[0]);
-        const float den = __fadd_rn(__fmul_rn(__fsqrt_rn(bf16_f(x[2])), k[5]), k[6]);
-        const float upd = __fdiv_rn(__fmul_rn(k[4], bf16_f(x[1])), den);
+        const float w = x[0];
+        const float den = __fadd_rn(__fmul_rn(__fsqrt_rn(x[2]), k[5]), k[6]);
+        const float upd = __fdiv_rn(__fmul_rn(k[4], x[1]), den);
         return __fsub_rn(__fsub_rn(w, __fmul_rn(k[7], w)), upd);
     }
 };
@@ -86,6 +90,7 @@ struct SgdSmem {
     static constexpr int kCtas = kFit < kWant ? kFit : kWant;
     static_assert(kKeepAll || (kSgdSpill & (kSgdSpill - 1)) == 0, "ring index uses a mask");
     static_assert(kRows % 4 == 0, "four-row groups");
+    static_assert(kRows * 16 < 1024, "a chunk's advance fits the positions' exact low 10 bits");
     static_assert(kBytes <= 227 * 1024 && kCtas >= 1, "shared memory of one CTA");
     // the pair reader's reads from the last slot image stay inside the CTA
     static_assert((NIN - 1) * kSlotIn + 33 * 1024 <= kBytes, "33 KB after every slot image");
@@ -133,13 +138,14 @@ struct InStream {
     uint64_t ovf_at;      // overflow index of spilled symbol k is ovf_at + k
 };
 
-// Symbol k of an input stream as a decode-table entry (exponent in bits 7..14).
+// Symbol k of an input stream as a float-ready decode-table entry (exponent
+// in bits 23..30, literal added).
 template <int W>
 __device__ __forceinline__ uint32_t in_take(InStream &s, uint32_t k, const uint32_t *lut, const uint8_t *ovf,
                                             bool ovf_ok)
 {
-    if (k < s.marker) return rd_take<W>(s.pos, s.col, lut);
-    return ovf_ok ? (uint32_t)__ldg(ovf + s.ovf_at + k) << 7 : 0u;
+    if (k < s.marker) return rd_take_f<W>(s.pos, s.col, lut);
+    return ovf_ok ? (uint32_t)__ldg(ovf + s.ovf_at + k) << 23 : 0u;
 }
 
 // Slot of a spilled new exponent in the staging rows: t = k - marker counts
@@ -150,22 +156,57 @@ __device__ __forceinline__ uint32_t stage_row(uint32_t t)
     return KEEP_ALL ? t : (t & (SP - 1));
 }
 
+// The four rows' values of a group from their entries (literals added) and
+// sign-fraction bytes: updated, rounded two at a time (NaN canonicalised when
+// CANON), sign-fraction bytes written; `same` collects where the new values
+// differ from the old weight's.
+template <int NIN, typename Op, bool CANON>
+__device__ __forceinline__ void round_group(const uint32_t (&ev)[NIN][4], uint8_t *const (&sf_s)[NIN], uint32_t sf_at,
+                                            const float *k, uint32_t mz, uint32_t (&P)[2], uint32_t &same,
+                                            uint8_t *sfo)
+{
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+        float r[2];
+        uint32_t xw[2];
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+            float x[NIN];
+#pragma unroll
+            for (int i = 0; i < NIN; ++i) {
+                const uint32_t f = join_f(sf_s[i][sf_at + (2 * q + t) * kStreams], ev[i][2 * q + t], mz);
+                x[i] = __uint_as_float(f);
+                if (i == 0) xw[t] = f;
+            }
+            r[t] = Op::apply(x, k);
+        }
+        P[q] = bf16x2_rn(r[0], r[1]);
+        if (CANON) P[q] = nan_canon2(P[q]);
+        if (Op::kTryCopy) same |= P[q] ^ __byte_perm(xw[0], xw[1], 0x7632);  // old weight values, packed the same way
+        const uint32_t sfp = sf_of2(P[q]);
+        sfo[(2 * q) * kStreams] = (uint8_t)sfp;
+        sfo[(2 * q + 1) * kStreams] = (uint8_t)(sfp >> 16);
+    }
+}
+
 // Four rows of every stream on the fast path (every input symbol of the rows
-// lies in its slot).  The inputs' symbols are decoded two at a time with the
-// escape literals deferred (a warp fixes them up only when one of its lanes
-// met an escape), the four values are updated and rounded two at a time, and
-// their sign-fraction bytes written.  When no new exponent of the warp's
-// streams differs from the old weight's, the new codes are the old weight's
-// codes bit for bit (same codebook, same stored shift), so the rows' bits are
-// appended straight from the old weight's stream window.  Otherwise the new
-// codes are looked up and appended, with the fit check per value only when
-// some stream of the warp may not keep all four.
+// lies in its slot).  The inputs' symbols are decoded two at a time with raw
+// float-ready entries (the positions carry the entries' upper fields above
+// bit 9; the caller restores exact positions after the chunk).  A warp adds
+// escape literals, and canonicalises NaN, only when one of its lanes met an
+// escape or an exponent of 255 (or every group does when canon_all); with no
+// such symbol and finite inputs an SGD step cannot produce NaN.  When no new
+// exponent of the warp's streams differs from the old weight's, the new codes
+// are the old weight's codes bit for bit (same codebook, same stored shift),
+// so the rows' bits are appended straight from the old weight's stream
+// window.  Otherwise the new codes are looked up and appended, with the fit
+// check per value only when some stream of the warp may not keep all four.
 template <int W, int NIN, typename Op, bool KEEP_ALL, int SP>
 __device__ __forceinline__ void update_group(InStream (&in)[NIN], const uint32_t (&col_s)[NIN],
                                              const uint32_t (&lut_s)[NIN], const Mul mul,
                                              uint8_t *const (&sf_s)[NIN], uint32_t sf_at, const float *k,
-                                             const uint2 *tbl, Writer &wo, uint32_t *colO, uint8_t *sfo,
-                                             uint8_t *ringj, uint32_t k0)
+                                             bool canon_all, const uint2 *tbl, Writer &wo, uint32_t *colO,
+                                             uint8_t *sfo, uint8_t *ringj, uint32_t k0)
 {
     uint32_t wv[NIN][4], ev[NIN][4], esc = 0;
     const uint32_t p0 = in[0].pos;
@@ -174,36 +215,21 @@ __device__ __forceinline__ void update_group(InStream (&in)[NIN], const uint32_t
 #pragma unroll
         for (int i = 0; i < NIN; ++i) {
             Rd r{in[i].pos, col_s[i]};
-            rd_pair(r, lut_s[i], mul, wv[i][2 * q], wv[i][2 * q + 1], ev[i][2 * q], ev[i][2 * q + 1]);
+            rd_pair_f(r, lut_s[i], mul, wv[i][2 * q], wv[i][2 * q + 1], ev[i][2 * q], ev[i][2 * q + 1]);
             in[i].pos = r.p;
             esc |= ev[i][2 * q] | ev[i][2 * q + 1];
         }
-    if (__any_sync(kFull, esc_bits(esc))) {
+    uint32_t P[2], same = 0;
+    if (__any_sync(kFull, esc & kEntFlag) || canon_all) {
 #pragma unroll
         for (int i = 0; i < NIN; ++i)
 #pragma unroll
-            for (int t = 0; t < 4; ++t) ev[i][t] = lit_fix(wv[i][t], ev[i][t]);
+            for (int t = 0; t < 4; ++t) ev[i][t] = lit_fix_f(wv[i][t], ev[i][t]);
+        round_group<NIN, Op, true>(ev, sf_s, sf_at, k, mul.z, P, same, sfo);
+    } else {
+        round_group<NIN, Op, !Op::kNanFree>(ev, sf_s, sf_at, k, mul.z, P, same, sfo);
     }
-    const uint32_t bc = in[0].pos - p0;  // the old weight's bits of these rows
-    uint32_t P[2], same = 0;
-#pragma unroll
-    for (int q = 0; q < 2; ++q) {
-        float r[2];
-        uint32_t xw[2];
-#pragma unroll
-        for (int t = 0; t < 2; ++t) {
-            uint32_t x[NIN];
-#pragma unroll
-            for (int i = 0; i < NIN; ++i) x[i] = join_one(sf_s[i][sf_at + (2 * q + t) * kStreams], ev[i][2 * q + t]);
-            xw[t] = x[0];
-            r[t] = Op::apply(x, k);
-        }
-        P[q] = bf16x2_rne(r[0], r[1]);
-        if (Op::kTryCopy) same |= P[q] ^ __byte_perm(xw[0], xw[1], 0x5410);  // old weight values, packed the same way
-        const uint32_t sfp = sf_of2(P[q]);
-        sfo[(2 * q) * kStreams] = (uint8_t)sfp;
-        sfo[(2 * q + 1) * kStreams] = (uint8_t)(sfp >> 16);
-    }
+    const uint32_t bc = (in[0].pos - p0) & 0x3FFu;  // the old weight's bits of these rows
     if (Op::kTryCopy && __all_sync(kFull, wo.alive && !(same & 0x7F807F80u) && bc <= 32u && bc <= wo.rem)) {
         wr_add(wo, make_uint2(wv[0][0] & ~(0xFFFFFFFFu >> bc), bc));
         wr_flush(wo, colO);
@@ -262,7 +288,7 @@ __global__ void __launch_bounds__(kSgdBlock, SgdSmem<LEVEL, INPLACE, UpdateOp<OP
         col_s[i] = smem_addr(slot[i] + threadIdx.x);
         lut_s[i] = smem_addr(lut[i]);
     }
-    const Mul mul{a.mul_row, a.mul_ent};
+    const Mul mul{a.mul_row, a.mul_ent, a.mul_sf};
     // bar_sf[s]: stage s of the ring has landed; bar_free[s]: every consumer
     // warp is done with stage s (the producer may refill it)
     __shared__ __align__(8) uint64_t bar_slot, bar_sf[S], bar_free[S];
@@ -338,7 +364,7 @@ __global__ void __launch_bounds__(kSgdBlock, SgdSmem<LEVEL, INPLACE, UpdateOp<OP
     }
 #pragma unroll
     for (int i = 0; i < NIN; ++i) {
-        lut[i][j] = dec_entry(a.cb[i], i == 0 ? delta_w : delta_in[i], j);
+        lut[i][j] = dec_entry_f(a.cb[i], i == 0 ? delta_w : delta_in[i], j);
         slot[i][W * kStreams + j] = 0u;
     }
     tbl[j] = enc_entry(a.cb[0], delta_w, j);
@@ -369,6 +395,7 @@ __global__ void __launch_bounds__(kSgdBlock, SgdSmem<LEVEL, INPLACE, UpdateOp<OP
     float k[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) k[i] = a.k[i];
+    const bool canon_all = !isfinite(k[0]);  // a non-finite eta can make NaN from finite inputs
 
     for (uint32_t c = 0; c < nchunks; ++c) {
         const bool bulk = c < nbulk;
@@ -381,22 +408,29 @@ __global__ void __launch_bounds__(kSgdBlock, SgdSmem<LEVEL, INPLACE, UpdateOp<OP
         for (int i = 0; i < NIN; ++i) in_slot = in_slot && in[i].marker >= kend;
         if (bulk && __all_sync(kFull, in_slot)) {
             const uint32_t sf_at = slot_c * R * kStreams;
+            uint32_t p_start[NIN];
+#pragma unroll
+            for (int i = 0; i < NIN; ++i) p_start[i] = in[i].pos;
 #pragma unroll
             for (int g = 0; g < R / 4; ++g)
                 update_group<W, NIN, Op, L::kKeepAll, SP>(in, col_s, lut_s, mul, sf_s, sf_at + g * 4 * kStreams + j,
-                                                          k, tbl, wo, colO, sfo + g * 4 * kStreams, ringj,
-                                                          c * R + g * 4);
+                                                          k, canon_all, tbl, wo, colO, sfo + g * 4 * kStreams,
+                                                          ringj, c * R + g * 4);
+            // exact positions again: a chunk advances a stream by at most
+            // R * 16 < 1024 bits, which the low 10 bits hold exactly
+#pragma unroll
+            for (int i = 0; i < NIN; ++i) in[i].pos = p_start[i] + ((in[i].pos - p_start[i]) & 0x3FFu);
         } else {
             for (int r = 0; r < R; ++r) {
                 const uint32_t kk = c * R + r;
                 if (kk >= nj) break;
                 const uint64_t at = base + (uint64_t)kk * kStreams + j;
-                uint32_t x[NIN];
+                float x[NIN];
 #pragma unroll
                 for (int i = 0; i < NIN; ++i) {
                     const uint32_t ei = in_take<W>(in[i], kk, lut[i], a.in[i].ovf, ovf_ok[i]);
                     const uint32_t fi = bulk ? sf_s[i][slot_c * R * kStreams + r * kStreams + j] : a.in[i].sf[at];
-                    x[i] = join_one(fi, ei);
+                    x[i] = __uint_as_float(join_f(fi, ei, mul.z));
                 }
                 const uint32_t hv = bf16_rne(Op::apply(x, k));
                 const uint32_t ev = exp_of(hv);
@@ -462,10 +496,11 @@ __global__ void __launch_bounds__(kSgdBlock, SgdSmem<LEVEL, INPLACE, UpdateOp<OP
             }
             for (uint32_t kk = 0; kk < kept_from; ++kk) {
                 const uint64_t at = base + (uint64_t)kk * kStreams + j;
-                uint32_t x[NIN];
+                float x[NIN];
 #pragma unroll
                 for (int i = 0; i < NIN; ++i)
-                    x[i] = join_one(a.in[i].sf[at], in_take<W>(re[i], kk, lut[i], a.in[i].ovf, ovf_ok[i]));
+                    x[i] = __uint_as_float(join_f(a.in[i].sf[at], in_take<W>(re[i], kk, lut[i], a.in[i].ovf, ovf_ok[i]),
+                                                  mul.z));
                 const uint32_t hv = bf16_rne(Op::apply(x, k));
                 if (kk >= marker) out[pre + (kk - marker)] = exp_of(hv);
             }

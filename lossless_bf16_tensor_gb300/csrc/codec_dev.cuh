@@ -568,12 +568,28 @@ __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;"
 
 // ------------------------------------------------ decoupled look-back
 
-constexpr unsigned long long kFlagAgg = 1ull << 62;  // block total published
+// A block's status word (one per block, in the tensor's scratch region):
+//   bits 62..63  0: nothing published yet, 1: the block's own overflow
+//                count, 2: the block's inclusive prefix
+//   bits 41..61  the block's own overflow count (at most 65,536 bytes)
+//   bits  0..40  the count (flag 1) or the inclusive prefix (flag 2)
+// Every word carries the block's own count, so the block offsets can also be
+// computed from the words afterwards (k_block_offsets), whatever mix of
+// flags the blocks left.
+constexpr unsigned long long kFlagAgg = 1ull << 62;  // block count published
 constexpr unsigned long long kFlagInc = 2ull << 62;  // inclusive prefix published
-constexpr unsigned long long kValMask = (1ull << 62) - 1;
+constexpr unsigned long long kValMask = (1ull << 41) - 1;
+constexpr int kOwnShift = 41;
+constexpr unsigned long long kOwnMask = (1ull << 21) - 1;
+
+__device__ __forceinline__ unsigned long long status_word(unsigned long long flag, unsigned long long own,
+                                                          unsigned long long value)
+{
+    return flag | ((own & kOwnMask) << kOwnShift) | (value & kValMask);
+}
 
 // A status word is read and written whole (one aligned 64-bit access) and
-// carries everything a successor uses from it: the flag and the count.  No
+// carries everything a successor uses from it: the flag and the counts.  No
 // other data is handed over through it, so relaxed accesses at GPU scope are
 // enough; a release would first have to make every earlier global store of
 // the CTA (its sign-fraction bytes and markers) visible.
@@ -603,10 +619,10 @@ static __device__ __noinline__ unsigned long long warp_lookback(unsigned long lo
     const int lane = threadIdx.x & 31;
     *timed_out = false;
     if (b == 0) {
-        if (lane == 0) st_status(&status[0], kFlagInc | total);
+        if (lane == 0) st_status(&status[0], status_word(kFlagInc, total, total));
         return 0;
     }
-    if (lane == 0) st_status(&status[b], kFlagAgg | total);
+    if (lane == 0) st_status(&status[b], status_word(kFlagAgg, total, total));
     unsigned long long excl = 0;
     int64_t nearest = (int64_t)b - 1;
     const uint64_t t0 = global_ns();
@@ -634,28 +650,66 @@ static __device__ __noinline__ unsigned long long warp_lookback(unsigned long lo
         if (inc) break;
         nearest -= 32;
     }
-    if (lane == 0) st_status(&status[b], kFlagInc | ((excl + total) & kValMask));
+    if (lane == 0) st_status(&status[b], status_word(kFlagInc, total, excl + total));
     return excl;
 }
 
-// The same protocol run by a single thread (used by the wait-timeout test hook).
+// For a block with no overflow bytes when the offsets are computed
+// afterwards (deferred placement): publish the count (0), then look back
+// through at most `rounds` windows of 32 predecessors without ever waiting.
+// If every one of them up to a published inclusive prefix has published its
+// count, this block's inclusive prefix is published as well, which keeps the
+// look-backs of later blocks that do have bytes to place short; otherwise the
+// count stays, which is all k_block_offsets needs.
+static __device__ __noinline__ void warp_publish_try(unsigned long long *status, uint32_t b, int rounds)
+{
+    const int lane = threadIdx.x & 31;
+    if (b == 0) {
+        if (lane == 0) st_status(&status[0], status_word(kFlagInc, 0, 0));
+        return;
+    }
+    if (lane == 0) st_status(&status[b], status_word(kFlagAgg, 0, 0));
+    unsigned long long excl = 0;
+    int64_t nearest = (int64_t)b - 1;
+    for (int r = 0; r < rounds; ++r) {
+        const int64_t idx = nearest - lane;
+        const unsigned long long v = idx >= 0 ? ld_status(&status[idx]) : kFlagInc;
+        const uint32_t flag = (uint32_t)(v >> 62);
+        const uint32_t inc = __ballot_sync(kFull, flag == 2u);
+        const uint32_t not_ready = __ballot_sync(kFull, flag == 0u);
+        const uint32_t upto = inc ? ((inc & (0u - inc)) << 1) - 1u : kFull;
+        if (not_ready & upto) return;
+        unsigned long long mine = ((upto >> lane) & 1u) ? (v & kValMask) : 0ull;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) mine += __shfl_xor_sync(kFull, mine, o);
+        excl += mine;
+        if (inc) {
+            if (lane == 0) st_status(&status[b], status_word(kFlagInc, 0, excl));
+            return;
+        }
+        nearest -= 32;
+    }
+}
+
+// The same protocol as warp_lookback run by a single thread (used by the
+// wait-timeout test hook).
 static __device__ __noinline__ unsigned long long lookback(unsigned long long *status, uint32_t b,
                                                            unsigned long long total, uint64_t wait_ns,
                                                            bool *timed_out)
 {
     *timed_out = false;
     if (b == 0) {
-        st_status(&status[0], kFlagInc | total);
+        st_status(&status[0], status_word(kFlagInc, total, total));
         return 0;
     }
-    st_status(&status[b], kFlagAgg | total);
+    st_status(&status[b], status_word(kFlagAgg, total, total));
     unsigned long long excl = 0;
     const uint64_t t0 = global_ns();
     uint32_t spins = 0;
     int64_t pred = (int64_t)b - 1;
     while (pred >= 0) {
         const unsigned long long v = ld_status(&status[pred]);
-        const unsigned long long flag = v & ~kValMask;
+        const unsigned long long flag = v >> 62;
         if (flag == 0) {
             ++spins;
             if (spins > (1u << 26) || ((spins & 63u) == 0 && global_ns() - t0 > wait_ns)) {
@@ -666,10 +720,10 @@ static __device__ __noinline__ unsigned long long lookback(unsigned long long *s
             continue;
         }
         excl += v & kValMask;
-        if (flag == kFlagInc) break;
+        if (flag == 2) break;
         --pred;
     }
-    st_status(&status[b], kFlagInc | ((excl + total) & kValMask));
+    st_status(&status[b], status_word(kFlagInc, total, excl + total));
     return excl;
 }
 

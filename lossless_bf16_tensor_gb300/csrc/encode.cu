@@ -247,27 +247,36 @@ __global__ void __launch_bounds__(kEncThreads, 4) k_encode(const __grid_constant
     }
     a.t.markers[(uint64_t)b * kStreams + j] = (uint16_t)marker;
 
-    // overflow offset of this block (single-pass decoupled look-back)
+    // Overflow offset of this block: the single-pass decoupled look-back, or,
+    // with deferred placement, a count published without waiting when the
+    // block has nothing to place (k_block_offsets writes the offsets after).
+    const bool leave = a.deferred && total == 0;
     if (warp == 0) {
-        bool timed_out;
-        const unsigned long long excl = warp_lookback(a.t.work, b, total, limit, &timed_out);
-        if (lane == 0) {
-            if (timed_out) latch(a.t.hdr, LCT_ERR_TIMEOUT);
-            a.t.blk_off[b] = excl;
-            if (b == a.t.nblocks - 1) {
-                a.t.blk_off[b + 1] = excl + total;
-                a.t.hdr->ovf_used = excl + total;
+        if (leave) {
+            warp_publish_try(a.t.work, b, 2);
+        } else {
+            bool timed_out;
+            const unsigned long long excl = warp_lookback(a.t.work, b, total, limit, &timed_out);
+            if (lane == 0) {
+                if (timed_out) latch(a.t.hdr, LCT_ERR_TIMEOUT);
+                if (!a.deferred) {
+                    a.t.blk_off[b] = excl;
+                    if (b == a.t.nblocks - 1) {
+                        a.t.blk_off[b + 1] = excl + total;
+                        a.t.hdr->ovf_used = excl + total;
+                    }
+                    if (excl + total > a.t.ovf_cap) latch(a.t.hdr, LCT_ERR_OVERFLOW_CAPACITY);
+                }
+                s_excl = excl;
             }
-            if (excl + total > a.t.ovf_cap) latch(a.t.hdr, LCT_ERR_OVERFLOW_CAPACITY);
-            s_excl = excl;
         }
     }
-    __syncthreads();
-
-    const unsigned long long excl = s_excl;
+    if (!leave) __syncthreads();  // uniform: total is the block's
+    const unsigned long long excl = leave ? 0ull : s_excl;
 
     // spilled exponents, raw, in (stream, symbol) order: one warp per stream
-    // at a time, lanes over the stream's spilled symbols
+    // at a time, lanes over the stream's spilled symbols (beyond the
+    // capacity nothing is written; the capacity error is latched)
     if (total > 0 && excl + total <= a.t.ovf_cap) {
         uint8_t *out = a.t.ovf + excl;
         for (int i = 0; i < 32; ++i) {
@@ -303,7 +312,11 @@ cudaError_t launch_level(const EncodeArgs &a, cudaStream_t s)
     constexpr int smem = EncodeSmem<LEVEL>::kBytes;
     cudaError_t err = cudaFuncSetAttribute(k_encode<LEVEL>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (err != cudaSuccess) return err;
-    return launch_pdl(k_encode<LEVEL>, dim3(a.t.nblocks), dim3(kEncThreads), smem, s, a);
+    EncodeArgs b = a;
+    b.deferred = deferred_placement(a.t.nblocks);
+    err = launch_pdl(k_encode<LEVEL>, dim3(a.t.nblocks), dim3(kEncThreads), smem, s, b);
+    if (err != cudaSuccess || !b.deferred) return err;
+    return launch_block_offsets(a.t, s);
 }
 
 }  // namespace dev

@@ -74,6 +74,7 @@ struct EncodeArgs {
     uint32_t pad;
     uint64_t wait_ns;
     uint32_t mul_row, mul_ent, mul_sf, pad_mul;  // 32, 4 and 0x01010000 (set_multipliers)
+    uint32_t deferred, pad_def;  // block offsets computed after the writer (set by its launcher)
 };
 
 struct DecodeArgs {
@@ -84,6 +85,7 @@ struct DecodeArgs {
     uint32_t first_block;  // the launch decodes blocks first_block .. + grid size
     uint32_t pad;
     uint32_t mul_row, mul_ent, mul_sf, pad_mul;  // 32, 4 and 0x01010000 (set_multipliers)
+    uint32_t deferred, pad_def;  // block offsets computed after the writer (set by its launcher)
 };
 
 // Weight updates of the fused one-pass kernel.
@@ -100,6 +102,7 @@ struct UpdateArgs {
     uint32_t pad;
     uint64_t wait_ns;
     uint32_t mul_row, mul_ent, mul_sf, pad_mul;  // 32, 4 and 0x01010000 (set_multipliers)
+    uint32_t deferred, pad_def;  // block offsets computed after the writer (set by its launcher)
 };
 
 // Updates of the fused two-state kernel (two compressed tensors and a dense
@@ -115,6 +118,7 @@ struct MomentumArgs {
     uint32_t in_place;  // an output shares its input's sign-fraction bytes
     uint64_t wait_ns;
     uint32_t mul_row, mul_ent, mul_sf, pad_mul;  // 32, 4 and 0x01010000 (set_multipliers)
+    uint32_t deferred, pad_def;  // block offsets computed after the writer (set by its launcher)
 };
 
 template <typename Args>
@@ -124,12 +128,21 @@ inline void set_multipliers(Args &a)
     a.mul_ent = 4;
     a.mul_sf = 0x01010000u;
     a.pad_mul = 0;
+    a.deferred = 0;
+    a.pad_def = 0;
 }
 
 cudaError_t launch_encode(const EncodeArgs &a, cudaStream_t s);
 cudaError_t launch_decode(const DecodeArgs &a, uint32_t nblocks, cudaStream_t s);
 cudaError_t launch_update(const UpdateArgs &a, cudaStream_t s);
 cudaError_t launch_momentum(const MomentumArgs &a, cudaStream_t s);
+// Deferred placement (grids of at least four blocks per SM): a block with no
+// overflow bytes publishes its count and leaves, blocks with bytes to place
+// still wait for their exclusive prefix, and launch_block_offsets (after the
+// writer) writes every block offset, ovf_used and the capacity check.
+bool deferred_placement(uint32_t nblocks);
+cudaError_t launch_block_offsets(const DevTensor &t, cudaStream_t s);
+cudaError_t launch_block_offsets2(const DevTensor &t0, const DevTensor &t1, cudaStream_t s);  // same nblocks
 cudaError_t launch_wait_probe(lct_header *hdr, unsigned long long *work, uint64_t wait_ns,
                               cudaStream_t s);
 

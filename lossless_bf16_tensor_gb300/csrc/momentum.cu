@@ -480,27 +480,37 @@ __global__ void __launch_bounds__(kMomBlock, INPLACE ? 1 : 2) k_momentum(const _
     a.w_out.markers[(uint64_t)b * kStreams + j] = (uint16_t)mk_w;
     a.m_out.markers[(uint64_t)b * kStreams + j] = (uint16_t)mk_m;
 
-    // warp 0 places W's overflow bytes, warp 1 places M's
+    // Warp 0 places W's overflow bytes, warp 1 places M's: the single-pass
+    // decoupled look-back, or, with deferred placement, a count published
+    // without waiting for an output with nothing to place (k_block_offsets
+    // writes the offsets after).
+    const bool leave = a.deferred && tot_w == 0 && tot_m == 0;
     if (warp < 2) {
         const DevTensor &t = warp == 0 ? a.w_out : a.m_out;
         const uint32_t total = warp == 0 ? tot_w : tot_m;
-        bool timed_out;
-        const unsigned long long excl = warp_lookback(t.work, b, total, limit, &timed_out);
+        bool timed_out = false;
+        unsigned long long excl = 0;
+        if (a.deferred && total == 0)
+            warp_publish_try(t.work, b, 2);
+        else
+            excl = warp_lookback(t.work, b, total, limit, &timed_out);
         if (lane == 0) {
             if (s_flags & 2u) latch(t.hdr, LCT_ERR_CORRUPT);
             if (timed_out || (s_flags & 1u)) latch(t.hdr, LCT_ERR_TIMEOUT);
-            t.blk_off[b] = excl;
-            if (b == t.nblocks - 1) {
-                t.blk_off[b + 1] = excl + total;
-                t.hdr->ovf_used = excl + total;
+            if (!a.deferred) {
+                t.blk_off[b] = excl;
+                if (b == t.nblocks - 1) {
+                    t.blk_off[b + 1] = excl + total;
+                    t.hdr->ovf_used = excl + total;
+                }
+                if (excl + total > t.ovf_cap) latch(t.hdr, LCT_ERR_OVERFLOW_CAPACITY);
             }
-            if (excl + total > t.ovf_cap) latch(t.hdr, LCT_ERR_OVERFLOW_CAPACITY);
             s_excl[warp] = excl;
         }
     }
-    cta_sync<1, kMomThreads>();
+    if (!leave) cta_sync<1, kMomThreads>();  // uniform: the totals are the block's
 
-    const unsigned long long excl_w = s_excl[0], excl_m = s_excl[1];
+    const unsigned long long excl_w = leave ? 0ull : s_excl[0], excl_m = leave ? 0ull : s_excl[1];
     const bool room_w = tot_w > 0 && excl_w + tot_w <= a.w_out.ovf_cap;
     const bool room_m = tot_m > 0 && excl_m + tot_m <= a.m_out.ovf_cap;
     uint8_t *out_w = a.w_out.ovf + excl_w;
@@ -571,7 +581,11 @@ cudaError_t launch_level(const MomentumArgs &a, cudaStream_t s)
     cudaError_t err =
         cudaFuncSetAttribute(k_momentum<LEVEL, INPLACE, OP>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (err != cudaSuccess) return err;
-    return launch_pdl(k_momentum<LEVEL, INPLACE, OP>, dim3(a.w_out.nblocks), dim3(kMomBlock), smem, s, a);
+    MomentumArgs b = a;
+    b.deferred = deferred_placement(a.w_out.nblocks);
+    err = launch_pdl(k_momentum<LEVEL, INPLACE, OP>, dim3(a.w_out.nblocks), dim3(kMomBlock), smem, s, b);
+    if (err != cudaSuccess || !b.deferred) return err;
+    return launch_block_offsets2(a.w_out, a.m_out, s);
 }
 
 template <int LEVEL, int OP>

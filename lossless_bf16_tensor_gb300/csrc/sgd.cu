@@ -453,24 +453,34 @@ __global__ void __launch_bounds__(kSgdBlock, SgdSmem<LEVEL, INPLACE, UpdateOp<OP
     const uint32_t pre = group_exclusive_scan<1, kSgdThreads>(spill, warp_tot, NW, 0, &total);
     a.w_out.markers[(uint64_t)b * kStreams + j] = (uint16_t)marker;
 
+    // Overflow offset of this block: the single-pass decoupled look-back, or,
+    // with deferred placement, a count published without waiting when the
+    // block has nothing to place (k_block_offsets writes the offsets after).
+    const bool leave = a.deferred && total == 0;
     if (warp == 0) {
-        bool timed_out;
-        const unsigned long long excl = warp_lookback(a.w_out.work, b, total, limit, &timed_out);
+        bool timed_out = false;
+        unsigned long long excl = 0;
+        if (leave)
+            warp_publish_try(a.w_out.work, b, 2);
+        else
+            excl = warp_lookback(a.w_out.work, b, total, limit, &timed_out);
         if (lane == 0) {
             if (s_flags & 2u) latch(a.w_out.hdr, LCT_ERR_CORRUPT);
             if (timed_out || (s_flags & 1u)) latch(a.w_out.hdr, LCT_ERR_TIMEOUT);
-            a.w_out.blk_off[b] = excl;
-            if (b == a.w_out.nblocks - 1) {
-                a.w_out.blk_off[b + 1] = excl + total;
-                a.w_out.hdr->ovf_used = excl + total;
+            if (!a.deferred) {
+                a.w_out.blk_off[b] = excl;
+                if (b == a.w_out.nblocks - 1) {
+                    a.w_out.blk_off[b + 1] = excl + total;
+                    a.w_out.hdr->ovf_used = excl + total;
+                }
+                if (excl + total > a.w_out.ovf_cap) latch(a.w_out.hdr, LCT_ERR_OVERFLOW_CAPACITY);
             }
-            if (excl + total > a.w_out.ovf_cap) latch(a.w_out.hdr, LCT_ERR_OVERFLOW_CAPACITY);
             s_excl = excl;
         }
     }
-    cta_sync<1, kSgdThreads>();
+    if (!leave) cta_sync<1, kSgdThreads>();  // uniform: total is the block's
 
-    const unsigned long long excl = s_excl;
+    const unsigned long long excl = leave ? 0ull : s_excl;
     if (total > 0 && excl + total <= a.w_out.ovf_cap) {
         uint8_t *out = a.w_out.ovf + excl;
         // spilled rows still kept in shared memory: one warp per stream at a time
@@ -525,7 +535,11 @@ cudaError_t launch_level(const UpdateArgs &a, cudaStream_t s)
     cudaError_t err =
         cudaFuncSetAttribute(k_update<LEVEL, INPLACE, OP>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (err != cudaSuccess) return err;
-    return launch_pdl(k_update<LEVEL, INPLACE, OP>, dim3(a.w_out.nblocks), dim3(kSgdBlock), smem, s, a);
+    UpdateArgs b = a;
+    b.deferred = deferred_placement(a.w_out.nblocks);
+    err = launch_pdl(k_update<LEVEL, INPLACE, OP>, dim3(a.w_out.nblocks), dim3(kSgdBlock), smem, s, b);
+    if (err != cudaSuccess || !b.deferred) return err;
+    return launch_block_offsets(a.w_out, s);
 }
 
 template <int LEVEL, int OP>

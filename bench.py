@@ -210,6 +210,15 @@ class ClockSampler:
 
 # ------------------------------------------------------------ GPU arm
 
+def placement_launches(n: int, level: str) -> int:
+    """Extra launches per written tensor: the writers place block offsets in a
+    separate one-CTA kernel on grids of at least four blocks per SM."""
+    import torch
+    block = 65536 if level == "CLEAN" else 32768
+    nblocks = (n + block - 1) // block
+    return 1 if nblocks >= 4 * torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count else 0
+
+
 def algorithmic_bytes(sizes, ovf_used: int) -> int:
     """Bytes of one compressed tensor that a pass over it moves: sign-fraction
     bytes, full fixed slots, markers, block offsets and the overflow used.
@@ -416,7 +425,7 @@ def run_gpu(args):
         },
         "clocks": clk,
         "e2e": e2e,
-        "gpu_launches": 5 * args.steps,
+        "gpu_launches": (5 + 2 * placement_launches(n, wl["level"])) * args.steps,
         "cpu_baseline": cpu,
     }
     return line
@@ -684,7 +693,8 @@ def run_gpu_momentum(args, rank, local_rank, world):
         "breakdown": {"compression_ratio_all_in_w": round(2.0 * n / (sizes.fixed_bytes + sw.ovf_used), 5),
                       "compression_ratio_all_in_m": round(2.0 * n / (sizes.fixed_bytes + sm_.ovf_used), 5),
                       "overflow_bytes_w": int(sw.ovf_used), "overflow_bytes_m": int(sm_.ovf_used)},
-        "clocks": clk, "e2e": None, "gpu_launches": 2 * args.steps, "cpu_baseline": cpu,
+        "clocks": clk, "e2e": None, "gpu_launches": (2 + placement_launches(n, wl["level"])) * args.steps,
+        "cpu_baseline": cpu,
     }
 
 
@@ -774,7 +784,8 @@ def run_gpu_adamw(args, rank, local_rank, world):
                      "algorithmic_bytes_per_launch": alg},
         "breakdown": {"compression_ratio_all_in": [round(2.0 * n / (sizes.fixed_bytes + s_.ovf_used), 5) for s_ in st],
                       "overflow_bytes": [int(s_.ovf_used) for s_ in st]},
-        "clocks": clk, "e2e": None, "gpu_launches": 4 * args.steps, "cpu_baseline": cpu,
+        "clocks": clk, "e2e": None, "gpu_launches": (4 + 2 * placement_launches(n, wl["level"])) * args.steps,
+        "cpu_baseline": cpu,
     }
 
 

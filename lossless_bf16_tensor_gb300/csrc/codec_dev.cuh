@@ -691,6 +691,12 @@ static __device__ __noinline__ void warp_publish_try(unsigned long long *status,
     }
 }
 
+// With deferred placement, every 32nd block waits in the look-back and
+// publishes its inclusive prefix even when it has nothing to place, so that
+// the look-back of a block that does (walking back over blocks that only
+// published their counts) reaches an inclusive prefix within two windows.
+__device__ __forceinline__ bool lookback_leader(uint32_t b) { return (b & 31u) == 31u; }
+
 // The same protocol as warp_lookback run by a single thread (used by the
 // wait-timeout test hook).
 static __device__ __noinline__ unsigned long long lookback(unsigned long long *status, uint32_t b,

@@ -250,7 +250,7 @@ __global__ void __launch_bounds__(kEncThreads, 4) k_encode(const __grid_constant
     // Overflow offset of this block: the single-pass decoupled look-back, or,
     // with deferred placement, a count published without waiting when the
     // block has nothing to place (k_block_offsets writes the offsets after).
-    const bool leave = a.deferred && total == 0;
+    const bool leave = a.deferred && total == 0 && !lookback_leader(b);
     if (warp == 0) {
         if (leave) {
             warp_publish_try(a.t.work, b, 2);

@@ -484,13 +484,13 @@ __global__ void __launch_bounds__(kMomBlock, INPLACE ? 1 : 2) k_momentum(const _
     // decoupled look-back, or, with deferred placement, a count published
     // without waiting for an output with nothing to place (k_block_offsets
     // writes the offsets after).
-    const bool leave = a.deferred && tot_w == 0 && tot_m == 0;
+    const bool leave = a.deferred && tot_w == 0 && tot_m == 0 && !lookback_leader(b);
     if (warp < 2) {
         const DevTensor &t = warp == 0 ? a.w_out : a.m_out;
         const uint32_t total = warp == 0 ? tot_w : tot_m;
         bool timed_out = false;
         unsigned long long excl = 0;
-        if (a.deferred && total == 0)
+        if (a.deferred && total == 0 && !lookback_leader(b))
             warp_publish_try(t.work, b, 2);
         else
             excl = warp_lookback(t.work, b, total, limit, &timed_out);

@@ -15,9 +15,14 @@ namespace lct {
 namespace dev {
 
 constexpr int kOffThreads = 1024;
+constexpr int kOffPer = 8;  // status words per thread per pass (8192 blocks a pass)
 
-// One CTA per tensor (the two-state update writes two), a CTA-wide scan per
-// 1024 status words with the running total carried between them.
+// One CTA per tensor (the two-state update writes two).  Each pass gives every
+// thread up to kOffPer consecutive status words, read together; their counts
+// are summed, the sums scanned across the CTA, and each thread writes its
+// words' offsets from its share of the scan.  One pass covers 8,192 blocks
+// (536M values in CLEAN blocks); larger tensors take more passes, the total so
+// far carried between them.
 __global__ void __launch_bounds__(kOffThreads) k_block_offsets(DevTensor t0, DevTensor t1)
 {
     const DevTensor &t = blockIdx.x == 0 ? t0 : t1;
@@ -28,16 +33,24 @@ __global__ void __launch_bounds__(kOffThreads) k_block_offsets(DevTensor t0, Dev
     __syncthreads();
     pdl_wait();  // every block of the writer has published its count
     pdl_launch_dependents();
+    const uint64_t nb = t.nblocks;
     unsigned long long carry = 0;
-    for (uint64_t first = 0; first < t.nblocks; first += kOffThreads) {
-        const uint64_t i = first + tid;
-        unsigned long long own = 0;
-        if (i < t.nblocks) {
-            const unsigned long long v = ld_status(&t.work[i]);
-            if ((v >> 62) == 0) s_missing = 1;  // a block that published nothing
-            own = (v >> kOwnShift) & kOwnMask;
+    for (uint64_t pass = 0; pass < nb; pass += (uint64_t)kOffThreads * kOffPer) {
+        const uint64_t first = pass + (uint64_t)tid * kOffPer;
+        unsigned long long own[kOffPer], sum = 0;
+        bool missing = false;
+#pragma unroll
+        for (int k = 0; k < kOffPer; ++k) {
+            own[k] = 0;
+            if (first + k < nb) {
+                const unsigned long long v = ld_status(&t.work[first + k]);
+                missing |= (v >> 62) == 0;  // a block that published nothing
+                own[k] = (v >> kOwnShift) & kOwnMask;
+            }
+            sum += own[k];
         }
-        unsigned long long inc = own;
+        if (missing) s_missing = 1;
+        unsigned long long inc = sum;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
             const unsigned long long u = __shfl_up_sync(kFull, inc, o);
@@ -45,18 +58,23 @@ __global__ void __launch_bounds__(kOffThreads) k_block_offsets(DevTensor t0, Dev
         }
         if (lane == 31) warp_sum[warp] = inc;
         __syncthreads();
-        unsigned long long before = 0, sum = 0;
+        unsigned long long before = 0, total = 0;
         for (int w = 0; w < kOffThreads / 32; ++w) {
             const unsigned long long u = warp_sum[w];
             if (w < warp) before += u;
-            sum += u;
+            total += u;
         }
-        if (i < t.nblocks) t.blk_off[i] = carry + before + inc - own;
-        carry += sum;
-        __syncthreads();  // warp_sum is written again by the next round
+        unsigned long long at = carry + before + inc - sum;
+#pragma unroll
+        for (int k = 0; k < kOffPer; ++k) {
+            if (first + k < nb) t.blk_off[first + k] = at;
+            at += own[k];
+        }
+        carry += total;
+        __syncthreads();  // warp_sum is written again by the next pass
     }
     if (tid == 0) {
-        t.blk_off[t.nblocks] = carry;
+        t.blk_off[nb] = carry;
         t.hdr->ovf_used = carry;
         if (s_missing) latch(t.hdr, LCT_ERR_CORRUPT);
         if (carry > t.ovf_cap) latch(t.hdr, LCT_ERR_OVERFLOW_CAPACITY);

@@ -456,7 +456,7 @@ __global__ void __launch_bounds__(kSgdBlock, SgdSmem<LEVEL, INPLACE, UpdateOp<OP
     // Overflow offset of this block: the single-pass decoupled look-back, or,
     // with deferred placement, a count published without waiting when the
     // block has nothing to place (k_block_offsets writes the offsets after).
-    const bool leave = a.deferred && total == 0;
+    const bool leave = a.deferred && total == 0 && !lookback_leader(b);
     if (warp == 0) {
         bool timed_out = false;
         unsigned long long excl = 0;

@@ -89,3 +89,19 @@ def test_compressed_linear_matches_dense_tiles(tile_blocks):
     full = x @ wd.t()
     assert torch.allclose(y.float(), full.float(), rtol=1e-2, atol=1e-2)
     assert ct.state().status == 0
+
+
+def test_compressed_linear_default_tile():
+    """Without a tile size the weight is decoded one wave of decode CTAs at a
+    time (here all 64 blocks at once): bit for bit the dense product on the
+    whole weight."""
+    out_f, in_f = 4096, 1024
+    w = synth.normal(out_f * in_f, 0.02, 13)
+    x = to_device(synth.normal(256 * in_f, 1.0, 14)).view(torch.bfloat16).reshape(256, in_f)
+    cb = B.lct_codebook_build(0, 0.02)
+    ct = B.CompressedTensor(w.size, 0)
+    B.lct_encode(to_device(w), cb, ct)
+    wd = to_device(w).view(torch.bfloat16).reshape(out_f, in_f)
+    y = compressed_linear(x, ct, cb, out_f, in_f)
+    torch.cuda.synchronize()
+    assert np.array_equal(_bits(y), _bits((wd @ x.t()).t()))

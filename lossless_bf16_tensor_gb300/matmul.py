@@ -41,9 +41,10 @@ def tile_rows(ct: B.CompressedTensor, in_features: int, tile_blocks: int) -> int
 def default_tile_blocks(w: B.CompressedTensor, in_features: int, device: torch.device) -> int:
     """A tile of about four blocks per SM (one full wave of decode CTAs),
     rounded down to whole rows, or the whole weight if that is smaller.  A
-    block's streams decode serially (about 40 us for a block alone on an SM on
-    a GB300), so a tile of a few blocks leaves most SMs idle and small tiles
-    cost far more than the GEMM they feed."""
+    block's streams decode serially (a decode launch of one block takes about
+    19 us on a GB300, of 608 blocks about 40 us), so a tile of a few blocks
+    leaves most SMs idle and small tiles cost far more than the GEMM they
+    feed."""
     idx = device.index if device.index is not None else torch.cuda.current_device()
     want = 4 * torch.cuda.get_device_properties(idx).multi_processor_count
     if want >= w.nblocks:

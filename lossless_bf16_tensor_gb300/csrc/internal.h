@@ -141,6 +141,8 @@ cudaError_t launch_momentum(const MomentumArgs &a, cudaStream_t s);
 // still wait for their exclusive prefix, and launch_block_offsets (after the
 // writer) writes every block offset, ovf_used and the capacity check.
 bool deferred_placement(uint32_t nblocks);
+// Grids of at most two blocks per SM (the launch is latency-bound).
+bool small_grid(uint32_t nblocks);
 cudaError_t launch_block_offsets(const DevTensor &t, cudaStream_t s);
 cudaError_t launch_block_offsets2(const DevTensor &t0, const DevTensor &t1, cudaStream_t s);  // same nblocks
 cudaError_t launch_wait_probe(lct_header *hdr, unsigned long long *work, uint64_t wait_ns,

@@ -92,6 +92,15 @@ bool deferred_placement(uint32_t nblocks)
     return (uint64_t)nblocks >= 4ull * (uint64_t)sms;
 }
 
+bool small_grid(uint32_t nblocks)
+{
+    int device = 0, sms = 0;
+    if (cudaGetDevice(&device) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess)
+        return false;
+    return (uint64_t)nblocks <= 2ull * (uint64_t)sms;
+}
+
 cudaError_t launch_block_offsets(const DevTensor &t, cudaStream_t s)
 {
     if (t.nblocks == 0) return cudaSuccess;

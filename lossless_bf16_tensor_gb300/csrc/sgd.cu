@@ -31,6 +31,7 @@ constexpr int kSgdThreads = 256;                 // consumer threads: one per st
 constexpr int kSgdBlock = kSgdThreads + 32;      // and one producer warp
 constexpr int kSgdRows = 8;        // rows per sign-fraction chunk
 constexpr int kSgdRowsClean = 8;   // rows per chunk out of place in CLEAN
+constexpr int kSgdRowsPipe = 16;   // rows per chunk of the software-pipelined small-grid kernel
 constexpr int kSgdSpill = 32;      // spilled new-exponent rows kept (out of place in CLEAN; 0 or a power of two)
 
 template <int OP>
@@ -67,7 +68,7 @@ struct UpdateOp<OP_ADAMW> {
     }
 };
 
-template <int LEVEL, bool INPLACE, int NIN>
+template <int LEVEL, bool INPLACE, int NIN, bool PIPE = false>
 struct SgdSmem {
     static constexpr int W = Geo<LEVEL>::W, NJ = Geo<LEVEL>::NJ;
     // Every spilled new exponent stays staged (at most NJ - 2W per stream, a
@@ -78,7 +79,7 @@ struct SgdSmem {
     static constexpr int kSpillRows = kKeepAll ? NJ - 2 * W : kSgdSpill;
     static constexpr int kStages = INPLACE ? 3 : 2;  // chunks in flight
     static constexpr int kSlotIn = (W + 1) * kStreams * 4;  // + zero guard row
-    static constexpr int kRows = kKeepAll ? kSgdRows : kSgdRowsClean;  // rows per chunk
+    static constexpr int kRows = PIPE ? kSgdRowsPipe : (kKeepAll ? kSgdRows : kSgdRowsClean);  // rows per chunk
     static constexpr int kRing = kStages * kRows * kStreams;  // per input
     static constexpr int kLuts = NIN * 256 * 4 + 256 * 8;
     static constexpr int kSpill = (kSpillRows * kRow + 127) / 128 * 128;
@@ -86,7 +87,7 @@ struct SgdSmem {
     // CTAs per SM the launch bounds ask for: as many as fit the SM's 228 KB
     // (1 KB of it reserved per CTA), at most 3 for the SGD and 2 for AdamW
     static constexpr int kFit = 228 * 1024 / (kBytes + 1024 + 256);
-    static constexpr int kWant = INPLACE ? 1 : (NIN == 2 ? 3 : 2);
+    static constexpr int kWant = INPLACE ? 1 : (PIPE ? 2 : (NIN == 2 ? 3 : 2));
     static constexpr int kCtas = kFit < kWant ? kFit : kWant;
     static_assert(kKeepAll || (kSgdSpill & (kSgdSpill - 1)) == 0, "ring index uses a mask");
     static_assert(kRows % 4 == 0, "four-row groups");
@@ -189,49 +190,60 @@ __device__ __forceinline__ void round_group(const uint32_t (&ev)[NIN][4], uint8_
     }
 }
 
-// Four rows of every stream on the fast path (every input symbol of the rows
-// lies in its slot).  The inputs' symbols are decoded two at a time with raw
+// The decoded symbols of one group of four rows: windows and entries per
+// input, the warp-wide OR of the entries (escape flags) and the old weight's
+// bits of these rows.
+template <int NIN>
+struct GroupIn {
+    uint32_t wv[NIN][4], ev[NIN][4], esc, bc;
+};
+
+// Four rows of every input stream, two symbols at a time, with raw
 // float-ready entries (the positions carry the entries' upper fields above
-// bit 9; the caller restores exact positions after the chunk).  A warp adds
-// escape literals, and canonicalises NaN, only when one of its lanes met an
-// escape or an exponent of 255 (or every group does when canon_all); with no
-// such symbol and finite inputs an SGD step cannot produce NaN.  When no new
-// exponent of the warp's streams differs from the old weight's, the new codes
-// are the old weight's codes bit for bit (same codebook, same stored shift),
-// so the rows' bits are appended straight from the old weight's stream
-// window.  Otherwise the new codes are looked up and appended, with the fit
-// check per value only when some stream of the warp may not keep all four.
-template <int W, int NIN, typename Op, bool KEEP_ALL, int SP>
-__device__ __forceinline__ void update_group(InStream (&in)[NIN], const uint32_t (&col_s)[NIN],
-                                             const uint32_t (&lut_s)[NIN], const Mul mul,
-                                             uint8_t *const (&sf_s)[NIN], uint32_t sf_at, const float *k,
-                                             bool canon_all, const uint2 *tbl, Writer &wo, uint32_t *colO,
-                                             uint8_t *sfo, uint8_t *ringj, uint32_t k0)
+// bit 9; the caller restores exact positions after the chunk).
+template <int NIN>
+__device__ __forceinline__ void decode_group(InStream (&in)[NIN], const uint32_t (&col_s)[NIN],
+                                             const uint32_t (&lut_s)[NIN], const Mul mul, GroupIn<NIN> &d)
 {
-    uint32_t wv[NIN][4], ev[NIN][4], esc = 0;
+    d.esc = 0;
     const uint32_t p0 = in[0].pos;
 #pragma unroll
     for (int q = 0; q < 2; ++q)
 #pragma unroll
         for (int i = 0; i < NIN; ++i) {
             Rd r{in[i].pos, col_s[i]};
-            rd_pair_f(r, lut_s[i], mul, wv[i][2 * q], wv[i][2 * q + 1], ev[i][2 * q], ev[i][2 * q + 1]);
+            rd_pair_f(r, lut_s[i], mul, d.wv[i][2 * q], d.wv[i][2 * q + 1], d.ev[i][2 * q], d.ev[i][2 * q + 1]);
             in[i].pos = r.p;
-            esc |= ev[i][2 * q] | ev[i][2 * q + 1];
+            d.esc |= d.ev[i][2 * q] | d.ev[i][2 * q + 1];
         }
-    uint32_t P[2], same = 0;
-    if (__any_sync(kFull, esc & kEntFlag) || canon_all) {
+    d.bc = (in[0].pos - p0) & 0x3FFu;
+}
+
+// Escape literals into the group's entries (a coded symbol's is a no-op).
+template <int NIN>
+__device__ __forceinline__ void fix_group(GroupIn<NIN> &d)
+{
 #pragma unroll
-        for (int i = 0; i < NIN; ++i)
+    for (int i = 0; i < NIN; ++i)
 #pragma unroll
-            for (int t = 0; t < 4; ++t) ev[i][t] = lit_fix_f(wv[i][t], ev[i][t]);
-        round_group<NIN, Op, true>(ev, sf_s, sf_at, k, mul.z, P, same, sfo);
-    } else {
-        round_group<NIN, Op, !Op::kNanFree>(ev, sf_s, sf_at, k, mul.z, P, same, sfo);
-    }
-    const uint32_t bc = (in[0].pos - p0) & 0x3FFu;  // the old weight's bits of these rows
+        for (int t = 0; t < 4; ++t) d.ev[i][t] = lit_fix_f(d.wv[i][t], d.ev[i][t]);
+}
+
+// The new codes of a group whose values are rounded (P, two BF16 per word;
+// `same` the difference from the old weight's values).  When no new exponent
+// of the warp's streams differs from the old weight's, the new codes are the
+// old weight's codes bit for bit (same codebook, same stored shift), so the
+// rows' bits are appended straight from the old weight's stream window.
+// Otherwise the new codes are looked up and appended, with the fit check per
+// value only when some stream of the warp may not keep all four.
+template <int NIN, typename Op, bool KEEP_ALL, int SP>
+__device__ __forceinline__ void write_group(const GroupIn<NIN> &d, const uint32_t (&P)[2], uint32_t same,
+                                            const uint2 *tbl, Writer &wo, uint32_t *colO, uint8_t *ringj,
+                                            uint32_t k0)
+{
+    const uint32_t bc = d.bc;
     if (Op::kTryCopy && __all_sync(kFull, wo.alive && !(same & 0x7F807F80u) && bc <= 32u && bc <= wo.rem)) {
-        wr_add(wo, make_uint2(wv[0][0] & ~(0xFFFFFFFFu >> bc), bc));
+        wr_add(wo, make_uint2(d.wv[0][0] & ~(0xFFFFFFFFu >> bc), bc));
         wr_flush(wo, colO);
         wo.rem -= bc;
         return;
@@ -260,14 +272,71 @@ __device__ __forceinline__ void update_group(InStream (&in)[NIN], const uint32_t
     }
 }
 
-template <int LEVEL, bool INPLACE, int OP>
-__global__ void __launch_bounds__(kSgdBlock, SgdSmem<LEVEL, INPLACE, UpdateOp<OP>::kInputs>::kCtas)
+// One fast-path chunk (every input symbol of its rows lies in its slot),
+// group by group.  A warp adds escape literals, and canonicalises NaN, only
+// when one of its lanes met an escape or an exponent of 255 (or every group
+// does when canon_all); with no such symbol and finite inputs an SGD step
+// cannot produce NaN.
+template <int W, int NIN, typename Op, bool KEEP_ALL, int SP, int G>
+__device__ __forceinline__ void update_chunk(InStream (&in)[NIN], const uint32_t (&col_s)[NIN],
+                                             const uint32_t (&lut_s)[NIN], const Mul mul,
+                                             uint8_t *const (&sf_s)[NIN], uint32_t sf_at, const float *k,
+                                             bool canon_all, const uint2 *tbl, Writer &wo, uint32_t *colO,
+                                             uint8_t *sfo, uint8_t *ringj, uint32_t k0)
+{
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+        GroupIn<NIN> d;
+        decode_group(in, col_s, lut_s, mul, d);
+        uint32_t P[2], same = 0;
+        if (__any_sync(kFull, d.esc & kEntFlag) || canon_all) {
+            fix_group(d);
+            round_group<NIN, Op, true>(d.ev, sf_s, sf_at + g * 4 * kStreams, k, mul.z, P, same, sfo + g * 4 * kStreams);
+        } else {
+            round_group<NIN, Op, !Op::kNanFree>(d.ev, sf_s, sf_at + g * 4 * kStreams, k, mul.z, P, same,
+                                                sfo + g * 4 * kStreams);
+        }
+        write_group<NIN, Op, KEEP_ALL, SP>(d, P, same, tbl, wo, colO, ringj, k0 + 4 * g);
+    }
+}
+
+// The same chunk software-pipelined for grids of at most two blocks per SM,
+// where a block's time is the latency of its streams' serial work: the next
+// group's symbols are decoded (and their literals added, unconditionally)
+// in the same straight-line code as this group's arithmetic and rounding
+// (NaN always canonicalised), so that a warp, which issues in order, overlaps
+// the two instead of waiting out the decode chain after every write.
+template <int W, int NIN, typename Op, bool KEEP_ALL, int SP, int G>
+__device__ __forceinline__ void update_chunk_pipelined(InStream (&in)[NIN], const uint32_t (&col_s)[NIN],
+                                                       const uint32_t (&lut_s)[NIN], const Mul mul,
+                                                       uint8_t *const (&sf_s)[NIN], uint32_t sf_at, const float *k,
+                                                       const uint2 *tbl, Writer &wo, uint32_t *colO, uint8_t *sfo,
+                                                       uint8_t *ringj, uint32_t k0)
+{
+    GroupIn<NIN> d[2];
+    decode_group(in, col_s, lut_s, mul, d[0]);
+    fix_group(d[0]);
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+        if (g + 1 < G) {
+            decode_group(in, col_s, lut_s, mul, d[(g + 1) & 1]);
+            fix_group(d[(g + 1) & 1]);
+        }
+        uint32_t P[2], same = 0;
+        round_group<NIN, Op, true>(d[g & 1].ev, sf_s, sf_at + g * 4 * kStreams, k, mul.z, P, same,
+                                   sfo + g * 4 * kStreams);
+        write_group<NIN, Op, KEEP_ALL, SP>(d[g & 1], P, same, tbl, wo, colO, ringj, k0 + 4 * g);
+    }
+}
+
+template <int LEVEL, bool INPLACE, int OP, bool PIPE>
+__global__ void __launch_bounds__(kSgdBlock, SgdSmem<LEVEL, INPLACE, UpdateOp<OP>::kInputs, PIPE>::kCtas)
     k_update(const __grid_constant__ UpdateArgs a)
 {
     using G = Geo<LEVEL>;
     using Op = UpdateOp<OP>;
     constexpr int NIN = Op::kInputs;
-    using L = SgdSmem<LEVEL, INPLACE, NIN>;
+    using L = SgdSmem<LEVEL, INPLACE, NIN, PIPE>;
     constexpr int W = G::W, R = L::kRows, S = L::kStages, SP = L::kSpillRows;
     constexpr int NW = kSgdThreads / 32;
     extern __shared__ __align__(128) uint8_t smem[];
@@ -411,11 +480,12 @@ __global__ void __launch_bounds__(kSgdBlock, SgdSmem<LEVEL, INPLACE, UpdateOp<OP
             uint32_t p_start[NIN];
 #pragma unroll
             for (int i = 0; i < NIN; ++i) p_start[i] = in[i].pos;
-#pragma unroll
-            for (int g = 0; g < R / 4; ++g)
-                update_group<W, NIN, Op, L::kKeepAll, SP>(in, col_s, lut_s, mul, sf_s, sf_at + g * 4 * kStreams + j,
-                                                          k, canon_all, tbl, wo, colO, sfo + g * 4 * kStreams,
-                                                          ringj, c * R + g * 4);
+            if (PIPE)
+                update_chunk_pipelined<W, NIN, Op, L::kKeepAll, SP, R / 4>(in, col_s, lut_s, mul, sf_s, sf_at + j, k,
+                                                                           tbl, wo, colO, sfo, ringj, c * R);
+            else
+                update_chunk<W, NIN, Op, L::kKeepAll, SP, R / 4>(in, col_s, lut_s, mul, sf_s, sf_at + j, k, canon_all,
+                                                                 tbl, wo, colO, sfo, ringj, c * R);
             // exact positions again: a chunk advances a stream by at most
             // R * 16 < 1024 bits, which the low 10 bits hold exactly
 #pragma unroll
@@ -528,16 +598,25 @@ __global__ void __launch_bounds__(kSgdBlock, SgdSmem<LEVEL, INPLACE, UpdateOp<OP
     }
 }
 
+template <int LEVEL, bool INPLACE, int OP, bool PIPE>
+cudaError_t launch_kernel(const UpdateArgs &b, cudaStream_t s)
+{
+    constexpr int smem = SgdSmem<LEVEL, INPLACE, UpdateOp<OP>::kInputs, PIPE>::kBytes;
+    const cudaError_t err =
+        cudaFuncSetAttribute(k_update<LEVEL, INPLACE, OP, PIPE>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (err != cudaSuccess) return err;
+    return launch_pdl(k_update<LEVEL, INPLACE, OP, PIPE>, dim3(b.w_out.nblocks), dim3(kSgdBlock), smem, s, b);
+}
+
 template <int LEVEL, bool INPLACE, int OP>
 cudaError_t launch_level(const UpdateArgs &a, cudaStream_t s)
 {
-    constexpr int smem = SgdSmem<LEVEL, INPLACE, UpdateOp<OP>::kInputs>::kBytes;
-    cudaError_t err =
-        cudaFuncSetAttribute(k_update<LEVEL, INPLACE, OP>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (err != cudaSuccess) return err;
     UpdateArgs b = a;
     b.deferred = deferred_placement(a.w_out.nblocks);
-    err = launch_pdl(k_update<LEVEL, INPLACE, OP>, dim3(a.w_out.nblocks), dim3(kSgdBlock), smem, s, b);
+    // grids of at most two blocks per SM run the software-pipelined SGD kernel
+    const bool pipe = OP == OP_SGD && small_grid(a.w_out.nblocks);
+    const cudaError_t err =
+        pipe ? launch_kernel<LEVEL, INPLACE, OP, true>(b, s) : launch_kernel<LEVEL, INPLACE, OP, false>(b, s);
     if (err != cudaSuccess || !b.deferred) return err;
     return launch_block_offsets(a.w_out, s);
 }

@@ -491,7 +491,35 @@ __global__ void __launch_bounds__(kSgdBlock, SgdSmem<LEVEL, INPLACE, UpdateOp<OP
 #pragma unroll
             for (int i = 0; i < NIN; ++i) in[i].pos = p_start[i] + ((in[i].pos - p_start[i]) & 0x3FFu);
         } else {
-            for (int r = 0; r < R; ++r) {
+            int r0 = 0;
+            if (bulk) {
+                // The groups of this chunk that end before the warp's first
+                // spilled input symbol still take the fast path, one by one;
+                // only the rows from there on go row by row.  (A stream whose
+                // input spilled reaches its marker in its last rows, so this
+                // keeps one such stream from slowing its whole warp's chunk.)
+                uint32_t first = in[0].marker;
+#pragma unroll
+                for (int i = 1; i < NIN; ++i) first = min(first, in[i].marker);
+                const uint32_t wmin = __reduce_min_sync(kFull, first);
+                const uint32_t fast = wmin > c * R ? min((wmin - c * R) / 4u, (uint32_t)(R / 4)) : 0u;
+                if (fast > 0) {
+                    const uint32_t sf_at = slot_c * R * kStreams;
+                    uint32_t p_start[NIN];
+#pragma unroll
+                    for (int i = 0; i < NIN; ++i) p_start[i] = in[i].pos;
+#pragma unroll 1
+                    for (uint32_t g = 0; g < fast; ++g)
+                        update_chunk<W, NIN, Op, L::kKeepAll, SP, 1>(in, col_s, lut_s, mul, sf_s,
+                                                                     sf_at + g * 4 * kStreams + j, k, canon_all, tbl,
+                                                                     wo, colO, sfo + g * 4 * kStreams, ringj,
+                                                                     c * R + 4 * g);
+#pragma unroll
+                    for (int i = 0; i < NIN; ++i) in[i].pos = p_start[i] + ((in[i].pos - p_start[i]) & 0x3FFu);
+                    r0 = 4 * (int)fast;
+                }
+            }
+            for (int r = r0; r < R; ++r) {
                 const uint32_t kk = c * R + r;
                 if (kk >= nj) break;
                 const uint64_t at = base + (uint64_t)kk * kStreams + j;
@@ -614,9 +642,12 @@ cudaError_t launch_level(const UpdateArgs &a, cudaStream_t s)
     UpdateArgs b = a;
     b.deferred = deferred_placement(a.w_out.nblocks);
     // grids of at most two blocks per SM run the software-pipelined SGD kernel
-    const bool pipe = OP == OP_SGD && small_grid(a.w_out.nblocks);
-    const cudaError_t err =
-        pipe ? launch_kernel<LEVEL, INPLACE, OP, true>(b, s) : launch_kernel<LEVEL, INPLACE, OP, false>(b, s);
+    cudaError_t err;
+    if constexpr (OP == OP_SGD)
+        err = small_grid(a.w_out.nblocks) ? launch_kernel<LEVEL, INPLACE, OP, true>(b, s)
+                                          : launch_kernel<LEVEL, INPLACE, OP, false>(b, s);
+    else
+        err = launch_kernel<LEVEL, INPLACE, OP, false>(b, s);
     if (err != cudaSuccess || !b.deferred) return err;
     return launch_block_offsets(a.w_out, s);
 }

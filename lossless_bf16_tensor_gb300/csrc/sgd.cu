@@ -14,14 +14,20 @@
 // per row it decodes one symbol of each input, updates the value, writes its
 // sign-fraction byte and appends its exponent to the new slot, whose words go
 // straight to global memory.  The slot images of the inputs come in by TMA
-// bulk copy; their sign-fraction bytes stream through a ring of row chunks.
-// A chunk in which no stream of a warp reaches a spill marker and every new
-// slot has room takes a fast path with no per-value checks.  A code is at
-// most 16 bits, so a stream holds at least 2W symbols of its slot and spills
-// at most NJ - 2W.  That many spilled new exponents are kept in place and for
-// the 128-row levels (MEDIUM, HIGH).  Out of place in CLEAN 32 rows are kept
-// (three CTAs per SM for the SGD), and a stream that spills more than that
-// re-decodes its older rows at the end.
+// bulk copy; their sign-fraction bytes stream through a ring of row chunks
+// that a producer warp keeps filled.  Rows go in groups of four: a group in
+// which no input symbol of a warp's streams lies past its spill marker takes
+// a fast path (symbols decoded two at a time, values rounded two at a time,
+// the fit check per value only when some new slot may not hold the group);
+// the rows from a warp's first spilled input symbol on go row by row.  A code
+// is at most 16 bits, so a stream holds at least 2W symbols of its slot and
+// spills at most NJ - 2W.  That many spilled new exponents are kept in place
+// and for the 128-row levels (MEDIUM, HIGH).  Out of place in CLEAN 32 rows
+// are kept (three CTAs per SM for the SGD), and a stream that spills more
+// than that re-decodes its older rows at the end.  Grids of at most two
+// blocks per SM run a software-pipelined instantiation of the SGD (16-row
+// chunks, two CTAs per SM), where a block's latency, not the SM's
+// throughput, sets the time.
 #include "codec_dev.cuh"
 
 namespace lct {

@@ -122,26 +122,6 @@ __device__ __forceinline__ uint32_t rd_take(uint32_t &p, const uint32_t *__restr
     return ent | esc_literal(win, ent);
 }
 
-// Two symbols of a stream from one 32-bit window: a symbol (escape and
-// literal included) is at most 16 bits, so after the first one the window
-// still holds the whole second one.  Both symbols must lie in the slot (the
-// caller has checked the marker).  Same results as two rd_take calls.
-template <int W>
-__device__ __forceinline__ void rd_take2(uint32_t &p, const uint32_t *__restrict__ col,
-                                         const uint32_t *__restrict__ lut, uint32_t &e0, uint32_t &e1)
-{
-    const uint32_t w = min(p >> 5, (uint32_t)(W - 1));
-    const uint32_t hi = col[w * kStreams], lo = col[(w + 1) * kStreams];
-    const uint32_t win = __funnelshift_l(lo, hi, p);  // the next 32 bits
-    const uint32_t ent0 = lut[win >> 24];
-    const uint32_t l0 = ent0 >> 27;
-    e0 = ent0 | esc_literal(win, ent0);
-    const uint32_t win1 = win << l0;
-    const uint32_t ent1 = lut[win1 >> 24];
-    e1 = ent1 | esc_literal(win1, ent1);
-    p += l0 + (ent1 >> 27);
-}
-
 // ------------------------------------------- pair reader, deferred literal
 
 // Shared-memory loads by 32-bit shared address.
@@ -319,9 +299,9 @@ __device__ __forceinline__ uint32_t sf_of2(uint32_t p) { return ((p >> 8) & 0x00
 // symbol's index is the marker.  Every append (of at most 32 bits) is
 // followed by a flush, so before an append fewer than 32 bits are pending and
 // they all sit in `hi`; an append ORs the code's head into `hi` and leaves the
-// bits that run past the word in `lo`, which a flush moves up.  `rem` is kept
-// exact only on the checked path (wr_fix_rem restores it after unchecked
-// appends).
+// bits that run past the word in `lo`, which a flush moves up.  `rem`, the
+// bits the slot still has room for, is kept exact: the unchecked paths
+// subtract what they appended.
 struct Writer {
     uint32_t hi, lo, nbits, wi, rem, marker;
     bool alive;
@@ -363,12 +343,6 @@ __device__ __forceinline__ void wr_flush(Writer &w, uint32_t *__restrict__ col)
         w.hi = w.lo;
         w.nbits -= 32u;
     }
-}
-
-template <int W>
-__device__ __forceinline__ void wr_fix_rem(Writer &w)
-{
-    w.rem = 32u * W - 32u * w.wi - w.nbits;
 }
 
 // Append with the fit check; returns true when symbol k spilled (it, and

@@ -98,6 +98,33 @@ def test_sgd_worst_case_spill(level, in_place):
     assert_same_format(got, ref)
 
 
+@pytest.mark.parametrize("level", [0, 1, 2])
+@pytest.mark.parametrize("in_place", [False, True])
+def test_sgd_spill_on_a_grid_of_more_than_two_blocks_per_sm(level, in_place):
+    """The worst-case spill data above on a grid of 2 * SMs + 40 blocks, which
+    runs the SGD kernel built for throughput (three CTAs per SM out of place)
+    instead of the software-pipelined one the small tests above reach; the
+    blocks that spill are spread over the grid."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    bsz = 65536 if level == 0 else 32768
+    nblocks = 2 * sms + 40
+    n = nblocks * bsz - 777
+    w = synth.normal(n, 0.02, 31)
+    for b in (0, nblocks // 3, nblocks - 1):  # blocks of NaN and of random bit patterns
+        w[b * bsz:b * bsz + bsz // 2] = synth.random_bits(bsz // 2, 32 + b)
+    w[bsz // 2:bsz] = 0x7FC1
+    m = synth.normal(n, 1e-3, 4)
+    W, M, cbw, cbm, oW, oM, ocbw, ocbm = _setup(w, m, level)
+    ref = oracle.sgd_step(oW, ocbw, oM, ocbm, ETA)
+    assert ref.ovf_used > 0
+    out = B.CompressedTensor(n, level, like=W) if in_place else B.CompressedTensor(n, level)
+    B.lct_sgd_step_fused(W, cbw, M, cbm, ETA, out)
+    torch.cuda.synchronize()
+    got = out.to_host()
+    assert got["status"] == ref.status == 0
+    assert_same_format(got, ref)
+
+
 def test_sgd_162m_step_one_full_and_sampled_steps():
     """162,000,000-value W ~ N(0, 0.02) and M ~ N(0, 1e-3), CLEAN, eta = 1e-3,
     100 steps on the GPU with ping-pong overflow buffers.  Step 1 is compared

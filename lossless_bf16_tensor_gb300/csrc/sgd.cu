@@ -24,10 +24,10 @@
 // spills at most NJ - 2W.  That many spilled new exponents are kept in place
 // and for the 128-row levels (MEDIUM, HIGH).  Out of place in CLEAN 32 rows
 // are kept (three CTAs per SM for the SGD), and a stream that spills more
-// than that re-decodes its older rows at the end.  Grids of at most two
-// blocks per SM run a software-pipelined instantiation of the SGD (16-row
-// chunks, two CTAs per SM), where a block's latency, not the SM's
-// throughput, sets the time.
+// than that re-decodes its older rows at the end.  Where a block's latency,
+// not the SM's throughput, sets the time -- grids of at most two blocks per
+// SM for the SGD, and every in-place step (one CTA per SM) -- a
+// software-pipelined instantiation runs (16-row chunks).
 #include "codec_dev.cuh"
 
 namespace lct {
@@ -647,11 +647,14 @@ cudaError_t launch_level(const UpdateArgs &a, cudaStream_t s)
 {
     UpdateArgs b = a;
     b.deferred = deferred_placement(a.w_out.nblocks);
-    // grids of at most two blocks per SM run the software-pipelined SGD kernel
+    // The software-pipelined kernel runs where a block's latency sets the
+    // time: grids of at most two blocks per SM (the SGD) and every step that
+    // runs one CTA per SM anyway (in place).
     cudaError_t err;
-    if constexpr (OP == OP_SGD)
-        err = small_grid(a.w_out.nblocks) ? launch_kernel<LEVEL, INPLACE, OP, true>(b, s)
-                                          : launch_kernel<LEVEL, INPLACE, OP, false>(b, s);
+    constexpr bool one_cta = SgdSmem<LEVEL, INPLACE, UpdateOp<OP>::kInputs, false>::kCtas == 1;
+    if constexpr (OP == OP_SGD || one_cta)
+        err = (one_cta || small_grid(a.w_out.nblocks)) ? launch_kernel<LEVEL, INPLACE, OP, true>(b, s)
+                                                       : launch_kernel<LEVEL, INPLACE, OP, false>(b, s);
     else
         err = launch_kernel<LEVEL, INPLACE, OP, false>(b, s);
     if (err != cudaSuccess || !b.deferred) return err;

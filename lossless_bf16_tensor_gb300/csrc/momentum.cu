@@ -229,54 +229,63 @@ __device__ __forceinline__ void mom_put4(Writer &wo, const uint32_t (&p)[2], con
     }
 }
 
-// Four rows of every stream on the fast path (every symbol of both inputs in
-// its slot): both inputs decoded two symbols at a time with the escape
-// literals deferred, both new states rounded two values at a time, their
-// sign-fraction bytes written and their codes appended.  The first state's
-// new codes are its old ones bit for bit when no new exponent of the warp's
-// streams differs (same codebook, same stored shift): then its rows' bits
-// are appended straight from the old stream window.
-template <int OP, int SP>
-__device__ __forceinline__ void mom_group(MomIn &sw, MomIn &sm, const uint32_t colw_s, const uint32_t colm_s,
-                                          const uint32_t lutw_s, const uint32_t lutm_s, const Mul mul,
-                                          const uint8_t *sfwc, const uint8_t *sfmc, const uint16_t *gc, const float *kc,
-                                          Writer &ow, Writer &om, const uint2 *tblW, const uint2 *tblM,
-                                          uint32_t *colW, uint32_t *colM, uint8_t *sfWo, uint8_t *sfMo,
-                                          uint8_t *stageW, uint8_t *stageM, uint32_t k0)
+// The decoded symbols of one group of four rows of both inputs: windows and
+// entries, the warp-wide OR of the entries (escape flags) and the first
+// state's old bits of these rows.
+struct MomGroupIn {
+    uint32_t wvw[4], evw[4], wvm[4], evm[4], esc, bc;
+};
+
+// Four rows of both input streams, two symbols at a time, escape literals
+// left out.
+__device__ __forceinline__ void mom_decode(MomIn &sw, MomIn &sm, const uint32_t colw_s, const uint32_t colm_s,
+                                           const uint32_t lutw_s, const uint32_t lutm_s, const Mul mul, MomGroupIn &d)
 {
-    using Op2 = TwoStateOp2<OP>;
-    uint32_t fw[4], fm[4], gv[4];
-#pragma unroll
-    for (int t = 0; t < 4; ++t) {
-        fw[t] = sfwc[t * kStreams];
-        fm[t] = sfmc[t * kStreams];
-        gv[t] = gc[t * kStreams];
-    }
-    uint32_t wvw[4], evw[4], wvm[4], evm[4], esc = 0;
+    d.esc = 0;
     const uint32_t p0 = sw.pos;
 #pragma unroll
     for (int q = 0; q < 2; ++q) {
         Rd rw{sw.pos, colw_s}, rm{sm.pos, colm_s};
-        rd_pair(rw, lutw_s, mul, wvw[2 * q], wvw[2 * q + 1], evw[2 * q], evw[2 * q + 1]);
-        rd_pair(rm, lutm_s, mul, wvm[2 * q], wvm[2 * q + 1], evm[2 * q], evm[2 * q + 1]);
+        rd_pair(rw, lutw_s, mul, d.wvw[2 * q], d.wvw[2 * q + 1], d.evw[2 * q], d.evw[2 * q + 1]);
+        rd_pair(rm, lutm_s, mul, d.wvm[2 * q], d.wvm[2 * q + 1], d.evm[2 * q], d.evm[2 * q + 1]);
         sw.pos = rw.p;
         sm.pos = rm.p;
-        esc |= evw[2 * q] | evw[2 * q + 1] | evm[2 * q] | evm[2 * q + 1];
+        d.esc |= d.evw[2 * q] | d.evw[2 * q + 1] | d.evm[2 * q] | d.evm[2 * q + 1];
     }
-    if (__any_sync(kFull, esc_bits(esc))) {
+    d.bc = sw.pos - p0;
+}
+
+// Escape literals into the group's entries (a coded symbol's is a no-op).
+__device__ __forceinline__ void mom_fix(MomGroupIn &d)
+{
 #pragma unroll
-        for (int t = 0; t < 4; ++t) {
-            evw[t] = lit_fix(wvw[t], evw[t]);
-            evm[t] = lit_fix(wvm[t], evm[t]);
-        }
+    for (int t = 0; t < 4; ++t) {
+        d.evw[t] = lit_fix(d.wvw[t], d.evw[t]);
+        d.evm[t] = lit_fix(d.wvm[t], d.evm[t]);
     }
-    const uint32_t bc = sw.pos - p0;  // the first state's old bits of these rows
+}
+
+// One decoded group (literals added): both new states rounded two values at
+// a time, their sign-fraction bytes written and their codes appended.  The
+// first state's new codes are its old ones bit for bit when no new exponent
+// of the warp's streams differs (same codebook, same stored shift): then its
+// rows' bits are appended straight from the old stream window.
+template <int OP, int SP>
+__device__ __forceinline__ void mom_finish(const MomGroupIn &d, const uint8_t *sfwc, const uint8_t *sfmc,
+                                           const uint16_t *gc, const float *kc, Writer &ow, Writer &om,
+                                           const uint2 *tblW, const uint2 *tblM, uint32_t *colW, uint32_t *colM,
+                                           uint8_t *sfWo, uint8_t *sfMo, uint8_t *stageW, uint8_t *stageM,
+                                           uint32_t k0)
+{
+    using Op2 = TwoStateOp2<OP>;
     uint32_t pa[2], pb[2], same = 0;
 #pragma unroll
     for (int q = 0; q < 2; ++q) {
-        const uint32_t xa[2] = {join_one(fw[2 * q], evw[2 * q]), join_one(fw[2 * q + 1], evw[2 * q + 1])};
-        const uint32_t xb[2] = {join_one(fm[2 * q], evm[2 * q]), join_one(fm[2 * q + 1], evm[2 * q + 1])};
-        const uint32_t g2[2] = {gv[2 * q], gv[2 * q + 1]};
+        const uint32_t xa[2] = {join_one(sfwc[(2 * q) * kStreams], d.evw[2 * q]),
+                                join_one(sfwc[(2 * q + 1) * kStreams], d.evw[2 * q + 1])};
+        const uint32_t xb[2] = {join_one(sfmc[(2 * q) * kStreams], d.evm[2 * q]),
+                                join_one(sfmc[(2 * q + 1) * kStreams], d.evm[2 * q + 1])};
+        const uint32_t g2[2] = {gc[(2 * q) * kStreams], gc[(2 * q + 1) * kStreams]};
         Op2::apply(xa, xb, g2, kc, pa[q], pb[q]);
         if (OP == OP2_MOMENTUM) same |= pa[q] ^ __byte_perm(xa[0], xa[1], 0x5410);
         const uint32_t sa = sf_of2(pa[q]), sb = sf_of2(pb[q]);
@@ -288,14 +297,61 @@ __device__ __forceinline__ void mom_group(MomIn &sw, MomIn &sm, const uint32_t c
     // A weight moves by a small step, so its exponents mostly stay; AdamW's
     // first moment is re-weighted every step and nearly always changes.
     constexpr bool kTryCopy = OP == OP2_MOMENTUM;
+    const uint32_t bc = d.bc;
     if (kTryCopy && __all_sync(kFull, ow.alive && !(same & 0x7F807F80u) && bc <= 32u && bc <= ow.rem)) {
-        wr_add(ow, make_uint2(wvw[0] & ~(0xFFFFFFFFu >> bc), bc));
+        wr_add(ow, make_uint2(d.wvw[0] & ~(0xFFFFFFFFu >> bc), bc));
         wr_flush(ow, colW);
         ow.rem -= bc;
     } else {
         mom_put4<SP>(ow, pa, tblW, k0, colW, stageW);
     }
     mom_put4<SP>(om, pb, tblM, k0, colM, stageM);
+}
+
+// Four rows of every stream on the fast path (every symbol of both inputs in
+// its slot): decoded two symbols at a time with the escape literals added
+// only when a lane of the warp met an escape, then finished.
+template <int OP, int SP>
+__device__ __forceinline__ void mom_group(MomIn &sw, MomIn &sm, const uint32_t colw_s, const uint32_t colm_s,
+                                          const uint32_t lutw_s, const uint32_t lutm_s, const Mul mul,
+                                          const uint8_t *sfwc, const uint8_t *sfmc, const uint16_t *gc, const float *kc,
+                                          Writer &ow, Writer &om, const uint2 *tblW, const uint2 *tblM,
+                                          uint32_t *colW, uint32_t *colM, uint8_t *sfWo, uint8_t *sfMo,
+                                          uint8_t *stageW, uint8_t *stageM, uint32_t k0)
+{
+    MomGroupIn d;
+    mom_decode(sw, sm, colw_s, colm_s, lutw_s, lutm_s, mul, d);
+    if (__any_sync(kFull, esc_bits(d.esc))) mom_fix(d);
+    mom_finish<OP, SP>(d, sfwc, sfmc, gc, kc, ow, om, tblW, tblM, colW, colM, sfWo, sfMo, stageW, stageM, k0);
+}
+
+// A fast-path chunk of G groups software-pipelined, for the in-place kernel
+// (one CTA per SM, where a block's latency sets the time): the next group's
+// symbols are decoded (and their literals added, unconditionally) in the
+// same straight-line code as this group's arithmetic and rounding, so that a
+// warp, which issues in order, overlaps the two.
+template <int OP, int SP, int G>
+__device__ __forceinline__ void mom_chunk_pipelined(MomIn &sw, MomIn &sm, const uint32_t colw_s,
+                                                    const uint32_t colm_s, const uint32_t lutw_s,
+                                                    const uint32_t lutm_s, const Mul mul, const uint8_t *sfwc,
+                                                    const uint8_t *sfmc, const uint16_t *gc, const float *kc,
+                                                    Writer &ow, Writer &om, const uint2 *tblW, const uint2 *tblM,
+                                                    uint32_t *colW, uint32_t *colM, uint8_t *sfWo, uint8_t *sfMo,
+                                                    uint8_t *stageW, uint8_t *stageM, uint32_t k0)
+{
+    MomGroupIn d[2];
+    mom_decode(sw, sm, colw_s, colm_s, lutw_s, lutm_s, mul, d[0]);
+    mom_fix(d[0]);
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+        if (g + 1 < G) {
+            mom_decode(sw, sm, colw_s, colm_s, lutw_s, lutm_s, mul, d[(g + 1) & 1]);
+            mom_fix(d[(g + 1) & 1]);
+        }
+        mom_finish<OP, SP>(d[g & 1], sfwc + g * 4 * kStreams, sfmc + g * 4 * kStreams, gc + g * 4 * kStreams, kc, ow,
+                           om, tblW, tblM, colW, colM, sfWo + g * 4 * kStreams, sfMo + g * 4 * kStreams, stageW,
+                           stageM, k0 + 4 * g);
+    }
 }
 
 template <int LEVEL, bool INPLACE, int OP>
@@ -438,12 +494,18 @@ __global__ void __launch_bounds__(kMomBlock, INPLACE ? 1 : 2) k_momentum(const _
         const uint64_t row0 = (uint64_t)c * kRowsB;
         const uint32_t k0 = c * R, kend = k0 + R;
         if (bulk && __all_sync(kFull, sw.marker >= kend && sm.marker >= kend)) {
+            if (INPLACE) {
+                mom_chunk_pipelined<OP, SP, R / 4>(sw, sm, colw_s, colm_s, lutw_s, lutm_s, mul, sfwc, sfmc, gc, kc, ow,
+                                                   om, tblW, tblM, colW, colM, sfWj + row0, sfMj + row0, stageW + j,
+                                                   stageM + j, k0);
+            } else {
 #pragma unroll
-            for (int g = 0; g < R / 4; ++g)
-                mom_group<OP, SP>(sw, sm, colw_s, colm_s, lutw_s, lutm_s, mul, sfwc + g * 4 * kStreams,
-                                  sfmc + g * 4 * kStreams, gc + g * 4 * kStreams, kc, ow, om, tblW, tblM, colW, colM,
-                                  sfWj + row0 + g * 4 * kStreams, sfMj + row0 + g * 4 * kStreams, stageW + j,
-                                  stageM + j, k0 + g * 4);
+                for (int g = 0; g < R / 4; ++g)
+                    mom_group<OP, SP>(sw, sm, colw_s, colm_s, lutw_s, lutm_s, mul, sfwc + g * 4 * kStreams,
+                                      sfmc + g * 4 * kStreams, gc + g * 4 * kStreams, kc, ow, om, tblW, tblM, colW,
+                                      colM, sfWj + row0 + g * 4 * kStreams, sfMj + row0 + g * 4 * kStreams,
+                                      stageW + j, stageM + j, k0 + g * 4);
+            }
         } else {
             for (int r = 0; r < R; ++r) {
                 const uint32_t k = k0 + r;

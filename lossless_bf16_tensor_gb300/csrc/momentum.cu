@@ -308,28 +308,12 @@ __device__ __forceinline__ void mom_finish(const MomGroupIn &d, const uint8_t *s
     mom_put4<SP>(om, pb, tblM, k0, colM, stageM);
 }
 
-// Four rows of every stream on the fast path (every symbol of both inputs in
-// its slot): decoded two symbols at a time with the escape literals added
-// only when a lane of the warp met an escape, then finished.
-template <int OP, int SP>
-__device__ __forceinline__ void mom_group(MomIn &sw, MomIn &sm, const uint32_t colw_s, const uint32_t colm_s,
-                                          const uint32_t lutw_s, const uint32_t lutm_s, const Mul mul,
-                                          const uint8_t *sfwc, const uint8_t *sfmc, const uint16_t *gc, const float *kc,
-                                          Writer &ow, Writer &om, const uint2 *tblW, const uint2 *tblM,
-                                          uint32_t *colW, uint32_t *colM, uint8_t *sfWo, uint8_t *sfMo,
-                                          uint8_t *stageW, uint8_t *stageM, uint32_t k0)
-{
-    MomGroupIn d;
-    mom_decode(sw, sm, colw_s, colm_s, lutw_s, lutm_s, mul, d);
-    if (__any_sync(kFull, esc_bits(d.esc))) mom_fix(d);
-    mom_finish<OP, SP>(d, sfwc, sfmc, gc, kc, ow, om, tblW, tblM, colW, colM, sfWo, sfMo, stageW, stageM, k0);
-}
-
-// A fast-path chunk of G groups software-pipelined, for the in-place kernel
-// (one CTA per SM, where a block's latency sets the time): the next group's
-// symbols are decoded (and their literals added, unconditionally) in the
-// same straight-line code as this group's arithmetic and rounding, so that a
-// warp, which issues in order, overlaps the two.
+// A fast-path chunk of G groups (every symbol of both inputs in its slot),
+// software-pipelined: the next group's symbols are decoded (and their
+// literals added, unconditionally) in the same straight-line code as this
+// group's arithmetic and rounding, so that a warp, which issues in order,
+// overlaps the two.  The kernel runs one CTA per SM in place and two out of
+// place, where a block's latency weighs on the time.
 template <int OP, int SP, int G>
 __device__ __forceinline__ void mom_chunk_pipelined(MomIn &sw, MomIn &sm, const uint32_t colw_s,
                                                     const uint32_t colm_s, const uint32_t lutw_s,
@@ -494,18 +478,9 @@ __global__ void __launch_bounds__(kMomBlock, INPLACE ? 1 : 2) k_momentum(const _
         const uint64_t row0 = (uint64_t)c * kRowsB;
         const uint32_t k0 = c * R, kend = k0 + R;
         if (bulk && __all_sync(kFull, sw.marker >= kend && sm.marker >= kend)) {
-            if (INPLACE) {
-                mom_chunk_pipelined<OP, SP, R / 4>(sw, sm, colw_s, colm_s, lutw_s, lutm_s, mul, sfwc, sfmc, gc, kc, ow,
-                                                   om, tblW, tblM, colW, colM, sfWj + row0, sfMj + row0, stageW + j,
-                                                   stageM + j, k0);
-            } else {
-#pragma unroll
-                for (int g = 0; g < R / 4; ++g)
-                    mom_group<OP, SP>(sw, sm, colw_s, colm_s, lutw_s, lutm_s, mul, sfwc + g * 4 * kStreams,
-                                      sfmc + g * 4 * kStreams, gc + g * 4 * kStreams, kc, ow, om, tblW, tblM, colW,
-                                      colM, sfWj + row0 + g * 4 * kStreams, sfMj + row0 + g * 4 * kStreams,
-                                      stageW + j, stageM + j, k0 + g * 4);
-            }
+            mom_chunk_pipelined<OP, SP, R / 4>(sw, sm, colw_s, colm_s, lutw_s, lutm_s, mul, sfwc, sfmc, gc, kc, ow, om,
+                                               tblW, tblM, colW, colM, sfWj + row0, sfMj + row0, stageW + j,
+                                               stageM + j, k0);
         } else {
             for (int r = 0; r < R; ++r) {
                 const uint32_t k = k0 + r;

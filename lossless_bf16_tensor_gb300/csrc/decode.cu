@@ -26,8 +26,9 @@ struct DecodeSmem {
     static constexpr int kSlot = (W + 1) * kStreams * 4;  // slot image + zero guard row
     static constexpr int kRing = kDecRing * kDecRows * kStreams;
     static constexpr int kLut = 256 * 2;
-    static constexpr int kBytes = kSlot + kRing + kLut;
-    static_assert(kBytes >= 33 * 1024, "the pair reader's reads stay inside the CTA");
+    // the readers' reads (word indices modulo 32, up to three words ahead)
+    // stay inside the CTA's shared memory: at least 35 KB from the slot image on
+    static constexpr int kBytes = kSlot + kRing + kLut < 35 * 1024 ? 35 * 1024 : kSlot + kRing + kLut;
     static_assert(kDecRows % 8 == 0, "eight-row groups");
 };
 
@@ -91,8 +92,33 @@ __device__ __forceinline__ uint32_t rd_take16(uint32_t &p, const uint32_t *__res
     return lit_fix16(win, ent);
 }
 
-template <int LEVEL>
-__global__ void __launch_bounds__(kDecThreads, 4) k_decode(const __grid_constant__ DecodeArgs a)
+// Two symbols with the stream's next three slot words held in registers
+// (w0 = word p/32, w1, w2), for grids of at most two blocks per SM where the
+// reader's dependent chain sets a block's time: the window needs no shared
+// load on the chain.  The word after the three is loaded at the start of the
+// pair (its address is known then) and shifted in when the pair crosses a
+// word boundary (a pair is at most 32 bits, so it crosses at most one).
+// Word indices are taken modulo 32 as in rd_pair; the load of the fourth
+// word reaches at most 35 words past the column's start.
+__device__ __forceinline__ void rd_pair16_w3(uint32_t &p, uint32_t &w0, uint32_t &w1, uint32_t &w2, uint32_t col,
+                                             uint32_t lut, const Mul m, uint32_t &win0, uint32_t &win1,
+                                             uint32_t &ent0, uint32_t &ent1)
+{
+    const uint32_t w3 = lds32(imad(p & 0x3E0u, m.x, col) + 3u * kStreams * 4u);
+    win0 = __funnelshift_l(w1, w0, p);
+    ent0 = lds16(imad(win0 >> 24, m.z, lut));
+    win1 = __funnelshift_l(0u, win0, ent0);
+    ent1 = lds16(imad(win1 >> 24, m.z, lut));
+    const uint32_t q = p + (ent0 & 31u) + (ent1 & 31u);
+    const bool cross = ((p ^ q) & 32u) != 0u;
+    w0 = cross ? w1 : w0;
+    w1 = cross ? w2 : w1;
+    w2 = cross ? w3 : w2;
+    p = q;
+}
+
+template <int LEVEL, bool WIN3>
+__global__ void __launch_bounds__(kDecThreads, WIN3 ? 2 : 4) k_decode(const __grid_constant__ DecodeArgs a)
 {
     using G = Geo<LEVEL>;
     using L = DecodeSmem<LEVEL>;
@@ -174,14 +200,26 @@ __global__ void __launch_bounds__(kDecThreads, 4) k_decode(const __grid_constant
             // eight rows at a time: the symbols two by two with the escape
             // literals deferred (added only when a lane of the warp met an
             // escape), then the sign-fraction bytes and the joined values
+            uint32_t x0 = 0, x1 = 0, x2 = 0;  // WIN3: slot words pos/32 .. pos/32 + 2
+            if (WIN3) {
+                const uint32_t a0 = imad(pos & 0x3E0u, mul.x, col_s);
+                x0 = lds32(a0);
+                x1 = lds32(a0 + kStreams * 4);
+                x2 = lds32(a0 + 2 * kStreams * 4);
+            }
 #pragma unroll
             for (int g = 0; g < R / 8; ++g) {
                 uint32_t wv[8], ev[8], esc = 0;
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
-                    Rd r{pos, col_s};
-                    rd_pair16(r, lut_s, mul, wv[2 * q], wv[2 * q + 1], ev[2 * q], ev[2 * q + 1]);
-                    pos = r.p;
+                    if (WIN3) {
+                        rd_pair16_w3(pos, x0, x1, x2, col_s, lut_s, mul, wv[2 * q], wv[2 * q + 1], ev[2 * q],
+                                     ev[2 * q + 1]);
+                    } else {
+                        Rd r{pos, col_s};
+                        rd_pair16(r, lut_s, mul, wv[2 * q], wv[2 * q + 1], ev[2 * q], ev[2 * q + 1]);
+                        pos = r.p;
+                    }
                     esc |= ev[2 * q] | ev[2 * q + 1];
                 }
                 if (__any_sync(kFull, esc & 0x8000u)) {
@@ -232,13 +270,21 @@ __global__ void __launch_bounds__(kDecThreads, 4) k_decode(const __grid_constant
     }
 }
 
+template <int LEVEL, bool WIN3>
+cudaError_t launch_kernel(const DecodeArgs &a, uint32_t nblocks, cudaStream_t s)
+{
+    constexpr int smem = DecodeSmem<LEVEL>::kBytes;
+    cudaError_t err = cudaFuncSetAttribute(k_decode<LEVEL, WIN3>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (err != cudaSuccess) return err;
+    return launch_pdl(k_decode<LEVEL, WIN3>, dim3(nblocks), dim3(kDecThreads), smem, s, a);
+}
+
+// Grids of at most two blocks per SM take the register-window reader (two
+// CTAs per SM, more registers): there a block's latency sets the time.
 template <int LEVEL>
 cudaError_t launch_level(const DecodeArgs &a, uint32_t nblocks, cudaStream_t s)
 {
-    constexpr int smem = DecodeSmem<LEVEL>::kBytes;
-    cudaError_t err = cudaFuncSetAttribute(k_decode<LEVEL>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (err != cudaSuccess) return err;
-    return launch_pdl(k_decode<LEVEL>, dim3(nblocks), dim3(kDecThreads), smem, s, a);
+    return small_grid(nblocks) ? launch_kernel<LEVEL, true>(a, nblocks, s) : launch_kernel<LEVEL, false>(a, nblocks, s);
 }
 
 }  // namespace dev

@@ -590,6 +590,9 @@ def run_sgd_config(B, synth, timer, stream, peak, w_np, wl, n, level):
     def one():
         B.lct_sgd_step_fused(Ws[k[0] % 2], cbw, M, cbm, eta, Ws[(k[0] + 1) % 2], stream)
         k[0] += 1
+    for _ in range(2):  # untimed: the kernel's first launch also loads its code
+        one()
+    torch.cuda.synchronize()
     t = timer(one, steps)
     torch.cuda.synchronize()
     cur = Ws[k[0] % 2]

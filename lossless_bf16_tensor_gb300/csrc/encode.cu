@@ -21,14 +21,15 @@ namespace lct {
 namespace dev {
 
 constexpr int kEncThreads = 256;
-constexpr int kEncRows = 16;    // rows per input chunk
+constexpr int kEncRows = 16;    // rows per input chunk (4 CTAs per SM)
+constexpr int kEncRowsSmall = 32;  // rows per input chunk on grids of at most two blocks per SM
 constexpr int kEncRing = 2;     // chunks in flight
 constexpr int kSpillRows = 32;  // spilled-exponent rows kept
 
-template <int LEVEL>
+template <int LEVEL, int ROWS>
 struct EncodeSmem {
     static constexpr int W = Geo<LEVEL>::W;
-    static constexpr int kIn = kEncRing * kEncRows * kStreams * 2;
+    static constexpr int kIn = kEncRing * ROWS * kStreams * 2;
     static constexpr int kSlot = W * kStreams * 4;
     static constexpr int kTbl = 256 * 8;
     static constexpr int kSpill = (kSpillRows * kRow + 127) / 128 * 128;
@@ -136,12 +137,16 @@ __global__ void __launch_bounds__(256) k_encode_prologue(const uint16_t *__restr
     cluster_sync();  // CTA 0 has read the other CTAs' counts
 }
 
-template <int LEVEL>
-__global__ void __launch_bounds__(kEncThreads, 4) k_encode(const __grid_constant__ EncodeArgs a)
+// ROWS rows of every stream per input chunk.  A grid of at most two blocks per
+// SM has no third or fourth CTA on an SM to hide the per-chunk barrier, so it
+// takes chunks twice as long (half the barriers, twice the loads in flight per
+// thread, 2 CTAs per SM by registers).
+template <int LEVEL, int ROWS>
+__global__ void __launch_bounds__(kEncThreads, ROWS == kEncRows ? 4 : 2) k_encode(const __grid_constant__ EncodeArgs a)
 {
     using G = Geo<LEVEL>;
-    using L = EncodeSmem<LEVEL>;
-    constexpr int W = G::W, R = kEncRows, S = kEncRing, SP = kSpillRows;
+    using L = EncodeSmem<LEVEL, ROWS>;
+    constexpr int W = G::W, R = ROWS, S = kEncRing, SP = kSpillRows;
     constexpr int NW = kEncThreads / 32;
     extern __shared__ __align__(128) uint8_t smem[];
     uint16_t *x_s = reinterpret_cast<uint16_t *>(smem);
@@ -306,17 +311,23 @@ __global__ void __launch_bounds__(kEncThreads, 4) k_encode(const __grid_constant
     }
 }
 
-template <int LEVEL>
-cudaError_t launch_level(const EncodeArgs &a, cudaStream_t s)
+template <int LEVEL, int ROWS>
+cudaError_t launch_kernel(const EncodeArgs &a, cudaStream_t s)
 {
-    constexpr int smem = EncodeSmem<LEVEL>::kBytes;
-    cudaError_t err = cudaFuncSetAttribute(k_encode<LEVEL>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    constexpr int smem = EncodeSmem<LEVEL, ROWS>::kBytes;
+    cudaError_t err = cudaFuncSetAttribute(k_encode<LEVEL, ROWS>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (err != cudaSuccess) return err;
     EncodeArgs b = a;
     b.deferred = deferred_placement(a.t.nblocks);
-    err = launch_pdl(k_encode<LEVEL>, dim3(a.t.nblocks), dim3(kEncThreads), smem, s, b);
+    err = launch_pdl(k_encode<LEVEL, ROWS>, dim3(a.t.nblocks), dim3(kEncThreads), smem, s, b);
     if (err != cudaSuccess || !b.deferred) return err;
     return launch_block_offsets(a.t, s);
+}
+
+template <int LEVEL>
+cudaError_t launch_level(const EncodeArgs &a, cudaStream_t s)
+{
+    return small_grid(a.t.nblocks) ? launch_kernel<LEVEL, kEncRowsSmall>(a, s) : launch_kernel<LEVEL, kEncRows>(a, s);
 }
 
 }  // namespace dev

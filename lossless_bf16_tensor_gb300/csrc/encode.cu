@@ -11,8 +11,8 @@
 // ring of row chunks filled by TMA bulk copies; each row's values are split,
 // their sign-fraction bytes written straight out, and their exponents
 // appended to the streams' slot images in shared memory.  A chunk in which
-// every stream of a warp has room for 16 more bits per row takes a fast path
-// with no fit checks.  Spilled exponents are kept in a 32-row ring; a stream
+// every stream of a warp has room for all of its codes takes a fast path
+// with no per-value fit checks.  Spilled exponents are kept in a 32-row ring; a stream
 // that spills more than that has its older spilled exponents read back from
 // the input.
 #include "codec_dev.cuh"
@@ -21,10 +21,10 @@ namespace lct {
 namespace dev {
 
 constexpr int kEncThreads = 256;
-constexpr int kEncRows = 16;    // rows per input chunk (4 CTAs per SM)
+constexpr int kEncRows = 16;       // rows per input chunk (4 CTAs per SM)
 constexpr int kEncRowsSmall = 32;  // rows per input chunk on grids of at most two blocks per SM
-constexpr int kEncRing = 2;     // chunks in flight
-constexpr int kSpillRows = 32;  // spilled-exponent rows kept
+constexpr int kEncRing = 2;        // chunks in flight
+constexpr int kSpillRows = 32;     // spilled-exponent rows kept
 
 template <int LEVEL, int ROWS>
 struct EncodeSmem {

@@ -191,3 +191,35 @@ def test_sgd_162m_step_one_full_and_sampled_steps():
             nj[(nb - 1) * 256:] = [max(0, -(-(last - j) // 256)) for j in range(256)]
             spill = (nj - got["markers"].astype(np.int64)).reshape(nb, 256).sum(1)
             assert np.array_equal(got["blk_off"], np.concatenate([[0], np.cumsum(spill)]).astype(np.uint64))
+
+
+@pytest.mark.parametrize("eta", [0.0, -1e-3, 0.5, 3.0e4, 1e-40, float("inf"), float("-inf"), float("nan")])
+@pytest.mark.parametrize("large", [False, True])
+def test_sgd_eta_edge_cases(eta, large):
+    """eta zero, negative, large (the exponents move, so few groups keep their
+    old codes and many values escape and spill), subnormal in float32, and
+    infinite or NaN (every new value infinite or NaN, exponent 255, which no
+    codebook codes).  The step is W' = bf16(fl32(w - fl32(eta*m))) for any
+    float32 eta ([EXP] "Training adds a second problem"), with NaN written as
+    0x7FC0; the new W must equal the oracle's bit for bit, both on a small grid
+    (the software-pipelined kernel) and on a grid of more than two blocks per
+    SM (the throughput kernel, which canonicalises NaN everywhere only when
+    eta is not finite)."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    nblocks = 2 * sms + 3 if large else 3
+    n = nblocks * 65536 - 555
+    w = synth.normal(n, 0.02, 41)
+    m = synth.normal(n, 1e-3, 42)
+    w[:4] = [0x0000, 0x8000, 0x0001, 0x7F80]  # +0, -0, a subnormal, +inf
+    m[:4] = [0x3F80, 0x0000, 0xBF80, 0x3F80]
+    eta32 = float(np.float32(eta))
+    W, M, cbw, cbm, oW, oM, ocbw, ocbm = _setup(w, m, 0)
+    ref = oracle.sgd_step(oW, ocbw, oM, ocbm, eta32)
+    out = B.CompressedTensor(n, 0)
+    B.lct_sgd_step_fused(W, cbw, M, cbm, eta32, out)
+    torch.cuda.synchronize()
+    got = out.to_host()
+    assert got["status"] == ref.status == 0
+    assert_same_format(got, ref)
+    rc, yref = oracle.decode(ref, ocbw)
+    assert np.array_equal(gpu_decode(out, cbw), yref)

@@ -111,3 +111,33 @@ def test_adamw_ten_steps_in_place():
             assert gt["status"] == rf.status == 0
             assert_same_format(gt, rf)
         cur = nxt
+
+
+EDGES = [dict(lr=0.0), dict(lr=-1e-3), dict(beta1=0.0), dict(beta2=0.0), dict(beta1=0.9999999, beta2=0.9999999),
+         dict(eps=1e-30), dict(weight_decay=0.0), dict(weight_decay=1e3), dict(t=1), dict(t=10 ** 6)]
+
+
+@pytest.mark.parametrize("edge", EDGES, ids=lambda e: ",".join("%s=%g" % kv for kv in e.items()))
+@pytest.mark.parametrize("in_place", [False, True])
+def test_adamw_hyperparameter_edge_cases(edge, in_place):
+    """Hyperparameters at the edges of what the ABI accepts: a zero or
+    negative learning rate, beta1 or beta2 zero or just below one, a tiny eps,
+    no or a large weight decay, the first step and a step far enough that the
+    bias corrections round to one.  The step constants come from the same
+    hyperparameters on both sides; every region of the three new tensors must
+    equal the oracle's."""
+    hp = dict(HP, t=3)
+    hp.update(edge)
+    n = 3 * 65536 - 555
+    w, m, v, g = _inputs(n, 7)
+    gpu, ref, cbs, ocbs = _setup(w, m, v, 0)
+    k = oracle.adamw_constants(hp["lr"], hp["beta1"], hp["beta2"], hp["eps"], hp["weight_decay"], hp["t"])
+    exp = oracle.adamw_step(ref[0], ocbs[0], ref[1], ocbs[1], ref[2], ocbs[2], g, k)
+    outs = [B.CompressedTensor(n, 0, like=x) if in_place else B.CompressedTensor(n, 0) for x in gpu]
+    B.lct_adamw_step_fused(gpu[0], cbs[0], gpu[1], cbs[1], gpu[2], cbs[2], to_device(g), hp["lr"], hp["beta1"],
+                           hp["beta2"], hp["eps"], hp["weight_decay"], hp["t"], *outs)
+    torch.cuda.synchronize()
+    for o, rf in zip(outs, exp):
+        gt = o.to_host()
+        assert gt["status"] == rf.status == 0
+        assert_same_format(gt, rf)

@@ -170,3 +170,33 @@ def test_momentum_162m_step_one_full_and_sampled_steps():
     y = gpu_decode(cw, cbw)
     rc, yref = oracle.decode(ow, ocbw)
     assert rc == 0 and np.array_equal(y[(nb - 1) * block:], yref)
+
+
+@pytest.mark.parametrize("eta, mu", [(0.0, 0.9), (1e-3, 0.0), (1e-3, -0.5), (0.75, 1.5), (1e-3, 1e-40),
+                                     (float("inf"), 0.9), (1e-3, float("inf")), (1e-3, float("nan")),
+                                     (float("nan"), 0.9)])
+@pytest.mark.parametrize("large", [False, True])
+def test_momentum_hyperparameter_edge_cases(eta, mu, large):
+    """eta and mu zero, negative, above one, subnormal in float32, infinite
+    and NaN.  Both new states follow M' = bf16(fl32(fl32(mu*m) + g)) and
+    W' = bf16(fl32(w - fl32(eta*M'))) for any float32 eta and mu, NaN written
+    as 0x7FC0; both must equal the oracle's bit for bit on a small grid and on
+    a grid of more than two blocks per SM."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    nblocks = 2 * sms + 3 if large else 3
+    n = nblocks * 65536 - 555
+    w = synth.normal(n, 0.02, 43)
+    m = synth.normal(n, 1e-3, 44)
+    g = synth.normal(n, 1e-4, 45)
+    w[:4] = [0x0000, 0x8000, 0x0001, 0x7F80]  # +0, -0, a subnormal, +inf
+    m[:4] = [0x3F80, 0x0000, 0xBF80, 0x0000]
+    eta32, mu32 = float(np.float32(eta)), float(np.float32(mu))
+    W, M, cbw, cbm, oW, oM, ocbw, ocbm = _setup(w, m, 0)
+    rw, rm = oracle.sgd_momentum_step(oW, ocbw, oM, ocbm, g, eta32, mu32)
+    ow, om = B.CompressedTensor(n, 0), B.CompressedTensor(n, 0)
+    B.lct_sgd_momentum_step_fused(W, cbw, M, cbm, to_device(g), eta32, mu32, ow, om)
+    torch.cuda.synchronize()
+    gw, gm = ow.to_host(), om.to_host()
+    assert gw["status"] == rw.status == 0 and gm["status"] == rm.status == 0
+    assert_same_format(gw, rw)
+    assert_same_format(gm, rm)

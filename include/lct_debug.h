@@ -17,13 +17,15 @@
 extern "C" {
 #endif
 
-/* Enqueue one tiny kernel that clears two scan words at d_work (device, at
- * least 16 bytes, 16-byte aligned) and then waits, as block 1, for block 0 to
- * publish -- which nothing does.  After limit_ns nanoseconds (1 .. 10^9) of
- * %globaltimer the wait gives up and LCT_ERR_TIMEOUT is latched into the
- * status word of the header at d_header (device, LCT_HEADER_BYTES, 16-byte
- * aligned; the latch only fires if the status is 0).  The kernel returns
- * normally; the CUDA context stays usable.
+/* Enqueue one tiny kernel (one warp) that clears two scan words at d_work
+ * (device, at least 16 bytes, 16-byte aligned) and then waits, as block 1,
+ * for block 0 to publish -- which nothing does -- in each form of the wait the
+ * writers use (a warp reading every predecessor, a warp walking back window
+ * by window, a single thread), one after the other.  Each gives up after
+ * limit_ns nanoseconds (1 .. 10^9) of %globaltimer; when all of them have,
+ * LCT_ERR_TIMEOUT is latched into the status word of the header at d_header
+ * (device, LCT_HEADER_BYTES, 16-byte aligned; the latch only fires if the
+ * status is 0).  The kernel returns normally; the CUDA context stays usable.
  * Errors: LCT_ERR_INVALID_ARG for NULL/misaligned pointers or a limit out of
  * range, LCT_ERR_CUDA for a launch failure. */
 lct_status lct_debug_wait_timeout(void *d_header, void *d_work, uint64_t limit_ns, void *stream);

@@ -419,16 +419,24 @@ namespace lct {
 namespace dev {
 
 // Runs the look-back of block 1 over a status array whose block 0 never
-// publishes; the bounded wait must run out and latch LCT_ERR_TIMEOUT.
+// publishes, in each of its forms (the warp reading every predecessor, the
+// warp walking back window by window, the single thread); every bounded wait
+// must run out, and only then is LCT_ERR_TIMEOUT latched.  One warp.
 __global__ void k_wait_probe(lct_header *hdr, unsigned long long *work, uint64_t wait_ns)
 {
-    if (threadIdx.x != 0) return;
-    work[0] = 0ull;
-    work[1] = 0ull;
-    __threadfence();
-    bool timed_out;
-    lookback(work, 1, 0, wait_ns, &timed_out);
-    if (timed_out) latch(hdr, LCT_ERR_TIMEOUT);
+    if (threadIdx.x == 0) {
+        work[0] = 0ull;
+        work[1] = 0ull;
+        __threadfence();
+    }
+    __syncwarp();
+    bool t_all = false, t_walk = false, t_one = false;
+    warp_lookback_all(work, 1, 0, wait_ns, &t_all);
+    warp_lookback_walk(work, 1, 0, wait_ns, &t_walk);
+    if (threadIdx.x == 0) {
+        lookback(work, 1, 0, wait_ns, &t_one);
+        if (t_all && t_walk && t_one) latch(hdr, LCT_ERR_TIMEOUT);
+    }
 }
 
 }  // namespace dev

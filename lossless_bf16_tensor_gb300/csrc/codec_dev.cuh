@@ -579,6 +579,65 @@ __device__ __forceinline__ void st_status(unsigned long long *p, unsigned long l
     asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
 }
 
+// Blocks below kAllPrev take every predecessor's own count at once: at most
+// kAllPrev / 32 loads per lane, all in flight together.
+constexpr uint32_t kAllPrev = 320;
+
+// A warp whose streams each spilled at most this many symbols writes its
+// overflow bytes lane by lane (each lane its own stream's run); otherwise one
+// stream at a time with the lanes over its symbols (coalesced for long runs).
+constexpr uint32_t kFewSpills = 8;
+
+// One full warp of block b < kAllPrev: publish the block's overflow byte
+// count, wait until every predecessor has published (each status word carries
+// its block's own count, whatever its flag), add all their counts in one
+// round, and publish the inclusive prefix.  When the blocks finish at nearly
+// the same time (a grid that fits the GPU at once) this takes one round of
+// loads after the last predecessor publishes, where walking back to the
+// nearest inclusive prefix takes one round per window of 32 blocks that has
+// none yet.  Every wait is bounded as in warp_lookback_walk.
+__device__ __forceinline__ unsigned long long warp_lookback_all(unsigned long long *status, uint32_t b,
+                                                                unsigned long long total, uint64_t wait_ns,
+                                                                bool *timed_out)
+{
+    const int lane = threadIdx.x & 31;
+    *timed_out = false;
+    if (b == 0) {
+        if (lane == 0) st_status(&status[0], status_word(kFlagInc, total, total));
+        return 0;
+    }
+    if (lane == 0) st_status(&status[b], status_word(kFlagAgg, total, total));
+    const uint64_t t0 = global_ns();
+    uint32_t spins = 0;
+    unsigned long long sum;
+    for (;;) {
+        unsigned long long v[kAllPrev / 32];
+#pragma unroll
+        for (int k = 0; k < (int)(kAllPrev / 32); ++k) {
+            const uint32_t idx = (uint32_t)lane + 32u * k;
+            v[k] = idx < b ? ld_status(&status[idx]) : kFlagInc;  // beyond b: ready, own count 0
+        }
+        bool ready = true;
+        sum = 0;
+#pragma unroll
+        for (int k = 0; k < (int)(kAllPrev / 32); ++k) {
+            ready = ready && (v[k] >> 62) != 0;
+            sum += (v[k] >> kOwnShift) & kOwnMask;
+        }
+        if (__all_sync(kFull, ready)) break;
+        ++spins;
+        if (spins > (1u << 24) || ((spins & 63u) == 0 && global_ns() - t0 > wait_ns)) {
+            *timed_out = true;
+            break;
+        }
+        __nanosleep(32);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(kFull, sum, o);
+    if (lane == 0) st_status(&status[b], status_word(kFlagInc, total, sum + total));
+    return sum;
+}
+
 // One full warp of block b: publish the block's overflow byte count, then
 // read the status words of the 32 nearest predecessors at once, add their
 // counts up to the nearest published inclusive prefix, and move 32 further
@@ -586,9 +645,9 @@ __device__ __forceinline__ void st_status(unsigned long long *p, unsigned long l
 // exclusive one (same value in every lane).  Every wait is bounded by wait_ns
 // of %globaltimer and an iteration cap; on expiry *timed_out is set and the
 // prefix found so far is used, so later blocks are never stuck.
-static __device__ __noinline__ unsigned long long warp_lookback(unsigned long long *status, uint32_t b,
-                                                                unsigned long long total, uint64_t wait_ns,
-                                                                bool *timed_out)
+static __device__ __noinline__ unsigned long long warp_lookback_walk(unsigned long long *status, uint32_t b,
+                                                                     unsigned long long total, uint64_t wait_ns,
+                                                                     bool *timed_out)
 {
     const int lane = threadIdx.x & 31;
     *timed_out = false;
@@ -626,6 +685,16 @@ static __device__ __noinline__ unsigned long long warp_lookback(unsigned long lo
     }
     if (lane == 0) st_status(&status[b], status_word(kFlagInc, total, excl + total));
     return excl;
+}
+
+// The exclusive overflow prefix of block b (see warp_lookback_all and
+// warp_lookback_walk); the inclusive one is published for later blocks.
+__device__ __forceinline__ unsigned long long warp_lookback(unsigned long long *status, uint32_t b,
+                                                           unsigned long long total, uint64_t wait_ns,
+                                                           bool *timed_out)
+{
+    if (b < kAllPrev) return warp_lookback_all(status, b, total, wait_ns, timed_out);
+    return warp_lookback_walk(status, b, total, wait_ns, timed_out);
 }
 
 // For a block with no overflow bytes when the offsets are computed

@@ -279,10 +279,18 @@ __global__ void __launch_bounds__(kEncThreads, ROWS == kEncRows ? 4 : 2) k_encod
     if (!leave) __syncthreads();  // uniform: total is the block's
     const unsigned long long excl = leave ? 0ull : s_excl;
 
-    // spilled exponents, raw, in (stream, symbol) order: one warp per stream
-    // at a time, lanes over the stream's spilled symbols (beyond the
-    // capacity nothing is written; the capacity error is latched)
-    if (total > 0 && excl + total <= a.t.ovf_cap) {
+    // spilled exponents, raw, in (stream, symbol) order: a few per stream
+    // lane by lane, otherwise one warp per stream at a time with the lanes
+    // over the stream's spilled symbols (beyond the capacity nothing is
+    // written; the capacity error is latched)
+    if (total > 0 && excl + total <= a.t.ovf_cap && __reduce_max_sync(kFull, spill) <= kFewSpills) {
+        uint8_t *out = a.t.ovf + excl + pre;
+        const uint32_t kept_from = nj > (uint32_t)SP ? nj - SP : 0u;  // older spills were overwritten
+        for (uint32_t l = 0; l < spill; ++l) {
+            const uint32_t k = marker + l;
+            out[l] = k >= kept_from ? ringj[(k & (SP - 1)) * kRow] : exp_of(a.x[base + (uint64_t)k * kStreams + j]);
+        }
+    } else if (total > 0 && excl + total <= a.t.ovf_cap) {
         uint8_t *out = a.t.ovf + excl;
         for (int i = 0; i < 32; ++i) {
             const uint32_t sm = __shfl_sync(kFull, marker, i);

@@ -552,8 +552,18 @@ __global__ void __launch_bounds__(kMomBlock, INPLACE ? 1 : 2) k_momentum(const _
     const bool room_m = tot_m > 0 && excl_m + tot_m <= a.m_out.ovf_cap;
     uint8_t *out_w = a.w_out.ovf + excl_w;
     uint8_t *out_m = a.m_out.ovf + excl_m;
-    // spilled rows still kept in shared memory: one warp per stream at a time
-    for (int i = 0; i < 32; ++i) {
+    // spilled rows still kept in shared memory: a few per stream lane by lane,
+    // otherwise one warp per stream at a time
+    static_assert(kFewSpills <= (uint32_t)SP, "a few spilled rows are all still staged");
+    const bool few = __reduce_max_sync(kFull, max(room_w ? sp_w : 0u, room_m ? sp_m : 0u)) <= kFewSpills;
+    if (few) {
+        const uint32_t sj = (uint32_t)j;
+        if (room_w)
+            for (uint32_t l = 0; l < sp_w; ++l) out_w[pre_w + l] = stageW[((mk_w + l) % SP) * kRow + sj];
+        if (room_m)
+            for (uint32_t l = 0; l < sp_m; ++l) out_m[pre_m + l] = stageM[((mk_m + l) % SP) * kRow + sj];
+    }
+    for (int i = 0; i < (few ? 0 : 32); ++i) {
         const uint32_t sj = (uint32_t)(warp * 32 + i);
         if (room_w) {
             const uint32_t smk = __shfl_sync(kFull, mk_w, i), ssp = __shfl_sync(kFull, sp_w, i);

@@ -587,14 +587,20 @@ __global__ void __launch_bounds__(kSgdBlock, SgdSmem<LEVEL, INPLACE, UpdateOp<OP
     const unsigned long long excl = leave ? 0ull : s_excl;
     if (total > 0 && excl + total <= a.w_out.ovf_cap) {
         uint8_t *out = a.w_out.ovf + excl;
-        // spilled rows still kept in shared memory: one warp per stream at a time
-        for (int i = 0; i < 32; ++i) {
-            const uint32_t ssp = __shfl_sync(kFull, spill, i);
-            const uint32_t spr = __shfl_sync(kFull, pre, i);
-            const uint32_t sj = (uint32_t)(warp * 32 + i);
-            const uint32_t kept_from = L::kKeepAll || ssp <= (uint32_t)SP ? 0u : ssp - SP;  // older ones were overwritten
-            for (uint32_t l = lane; l < ssp; l += 32)
-                if (L::kKeepAll || l >= kept_from) out[spr + l] = ring[stage_row<L::kKeepAll, SP>(l) * kRow + sj];
+        static_assert(L::kKeepAll || kFewSpills <= (uint32_t)SP, "a few spilled rows are all still staged");
+        if (__reduce_max_sync(kFull, spill) <= kFewSpills) {
+            // a few spilled rows per stream, all still staged: lane by lane
+            for (uint32_t l = 0; l < spill; ++l) out[pre + l] = ringj[stage_row<L::kKeepAll, SP>(l) * kRow];
+        } else {
+            // spilled rows still kept in shared memory: one warp per stream at a time
+            for (int i = 0; i < 32; ++i) {
+                const uint32_t ssp = __shfl_sync(kFull, spill, i);
+                const uint32_t spr = __shfl_sync(kFull, pre, i);
+                const uint32_t sj = (uint32_t)(warp * 32 + i);
+                const uint32_t kept_from = L::kKeepAll || ssp <= (uint32_t)SP ? 0u : ssp - SP;  // older ones were overwritten
+                for (uint32_t l = lane; l < ssp; l += 32)
+                    if (L::kKeepAll || l >= kept_from) out[spr + l] = ring[stage_row<L::kKeepAll, SP>(l) * kRow + sj];
+            }
         }
         const uint32_t kept_from = nj > (uint32_t)SP ? nj - SP : 0u;
         if (!L::kKeepAll && marker < kept_from) {

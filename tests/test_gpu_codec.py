@@ -193,7 +193,9 @@ def test_bad_magic_and_wrong_codebook():
 
 def test_bounded_wait_runs_out():
     """A block waiting for a predecessor that never publishes gives up after
-    the limit and latches LCT_ERR_TIMEOUT; the context stays usable."""
+    the limit in every form of the wait (all predecessors at once, window by
+    window, single thread) and latches LCT_ERR_TIMEOUT; the context stays
+    usable."""
     hdr = torch.zeros(64, dtype=torch.uint8, device="cuda")
     work = torch.zeros(64, dtype=torch.uint8, device="cuda")
     B.lct_debug_wait_timeout(hdr, work, 2_000_000)

@@ -117,6 +117,22 @@ __device__ __forceinline__ void rd_pair16_w3(uint32_t &p, uint32_t &w0, uint32_t
     p = q;
 }
 
+// A stream's spilled exponents are bytes [p, p + count) of the overflow
+// region, taken one per row at the end of the stream: each load's address is
+// known from the block's start, but its result is needed before the next row.
+// Asking for their lines in L1 at the block's start takes the DRAM latency off
+// every one of those rows.  The first two 128-byte lines hold all of a
+// stream's spilled bytes in MEDIUM and HIGH (at most 96 and 88) and all but
+// the longest CLEAN spills.
+__device__ __forceinline__ void prefetch_spill(const uint8_t *p, uint32_t count)
+{
+    if (count == 0) return;
+    asm volatile("prefetch.global.L1 [%0];" ::"l"(p));
+    const uint8_t *last = p + count - 1;
+    if (((reinterpret_cast<uintptr_t>(p) ^ reinterpret_cast<uintptr_t>(last)) >> 7) != 0)
+        asm volatile("prefetch.global.L1 [%0];" ::"l"(p + 128 <= last ? p + 128 : last));
+}
+
 template <int LEVEL, bool WIN3>
 __global__ void __launch_bounds__(kDecThreads, WIN3 ? 2 : 4) k_decode(const __grid_constant__ DecodeArgs a)
 {
@@ -182,6 +198,7 @@ __global__ void __launch_bounds__(kDecThreads, WIN3 ? 2 : 4) k_decode(const __gr
     const uint32_t pre = group_exclusive_scan(nj - marker, warp_tot, kDecThreads / 32, 0, &total);
     const bool ovf_ok = off1 <= a.t.ovf_cap && off0 <= off1 && off1 - off0 == total;
     const uint64_t ovf_at = off0 + pre - marker;  // overflow index of spilled symbol k is ovf_at + k
+    if (ovf_ok) prefetch_spill(a.t.ovf + off0 + pre, nj - marker);
 
     if (!mbar_wait(&bar_slot, 0, limit)) s_timeout = 1;
     const uint32_t *col = slot_s + j;
